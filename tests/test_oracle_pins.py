@@ -1,0 +1,329 @@
+"""Pins for the CPU oracle: closed forms, invariants, exact integer cases,
+library cross-checks and hand-worked rounding cases.
+
+The oracle is the GEMM definition C = alpha*op(A)*op(B) + beta*C of
+"Optimising fp32 GEMM on A100" (section "What is GEMM?").  Each pin below
+fixes its output by something other than the oracle itself, so that a dropped
+term, a flipped sign, a wrong index or a transposed operand fails at least one
+of them.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import gemm_inputs as gi
+
+LAYOUTS = [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")]
+U = 2.0 ** -24
+
+
+def stored(op_mat, trans, ld_pad=0, fill=np.nan):
+    """Stored fp32 array (with ld padding) whose op() is op_mat."""
+    base = op_mat if trans == "N" else op_mat.T
+    rows, cols = base.shape
+    ld = max(cols + ld_pad, 1)
+    out = np.full((rows, ld), fill, dtype=np.float32)
+    out[:, :cols] = base
+    return out, ld
+
+
+def run_f64(orc, ta, tb, opA, opB, alpha, beta, C=None, pad=(0, 0, 0)):
+    M, K = opA.shape
+    N = opB.shape[1]
+    A, lda = stored(opA, ta, pad[0])
+    B, ldb = stored(opB, tb, pad[1])
+    ldc = max(N + pad[2], 1)
+    Cs = None
+    if C is not None:
+        Cs = np.full((M, ldc), np.nan, dtype=np.float32)
+        Cs[:, :N] = C
+    return orc.gemm_f64(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, Cs, ldc)
+
+
+def run_f32(orc, ta, tb, opA, opB, alpha, beta, C=None):
+    M, K = opA.shape
+    N = opB.shape[1]
+    A, lda = stored(opA, ta)
+    B, ldb = stored(opB, tb)
+    return orc.gemm_f32_seq(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta,
+                            C, max(N, 1))
+
+
+# ---------------------------------------------------------------- P1 ones
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (5, 7, 3), (33, 17, 3001)])
+def test_all_ones(oracle_mod, ta, tb, M, N, K):
+    opA = np.ones((M, K), np.float32)
+    opB = np.ones((K, N), np.float32)
+    ref, bound = run_f64(oracle_mod, ta, tb, opA, opB, 1.0, 0.0)
+    assert np.all(ref == K)
+    assert np.allclose(bound, 4 * K * U * K, rtol=0, atol=0)
+    # with beta: alpha*K + beta*c, every term exact in double
+    C = np.full((M, N), 3.0, np.float32)
+    ref, bound = run_f64(oracle_mod, ta, tb, opA, opB, 2.0, -0.5, C)
+    assert np.all(ref == 2.0 * K - 1.5)
+    assert np.all(bound == 4 * K * U * (2.0 * K + 0.5 * 3.0))
+    # fp32 sequential order: K < 2^24 so every partial sum is exact
+    out = run_f32(oracle_mod, ta, tb, opA, opB, 1.0, 0.0)
+    assert np.all(out == np.float32(K))
+
+
+# ---------------------------------------------------------------- P2 identity
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_identity_left_and_right(oracle_mod, ta, tb):
+    M, N = 19, 23
+    X = gi.random_matrix(11, M, N)          # any values
+    # op(A) = I_M  =>  C = op(B)
+    ref, _ = run_f64(oracle_mod, ta, tb, np.eye(M, dtype=np.float32), X, 1.0, 0.0)
+    assert np.array_equal(ref, X.astype(np.float64))
+    # op(B) = I_N  =>  C = op(A)
+    ref, _ = run_f64(oracle_mod, ta, tb, X, np.eye(N, dtype=np.float32), 1.0, 0.0)
+    assert np.array_equal(ref, X.astype(np.float64))
+    # alpha, beta with identity: 1.5*x + 0.25*c is one double rounding of
+    # two exact products, i.e. the correctly rounded value of the real result
+    C = gi.random_matrix(12, M, N)
+    ref, _ = run_f64(oracle_mod, ta, tb, np.eye(M, dtype=np.float32), X, 1.5, 0.25, C)
+    exact = 1.5 * X.astype(np.float64) + 0.25 * C.astype(np.float64)
+    assert np.array_equal(ref, exact)
+
+
+# ---------------------------------------------------------------- P3 permutation
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_permutation(oracle_mod, ta, tb):
+    rng = np.random.default_rng(3)
+    M, K, N = 13, 13, 29
+    perm = rng.permutation(K)
+    P = np.zeros((M, K), np.float32)
+    P[np.arange(M), perm] = 1.0              # row i of P picks k = perm[i]
+    X = gi.random_matrix(21, K, N)
+    ref, _ = run_f64(oracle_mod, ta, tb, P, X, 1.0, 0.0)
+    assert np.array_equal(ref, X[perm].astype(np.float64))
+    # right permutation: column j of Q picks row sigma[j] of op(B)=Q
+    N2 = 17
+    sigma = rng.permutation(N2)
+    Q = np.zeros((N2, N2), np.float32)
+    Q[sigma, np.arange(N2)] = 1.0
+    Y = gi.random_matrix(22, 9, N2)
+    ref, _ = run_f64(oracle_mod, ta, tb, Y, Q, 1.0, 0.0)
+    assert np.array_equal(ref, Y[:, sigma].astype(np.float64))
+
+
+# ---------------------------------------------------------------- P4 rank one
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_rank_one_closed_forms(oracle_mod, ta, tb):
+    M, N, K = 11, 14, 37
+    u = (np.arange(M) - 5).astype(np.float32)            # small integers
+    v = (2.0 ** -np.arange(N)).astype(np.float32)         # powers of two
+    opA = np.repeat(u[:, None], K, axis=1)                # A_ik = u_i
+    opB = np.repeat(v[None, :], K, axis=0)                # B_kj = v_j
+    ref, _ = run_f64(oracle_mod, ta, tb, opA, opB, 1.0, 0.0)
+    assert np.array_equal(ref, K * np.outer(u, v).astype(np.float64))
+    # A = u e0^T, B = e0 v^T  =>  C = u v^T
+    a = np.zeros((M, K), np.float32); a[:, 0] = u
+    b = np.zeros((K, N), np.float32); b[0, :] = v
+    ref, _ = run_f64(oracle_mod, ta, tb, a, b, -1.0, 0.0)
+    assert np.array_equal(ref, -np.outer(u, v).astype(np.float64))
+
+
+# ---------------------------------------------------------------- P5 integers
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-1.0, 1.0), (2.0, -1.0), (0.5, 2.0)])
+def test_small_integers_exact(oracle_mod, ta, tb, alpha, beta):
+    M, N, K = 31, 45, 129
+    Ai = gi.small_ints(1, (M, K))
+    Bi = gi.small_ints(2, (K, N))
+    Ci = gi.small_ints(3, (M, N))
+    exact = Ai.astype(np.int64) @ Bi.astype(np.int64)      # library integer matmul
+    want = alpha * exact.astype(np.float64) + (beta * Ci.astype(np.float64) if beta else 0.0)
+    ref, _ = run_f64(oracle_mod, ta, tb, Ai, Bi, alpha, beta, Ci if beta else None)
+    assert np.array_equal(ref, want)
+    # fp32 sequential: all partial sums are integers < 2^24, exact too
+    out = run_f32(oracle_mod, ta, tb, Ai, Bi, alpha, beta, Ci if beta else None)
+    assert np.array_equal(out.astype(np.float64), want)
+
+
+# ---------------------------------------------------------------- P6 library
+SHAPES = [1, 2, 3, 7, 8, 9, 16, 17, 33]
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_brute_force_vs_numpy(oracle_mod, ta, tb):
+    rng = np.random.default_rng(7)
+    combos = list(itertools.product(SHAPES, SHAPES, SHAPES))
+    idx = rng.choice(len(combos), size=40, replace=False)
+    for t, i in enumerate(idx):
+        M, N, K = combos[i]
+        opA = gi.random_matrix(100 + t, M, K)
+        opB = gi.random_matrix(200 + t, K, N)
+        C = gi.random_matrix(300 + t, M, N)
+        alpha, beta = [(1.0, 0.0), (-1.0, 0.5), (1.5, 1.0), (0.0, 0.5)][t % 4]
+        ref, bound = run_f64(oracle_mod, ta, tb, opA, opB, alpha, beta, C,
+                             pad=(t % 3, (t + 1) % 3, t % 2))
+        A64, B64, C64 = (x.astype(np.float64) for x in (opA, opB, C))
+        lib = alpha * np.matmul(A64, B64) + (beta * C64 if beta else 0.0)
+        mag = abs(alpha) * np.matmul(np.abs(A64), np.abs(B64)) + abs(beta) * np.abs(C64)
+        assert np.all(np.abs(ref - lib) <= 1e-13 * mag + 1e-300)
+        assert np.allclose(bound, 4 * K * U * mag, rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_f32_sequential_within_bound(oracle_mod, ta, tb):
+    """The fp32 evaluation obeys the fp32 error bound of the definition."""
+    for t, (M, N, K) in enumerate([(5, 6, 7), (17, 9, 300), (3, 40, 1025)]):
+        opA = gi.random_matrix(400 + t, M, K, dist="normal")
+        opB = gi.random_matrix(500 + t, K, N, dist="normal")
+        C = gi.random_matrix(600 + t, M, N)
+        out = run_f32(oracle_mod, ta, tb, opA, opB, 1.25, -0.75, C)
+        ref, bound = run_f64(oracle_mod, ta, tb, opA, opB, 1.25, -0.75, C)
+        rep = oracle_mod.compare(out, ref, bound, K, 1.25)
+        assert rep["pass"], rep
+        assert rep["max_err_over_bound"] < 0.25
+
+
+# ---------------------------------------------------------------- P7 special
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_special_cases(oracle_mod, ta, tb):
+    M, N, K = 6, 5, 4
+    C = gi.random_matrix(31, M, N)
+    # alpha == 0: C = beta*C and A, B are never read (null pointers accepted)
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, 0.0, None, max(K if ta == "N" else M, 1),
+                                     None, max(N if tb == "N" else K, 1), 0.5, C, N)
+    assert np.array_equal(ref, 0.5 * C.astype(np.float64))
+    out = oracle_mod.gemm_f32_seq(ta, tb, M, N, K, 0.0, None, max(K if ta == "N" else M, 1),
+                                  None, max(N if tb == "N" else K, 1), 0.5, C, N)
+    assert np.array_equal(out, np.float32(0.5) * C)
+    # K == 0: no product term, bound 0
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, 0, 1.0, None, max(1 if ta == "N" else M, 1),
+                                     None, max(N if tb == "N" else 1, 1), -2.0, C, N)
+    assert np.array_equal(ref, -2.0 * C.astype(np.float64)) and np.all(bound == 0)
+    # beta == 0 with NaN in C: C is not read
+    Cnan = np.full((M, N), np.nan, np.float32)
+    opA = gi.random_matrix(32, M, K)
+    opB = gi.random_matrix(33, K, N)
+    ref, _ = run_f64(oracle_mod, ta, tb, opA, opB, 1.0, 0.0, Cnan)
+    assert np.all(np.isfinite(ref))
+    # alpha == 0 and beta == 0: zero, even over NaN C
+    ref, _ = run_f64(oracle_mod, ta, tb, opA, opB, 0.0, 0.0, Cnan)
+    assert np.all(ref == 0)
+    # empty outputs
+    r0, b0 = oracle_mod.gemm_f64(ta, tb, 0, N, K, 1.0, None, max(K if ta == "N" else 1, 1),
+                                 opB, max(N if tb == "N" else K, 1), 0.0, None, N)
+    assert r0.shape == (0, N)
+
+
+def test_argument_errors(oracle_mod):
+    A = np.zeros(64, np.float32)
+    with pytest.raises(oracle_mod.OracleArgError, match="argument 1"):
+        oracle_mod.gemm_f64("X", "N", 2, 2, 2, 1.0, A, 2, A, 2, 0.0, None, 2)
+    with pytest.raises(oracle_mod.OracleArgError, match="argument 2"):
+        oracle_mod.gemm_f64("N", "Q", 2, 2, 2, 1.0, A, 2, A, 2, 0.0, None, 2)
+    with pytest.raises(oracle_mod.OracleArgError, match="argument 3"):
+        oracle_mod.gemm_f64("N", "N", -1, 2, 2, 1.0, A, 2, A, 2, 0.0, None, 2)
+    with pytest.raises(oracle_mod.OracleArgError, match="argument 8"):
+        oracle_mod.gemm_f64("N", "N", 2, 2, 3, 1.0, A, 2, A, 2, 0.0, None, 2)
+    with pytest.raises(oracle_mod.OracleArgError, match="argument 10"):
+        oracle_mod.gemm_f64("N", "T", 2, 2, 3, 1.0, A, 3, A, 2, 0.0, None, 2)
+    with pytest.raises(oracle_mod.OracleArgError, match="argument 13"):
+        oracle_mod.gemm_f64("N", "N", 2, 5, 3, 1.0, A, 3, A, 5, 0.0, None, 4)
+
+
+# ---------------------------------------------------------------- P8 order
+def test_f32_sequential_order_hand_worked(oracle_mod):
+    """Hand-worked fp32 cases that fix the summation order and the FMA.
+
+    Row [1, 2^24, -2^24] times a column of ones, k ascending:
+      fma(1,1,0) = 1;  fma(2^24,1,1) = 2^24+1 -> tie, rounds to even 2^24;
+      fma(-2^24,1,2^24) = 0.   Exact (fp64) answer: 1.  Descending order: 1.
+    So the ascending fp32 loop must give exactly 0.
+    """
+    a = np.array([[1.0, 2.0 ** 24, -(2.0 ** 24)]], np.float32)
+    b = np.ones((3, 1), np.float32)
+    out = run_f32(oracle_mod, "N", "N", a, b, 1.0, 0.0)
+    assert out[0, 0] == 0.0
+    ref, _ = run_f64(oracle_mod, "N", "N", a, b, 1.0, 0.0)
+    assert ref[0, 0] == 1.0
+    # reversed k order gives the exact value 1: the order is what decides
+    out_rev = run_f32(oracle_mod, "N", "N", a[:, ::-1].copy(), b, 1.0, 0.0)
+    assert out_rev[0, 0] == 1.0
+
+    # Fused multiply-add, not multiply then add:
+    # x = 1 + 2^-12, x*x = 1 + 2^-11 + 2^-24.  fma(x, x, -1) keeps the
+    # 2^-24 (result 2^-11 + 2^-24, exact in fp32); a rounded multiply would
+    # tie-round x*x to 1 + 2^-11 and give 2^-11.
+    x = np.float32(1.0 + 2.0 ** -12)
+    a = np.array([[-1.0, x]], np.float32)
+    b = np.array([[1.0], [x]], np.float32)
+    out = run_f32(oracle_mod, "N", "N", a, b, 1.0, 0.0)
+    assert out[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+
+    # epilogue fmaf(alpha, acc, beta*c): alpha = x, acc = x, beta*c = -1
+    a = np.array([[x]], np.float32)
+    b = np.array([[1.0]], np.float32)
+    c = np.array([[-1.0]], np.float32)
+    out = run_f32(oracle_mod, "N", "N", a, b, float(x), 1.0, c)
+    assert out[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+    # beta == 0: plain rounded product alpha*acc = fl(x*x) = 1 + 2^-11
+    out = run_f32(oracle_mod, "N", "N", a, b, float(x), 0.0, None)
+    assert out[0, 0] == np.float32(1.0 + 2.0 ** -11)
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_transpose_symmetry(oracle_mod, ta, tb):
+    """(op(A) op(B))^T = op(B)^T op(A)^T via the swapped, flag-flipped call."""
+    M, N, K = 12, 9, 21
+    opA = gi.random_matrix(41, M, K)
+    opB = gi.random_matrix(42, K, N)
+    A, lda = stored(opA, ta)
+    B, ldb = stored(opB, tb)
+    ref, _ = oracle_mod.gemm_f64(ta, tb, M, N, K, 1.0, A, lda, B, ldb, 0.0, None, N)
+    flip = {"N": "T", "T": "N"}
+    refT, _ = oracle_mod.gemm_f64(flip[tb], flip[ta], N, M, K, 1.0, B, ldb, A, lda,
+                                  0.0, None, M)
+    assert np.array_equal(ref, refT.T)
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_leading_dimension_gaps(oracle_mod, ta, tb):
+    """NaN in every gap element changes nothing (gaps are never read)."""
+    M, N, K = 10, 7, 13
+    opA = gi.random_matrix(51, M, K)
+    opB = gi.random_matrix(52, K, N)
+    C = gi.random_matrix(53, M, N)
+    r0, b0 = run_f64(oracle_mod, ta, tb, opA, opB, 1.0, 1.0, C)
+    r1, b1 = run_f64(oracle_mod, ta, tb, opA, opB, 1.0, 1.0, C, pad=(3, 5, 2))
+    assert np.array_equal(r0, r1) and np.array_equal(b0, b1)
+
+
+def test_sampled_points_match_full(oracle_mod):
+    M, N, K = 40, 33, 50
+    opA = gi.random_matrix(61, M, K)
+    opB = gi.random_matrix(62, K, N)
+    C = gi.random_matrix(63, M, N)
+    full, fb = oracle_mod.gemm_f64("N", "T", M, N, K, 1.0, opA, K, opB.T.copy(), K, 0.5, C, N)
+    rows, cols = gi.sample_points(M, N, 200, seed=9)
+    s, sb = oracle_mod.gemm_f64("N", "T", M, N, K, 1.0, opA, K, opB.T.copy(), K, 0.5, C, N,
+                                points=(rows, cols))
+    assert np.array_equal(s, full[rows, cols]) and np.array_equal(sb, fb[rows, cols])
+    f32 = oracle_mod.gemm_f32_seq("N", "T", M, N, K, 1.0, opA, K, opB.T.copy(), K, 0.5, C, N)
+    f32s = oracle_mod.gemm_f32_seq("N", "T", M, N, K, 1.0, opA, K, opB.T.copy(), K, 0.5, C, N,
+                                   points=(rows, cols))
+    assert np.array_equal(f32s, f32[rows, cols])
+
+
+def test_compare_detects_errors(oracle_mod):
+    """The comparison flags an off-by-one-ulp-of-bound error and NaN."""
+    M, N, K = 8, 8, 16
+    opA = gi.random_matrix(71, M, K)
+    opB = gi.random_matrix(72, K, N)
+    ref, bound = run_f64(oracle_mod, "N", "N", opA, opB, 1.0, 0.0)
+    good = ref.astype(np.float32)
+    assert oracle_mod.compare(good, ref, bound, K, 1.0)["pass"]
+    bad = good.copy()
+    bad[3, 4] = np.float32(ref[3, 4] + 2 * bound[3, 4])
+    rep = oracle_mod.compare(bad, ref, bound, K, 1.0)
+    assert not rep["pass"] and rep["n_bad"] == 1
+    bad = good.copy()
+    bad[0, 0] = np.nan
+    assert not oracle_mod.compare(bad, ref, bound, K, 1.0)["pass"]
