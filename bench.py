@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark: SGEMM TFLOP/s at 4096^3 fp32 and % of the GB300 FP32 FFMA peak.
+
+One step = one sgemm() call (the library's public entry point, path chosen by
+its selector) on the 4096 x 4096 x 4096 row-major NN problem, alpha = 1,
+beta = 0, A and B uniform[-1, 1] from seed 3, inputs resident in HBM.  L2 is
+flushed between steps by writing a 256 MB buffer; the flush is outside the
+CUDA events that time each step.
+
+Prints ONE JSON line (rank 0).  Keys beyond the base contract:
+  roofline      dominant kernel: achieved / peak (FFMA: "alu" bound, peak =
+                SMs x 128 lanes x 2 flop x max SM clock; also at the median
+                clock sampled during the run), DRAM traffic from the
+                committed ncu summary when it matches the current kernel.
+  cpu_baseline  the CPU oracle (fp64 triple loop) timed on a bounded sample
+                of the same workload on the host cores.
+  e2e           the same metric with host buffers: pinned H2D of A and B,
+                the GEMM, D2H of C, all inside the timed region.
+  paths         every GPU path timed on the same workload (TFLOP/s, fraction
+                of its roofline, error vs the oracle on sample points).
+  clocks        nvidia-smi SM clock samples during the timed region.
+
+--impl reference times the CPU oracle itself (the reference arm).
+Under torchrun (N > 1) every rank runs an independent replica (the
+problem is not sharded); value = all ranks' flops / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gemm_inputs as gi  # noqa: E402
+
+METRIC = "SGEMM TFLOP/s at 4096^3 fp32 and % of GB300 FP32 FFMA peak (1 GPU)"
+UNIT = "TFLOP/s"
+WORKLOAD = gi.HEADLINE
+FLUSH_BYTES = 256 << 20
+FP32_LANES_PER_SM = 128
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_gemm_05_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel_key: str, units_per_launch: float):
+    """DRAM bytes per launch of `kernel_key` from profiles/traffic.json, if
+    that capture was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        tab = json.load(f)
+    ent = tab.get(kernel_key)
+    if not ent or ent.get("source_sha") != kernel_source_sha():
+        return None
+    return ent["dram_bytes_per_unit"] * units_per_launch
+
+
+def oracle_sample(w, A, B, C, seconds_target=12.0, max_rows=None):
+    """Times the CPU oracle on whole rows of C (bounded sample).
+
+    Returns (flops_per_s, rows, seconds, threads).
+    """
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+
+    def run(rows):
+        r = np.repeat(np.arange(rows, dtype=np.int64), w.N)
+        c = np.tile(np.arange(w.N, dtype=np.int64), rows)
+        t0 = time.perf_counter()
+        oracle.gemm_f64(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A, A.shape[1], B,
+                        B.shape[1], w.beta, C, w.N, points=(r, c))
+        return time.perf_counter() - t0
+
+    probe_rows = max(1, threads // 4)
+    dt = run(probe_rows)
+    per_row = max(dt / probe_rows, 1e-6)
+    rows = int(max(1, min(w.M, seconds_target / per_row)))
+    if max_rows:
+        rows = min(rows, max_rows)
+    dt = run(rows)
+    flops = 2.0 * rows * w.N * w.K
+    return flops / dt, rows, dt, threads
+
+
+# ------------------------------------------------------------------ reference arm
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = gi.WORKLOADS[WORKLOAD]
+    A, B, C = gi.make_inputs(w)
+    # size each step so the whole run stays near 2.5 minutes of CPU time
+    per_step = max(1.0, min(args.ref_seconds, 150.0 / (args.steps + 0.25 * args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, A, B, C, seconds_target=per_step / 4)
+    vals, rows_l, secs = [], [], []
+    for _ in range(args.steps):
+        v, rows, dt, threads = oracle_sample(w, A, B, C, seconds_target=per_step)
+        vals.append(v)
+        rows_l.append(rows)
+        secs.append(dt)
+    value = sum(2.0 * r * w.N * w.K for r in rows_l) / sum(secs) / 1e12
+    sample = (f"rows 0..{rows_l[-1] - 1} of C ({rows_l[-1]} x {w.N} outputs, "
+              f"{2 * rows_l[-1] * w.N * w.K:.3e} flop per step) of the {w.M}x{w.N}x{w.K} NN problem")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * statistics.mean(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, flushed=False),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, flushed=True):
+    cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+           "layout": w.transA + w.transB, "alpha": w.alpha, "beta": w.beta,
+           "dist": w.dist, "seed": w.seed, "storage": "row-major fp32"}
+    if flushed:
+        cfg["l2"] = f"flushed between steps ({FLUSH_BYTES >> 20} MB write, outside the timed events)"
+    return cfg
+
+
+# ------------------------------------------------------------------ GPU arm
+def gpu_arm(args):
+    import torch
+    import dense_fp32_gemm_05_gb300 as sg
+    from dense_fp32_gemm_05_gb300 import build as sgbuild
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sgbuild.build()
+    sg.load()
+
+    w = gi.WORKLOADS[WORKLOAD]
+    A, B, C = gi.make_inputs(w)
+    dA = torch.from_numpy(A).to(dev)
+    dB = torch.from_numpy(B).to(dev)
+    dC = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    lda, ldb, ldc = A.shape[1], B.shape[1], w.N
+
+    def call(path=sg.PATH_AUTO, out=dC, a=dA, b=dB):
+        st = sg.sgemm_ex(w.transA, w.transB, w.M, w.N, w.K, w.alpha, a.data_ptr(), lda,
+                         b.data_ptr(), ldb, w.beta, out.data_ptr(), ldc, stream, path, 0)
+        if st != 0:
+            raise sg.SgemmError(st)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, per-step CUDA events on the launching stream
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps * w.flops / (total_ms / 1e3) / 1e12
+    clocks = sampler.summary()
+
+    # ---- plan of the timed call: which kernels ran
+    st, plan = sg.sgemm_plan(w.transA, w.transB, w.M, w.N, w.K, lda, ldb, ldc, True, True, True,
+                             sg.PATH_AUTO, 0, sms)
+    launches_per_step = 1 + (1 if plan["path"] == sg.PATH_FFMA and plan["split"] > 1 else 0)
+    if plan["path"] in (sg.PATH_3XTF32, sg.PATH_TF32):
+        launches_per_step = 2 + (1 if plan["path"] == sg.PATH_3XTF32 else 0)
+
+    # ---- per-path timings on the same workload (outside the timed region)
+    peaks, peak_src = measured_peaks()
+    max_mhz = clocks["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
+    med_mhz = clocks["sm_mhz"] or max_mhz
+    ffma_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    ffma_peak_med = sms * FP32_LANES_PER_SM * 2 * med_mhz * 1e6 / 1e12
+    # TF32 tensor peak: measured bf16 (burst) x nominal tf32/bf16 ratio (1.1/2.25)
+    tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
+    paths = {}
+    rows_s, cols_s = gi.sample_points(w.M, w.N, 2048, seed=w.seed)
+    ref = bound = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        ref, bound = oracle.gemm_f64(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A, lda, B, ldb,
+                                     w.beta, C, ldc, points=(rows_s, cols_s))
+    for name, pid in (("ffma", sg.PATH_FFMA), ("3xtf32", sg.PATH_3XTF32), ("tf32", sg.PATH_TF32)):
+        try:
+            call(pid)
+        except sg.SgemmError as e:
+            paths[name] = {"status": e.status, "note": sg.sgemm_status_string(e.status)}
+            continue
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(max(3, args.path_reps)):
+            flush.fill_(0.5)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(pid)
+            e1.record(stream)
+            ms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = statistics.median([a.elapsed_time(b) for a, b in ms])
+        tfl = w.flops / (t / 1e3) / 1e12
+        ent = {"ms": t, "tflops": tfl}
+        if name == "ffma":
+            ent["frac_ffma_peak_max_clock"] = tfl / ffma_peak
+            ent["frac_ffma_peak_median_clock"] = tfl / ffma_peak_med
+        else:
+            mult = 3 if name == "3xtf32" else 1
+            ent["tensor_tflops"] = mult * tfl
+            ent["frac_tf32_tensor_peak"] = mult * tfl / tf32_peak
+        if ref is not None:
+            import oracle
+            out = dC.cpu().numpy()[rows_s, cols_s]
+            rep = oracle.compare(out, ref, bound, w.K, w.alpha)
+            ent.update({"oracle_pass": rep["pass"], "max_err_over_bound": rep["max_err_over_bound"],
+                        "max_rel": rep["max_rel"]})
+        paths[name] = ent
+
+    # ---- dominant kernel of the timed call: its launches measured alone
+    main_name = {sg.PATH_FFMA: "ffma", sg.PATH_3XTF32: "3xtf32", sg.PATH_TF32: "tf32"}[plan["path"]]
+    achieved = paths.get(main_name, {}).get("tflops", value)
+    if main_name == "ffma":
+        roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
+                    "frac": achieved / ffma_peak,
+                    "peak_median_clock": ffma_peak_med, "frac_median_clock": achieved / ffma_peak_med,
+                    "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x "
+                                  f"{max_mhz:.0f} MHz max SM clock (median under load {med_mhz:.0f} MHz)",
+                    "kernel": "ffma_gemm_kernel"}
+    else:
+        tt = paths[main_name]["tensor_tflops"]
+        roofline = {"bound": "tensor", "achieved": tt, "peak": tf32_peak, "unit": "TFLOP/s",
+                    "frac": tt / tf32_peak,
+                    "peak_basis": f"{peak_src} bf16 {peaks['bf16_tflops']} TFLOP/s x 1.1/2.25 "
+                                  "(nominal tf32/bf16 ratio)",
+                    "kernel": "tc_gemm_kernel"}
+    roofline["traffic"] = traffic_from_profiles(roofline["kernel"] + ":" + w.name, 1.0)
+
+    # ---- end to end: pinned host buffers, copies inside the timed region
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    eA = torch.empty_like(dA)
+    eB = torch.empty_like(dB)
+    for _ in range(2):
+        eA.copy_(hA, non_blocking=True)
+        eB.copy_(hB, non_blocking=True)
+        call(a=eA, b=eB)
+        hC.copy_(dC, non_blocking=True)
+    barrier()
+    e_steps = max(3, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        eA.copy_(hA, non_blocking=True)
+        eB.copy_(hB, non_blocking=True)
+        call(a=eA, b=eB)
+        hC.copy_(dC, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e_dt = time.perf_counter() - t0
+    e2e_val = world * e_steps * w.flops / e_dt / 1e12
+    h2d = A.nbytes + B.nbytes
+    d2h = w.M * w.N * 4
+
+    # ---- CPU oracle baseline (rank 0, N == 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, rows, dt, threads = oracle_sample(w, A, B, C, seconds_target=args.ref_seconds)
+        cpu = {"value": v / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of C ({rows} x {w.N} outputs, "
+                         f"{2 * rows * w.N * w.K:.3e} flop), {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(w),
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"], "samples": clocks["samples"]},
+            "plan": plan, "paths": paths, "ffma_peak_tflops": ffma_peak,
+            "wall_s_timed": t_wall, "peaks_source": peak_src,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--path-reps", type=int, default=10)
+    ap.add_argument("--ref-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-check", action="store_true", help="skip the oracle sample check")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,244 @@
+// C-ABI entry points of the single-precision GEMM library: argument checks,
+// the per-shape selector, workspace handling and kernel launches.
+// The interface is declared and documented in include/sgemm_gb300.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/sgemm_gb300.h"
+#include "ffma_kernel.cuh"
+#include "plan.h"
+#include "tc_gemm.h"
+
+namespace sgemm_gb300 {
+
+// ------------------------------------------------------------ device state
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+static std::mutex g_mu;
+static std::map<int, DeviceState> g_dev;
+// per (device, stream) workspace so that concurrent streams never share one
+static std::map<std::pair<int, cudaStream_t>, std::pair<void *, size_t>> g_ws;
+
+static int device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+        d.ready = true;
+    }
+    *out = &d;
+    return SGEMM_OK;
+}
+
+// Returns a workspace of at least `bytes` private to (device, stream).  It is
+// allocated and, when it must grow, freed in stream order on `stream`.
+int workspace(cudaStream_t stream, size_t bytes, void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto &slot = g_ws[{dev, stream}];
+    if (slot.second < bytes) {
+        if (slot.first) cudaFreeAsync(slot.first, stream);
+        slot = {nullptr, 0};
+        size_t want = std::max<size_t>(bytes, size_t(1) << 20);
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, want, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_NOMEM;
+        }
+        slot = {p, want};
+    }
+    *out = slot.first;
+    return SGEMM_OK;
+}
+
+static int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return SGEMM_OK;
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+        return SGEMM_ERR_UNSUPPORTED;
+    return SGEMM_ERR_CUDA;
+}
+
+static int grid_for(int64_t total, int sms) {
+    int64_t blocks = (total + 255) / 256;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)sms * 8));
+}
+
+// ------------------------------------------------------------ FFMA launch
+template <bool AK, bool BK_, bool V>
+static void launch_ffma_t(const ffma::Params &p, int grid, cudaStream_t s) {
+    ffma::ffma_gemm_kernel<AK, BK_, V><<<grid, ffma::THREADS, 0, s>>>(p);
+}
+
+static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K,
+                    float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                    float beta, float *C, int64_t ldc, cudaStream_t s) {
+    ffma::Params p{};
+    p.A = A; p.B = B; p.C = C; p.partial = nullptr;
+    p.lda = lda; p.ldb = ldb; p.ldc = ldc;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.alpha = alpha; p.beta = beta;
+    p.tiles_m = (int)((M + ffma::BM - 1) / ffma::BM);
+    p.tiles_n = (int)((N + ffma::BN - 1) / ffma::BN);
+    p.group_m = pl.group_m;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int total_kt = (int)((K + ffma::BK - 1) / ffma::BK);
+    int split = std::max(1, std::min(pl.split, total_kt));
+    int kt_per = (total_kt + split - 1) / split;
+    split = (total_kt + kt_per - 1) / kt_per;          // every slice owns >= 1 k-tile
+    p.dp_tiles = split == 1 ? tiles : std::min(pl.dp_tiles, tiles);
+    p.split = split;
+    p.kt_per_split = kt_per;
+    p.c_vec = pl.c_vector;
+    const int tail = tiles - p.dp_tiles;
+    if (tail > 0) {
+        void *ws = nullptr;
+        const size_t bytes = (size_t)tail * split * ffma::BM * ffma::BN * sizeof(float);
+        int st = workspace(s, bytes, &ws);
+        if (st != SGEMM_OK) return st;
+        p.partial = static_cast<float *>(ws);
+    }
+    const int grid = p.dp_tiles + tail * split;
+    const bool ak = is_notrans(ta), bk = !is_notrans(tb);
+    const bool v = pl.vector != 0;
+    if (ak && !bk && v) launch_ffma_t<true, false, true>(p, grid, s);
+    else if (ak && !bk && !v) launch_ffma_t<true, false, false>(p, grid, s);
+    else if (ak && bk && v) launch_ffma_t<true, true, true>(p, grid, s);
+    else if (ak && bk && !v) launch_ffma_t<true, true, false>(p, grid, s);
+    else if (!ak && !bk && v) launch_ffma_t<false, false, true>(p, grid, s);
+    else if (!ak && !bk && !v) launch_ffma_t<false, false, false>(p, grid, s);
+    else if (!ak && bk && v) launch_ffma_t<false, true, true>(p, grid, s);
+    else launch_ffma_t<false, true, false>(p, grid, s);
+    int st = launch_status();
+    if (st != SGEMM_OK) return st;
+    if (tail > 0) {
+        ffma::splitk_reduce_kernel<<<tail, 256, 0, s>>>(p);
+        st = launch_status();
+    }
+    return st;
+}
+
+static int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                     float *C, int64_t ldc, cudaStream_t s, int path, int split) {
+    int st = check_args(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (st != SGEMM_OK) return st;
+    if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_TF32) return SGEMM_ERR_ARG;
+    if (split < 0) return SGEMM_ERR_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+
+    DeviceState *d = nullptr;
+    st = device_state(&d);
+    if (st != SGEMM_OK) return st;
+    if (!(d->cc_major == 10 && d->cc_minor == 3)) return SGEMM_ERR_UNSUPPORTED;
+
+    if (K == 0 || alpha == 0.0f) {
+        if (beta == 1.0f) return SGEMM_OK;
+        ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc);
+        return launch_status();
+    }
+    Plan pl;
+    st = make_plan(ta, tb, M, N, K, lda, ldb, ldc, aligned16(A), aligned16(B), aligned16(C),
+                   path, split, d->sms, &pl);
+    if (st != SGEMM_OK) return st;
+    if (pl.path == SGEMM_PATH_FFMA)
+        return run_ffma(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s);
+    return run_tc(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms);
+}
+
+}  // namespace sgemm_gb300
+
+using namespace sgemm_gb300;
+
+extern "C" int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                     float *C, int64_t ldc, sgemm_stream_t stream) {
+    return gemm_impl(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     reinterpret_cast<cudaStream_t>(stream), SGEMM_PATH_AUTO, 0);
+}
+
+extern "C" int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                        float *C, int64_t ldc, sgemm_stream_t stream, int path, int split) {
+    return gemm_impl(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     reinterpret_cast<cudaStream_t>(stream), path, split);
+}
+
+extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc, int a_aligned, int b_aligned,
+                          int c_aligned, int path, int split, int num_sms, int *out_path,
+                          int *out_split, int *out_tile_m, int *out_tile_n, int *out_vector) {
+    int st = check_args(transA, transB, M, N, K, 1.0f, nullptr, lda, nullptr, ldb, 0.0f,
+                        nullptr, ldc, /*pointers_checked=*/false);
+    if (st != SGEMM_OK) return st;
+    if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_TF32 || split < 0 || num_sms <= 0)
+        return SGEMM_ERR_ARG;
+    Plan pl;
+    st = make_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned != 0, b_aligned != 0,
+                   c_aligned != 0, path, split, num_sms, &pl);
+    if (st != SGEMM_OK) return st;
+    if (out_path) *out_path = pl.path;
+    if (out_split) *out_split = pl.split;
+    if (out_tile_m) *out_tile_m = pl.tile_m;
+    if (out_tile_n) *out_tile_n = pl.tile_n;
+    if (out_vector) *out_vector = pl.vector;
+    return SGEMM_OK;
+}
+
+extern "C" const char *sgemm_status_string(int status) {
+    if (status < 0) return "invalid argument (the negated value is its 1-based position)";
+    switch (status) {
+    case SGEMM_OK: return "success";
+    case SGEMM_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case SGEMM_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case SGEMM_ERR_NOMEM: return "workspace allocation failed";
+    case SGEMM_ERR_UNSUPPORTED: return "path or device not supported for this problem";
+    case SGEMM_ERR_ARG: return "invalid argument to an auxiliary entry point";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int sgemm_device_error(sgemm_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return tc_take_device_error();
+}
+
+extern "C" int sgemm_set_wait_limit(uint64_t nanoseconds) {
+    tc_set_wait_limit(nanoseconds);
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_release_workspace(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto it = g_ws.begin(); it != g_ws.end();) {
+        if (it->first.first == dev) {
+            if (it->second.first) cudaFree(it->second.first);
+            it = g_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_version(void) { return 100; }

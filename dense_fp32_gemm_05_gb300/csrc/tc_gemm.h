@@ -1,0 +1,26 @@
+// Tensor-core (tcgen05 kind::tf32) path: 3xTF32 and single-pass TF32.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+
+namespace sgemm_gb300 {
+
+// Runs the tensor-core path chosen in `pl` (SGEMM_PATH_3XTF32 or _TF32).
+int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
+           const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+           int64_t ldc, cudaStream_t s, int sms);
+
+// Reads and clears the current device's sticky device error word.
+int tc_take_device_error();
+
+// Sets the bounded-wait limit (ns; 0 = default).
+void tc_set_wait_limit(uint64_t ns);
+
+// Library-owned per-(device, stream) workspace, grown on demand.
+int workspace(cudaStream_t stream, size_t bytes, void **out);
+
+}  // namespace sgemm_gb300

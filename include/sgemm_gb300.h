@@ -1,0 +1,158 @@
+/*
+ * sgemm_gb300.h - single-precision GEMM on one GB300 (sm_103a), C ABI.
+ *
+ *   C = alpha * op(A) * op(B) + beta * C
+ *
+ * The operation is the GEMM definition of "Optimising fp32 GEMM on A100",
+ * section "What is GEMM?" (A is M x K, B is K x N, C is M x N, alpha and beta
+ * scalars), with the alpha/beta epilogue of "CuTe-ly writing an SM86 SGEMM",
+ * section "epilogue" (C_out = alpha*(AB) + beta*C_in).  The argument list
+ * follows the BLAS xGEMM order; the host function of "CuTe-ly writing an SM86
+ * SGEMM", section "host-side setup", takes the same sizes, scalars, pointers,
+ * leading dimensions and stream.
+ *
+ * Storage: ROW-MAJOR.
+ *   transA 'N': A is stored M x K, lda >= max(1, K), op(A)(i,k) = A[i*lda + k]
+ *   transA 'T': A is stored K x M, lda >= max(1, M), op(A)(i,k) = A[k*lda + i]
+ *   transB 'N': B is stored K x N, ldb >= max(1, N), op(B)(k,j) = B[k*ldb + j]
+ *   transB 'T': B is stored N x K, ldb >= max(1, K), op(B)(k,j) = B[j*ldb + k]
+ *   C is stored M x N, ldc >= max(1, N), C(i,j) = C[i*ldc + j]
+ *   'n'/'t' are accepted; 'C'/'c' mean 'T' for real data.
+ *   A column-major caller computes its C by swapping A<->B, M<->N and the two
+ *   trans flags (C^T = op(B)^T op(A)^T).
+ *
+ * Pointers: A, B, C are DEVICE pointers owned by the caller; the library never
+ * frees or retains them.  A and B are only read.  C is read only when
+ * beta != 0 and written only inside its M x N window (the ld gap is never
+ * touched).  A and B may be NULL when M, N, K or alpha make them unused.
+ * C may not overlap A or B.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and never synchronises.  Calls on different
+ * streams may run concurrently.  The tensor-core paths use a library-owned
+ * workspace (per device, grown on demand with cudaMallocAsync on the calling
+ * stream, kept until sgemm_release_workspace()).
+ *
+ * Errors: arguments are checked before anything is launched.  A negative
+ * return value -i names the i-th argument (1-based, BLAS style) as invalid:
+ * -1 transA, -2 transB, -3 M, -4 N, -5 K, -7 A, -8 lda, -9 B, -10 ldb,
+ * -12 C, -13 ldc.  Positive values are sgemm_status codes below.
+ *
+ * Quick returns (BLAS rules): M == 0 or N == 0 does nothing.  K == 0 or
+ * alpha == 0 sets C = beta*C without reading A or B, and C = 0 when
+ * beta == 0 (C is not read, so NaN in C does not propagate).
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *sgemm_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_CUDA = 1,        /* a CUDA call or a kernel launch failed      */
+    SGEMM_ERR_TIMEOUT = 2,     /* a bounded device-side wait ran out          */
+    SGEMM_ERR_NOMEM = 3,       /* the workspace could not be allocated        */
+    SGEMM_ERR_UNSUPPORTED = 4, /* the forced path cannot run this problem or
+                                  this device (e.g. not compute capability 10.3) */
+    SGEMM_ERR_ARG = 5          /* an argument of an auxiliary entry point     */
+} sgemm_status;
+
+/* Arithmetic path.  AUTO lets the per-shape selector choose among the
+   fp32-accurate paths (FFMA and 3xTF32); TF32 is never chosen by AUTO. */
+typedef enum {
+    SGEMM_PATH_AUTO = 0,
+    SGEMM_PATH_FFMA = 1,   /* CUDA-core fp32 FMA, 128x128 block tiles, 8x8
+                              register outer products ("Matmul II: register
+                              blocking, warp tiling, tensor cores", sections
+                              3-5).  Sums each output in ascending k with
+                              fused multiply-adds, so with split == 1 its
+                              result is bit-identical to the naive loop
+                              ("How to get a matmul kernel into the top
+                              percentile (worklog)", "Optimization 1").     */
+    SGEMM_PATH_3XTF32 = 2, /* tensor cores (tcgen05 kind::tf32, TMEM
+                              accumulators, TMA operand loads) with each
+                              operand split x = hi + lo into two TF32 parts
+                              and the three products lo*hi + hi*lo + hi*hi
+                              accumulated in fp32: fp32-level accuracy.      */
+    SGEMM_PATH_TF32 = 3    /* the same tensor-core kernel with only hi*hi:
+                              single-pass TF32, LOWER accuracy than fp32
+                              ("Optimising fp32 GEMM on A100", "Kernel 1").  */
+} sgemm_path;
+
+/*
+ * sgemm - C = alpha*op(A)*op(B) + beta*C on `stream`, path chosen per shape.
+ * Returns SGEMM_OK, a negative argument index, or an sgemm_status code.
+ */
+int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
+          float alpha, const float *A, int64_t lda,
+          const float *B, int64_t ldb,
+          float beta, float *C, int64_t ldc, sgemm_stream_t stream);
+
+/*
+ * sgemm_ex - as sgemm, with the path forced (sgemm_path) and the split-K
+ * factor forced (split >= 1, or 0 to let the selector decide).  The split
+ * applies to the FFMA path: split > 1 sums K in `split` contiguous slices
+ * whose partial results are added in a fixed order (deterministic, but no
+ * longer bit-identical to the naive loop).
+ * Returns SGEMM_ERR_UNSUPPORTED when the forced path cannot run the problem.
+ */
+int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
+             float alpha, const float *A, int64_t lda,
+             const float *B, int64_t ldb,
+             float beta, float *C, int64_t ldc, sgemm_stream_t stream,
+             int path, int split);
+
+/*
+ * sgemm_plan - the selector's decision for a problem, without launching
+ * anything and without touching the GPU.  `path` and `split` as in
+ * sgemm_ex (0 = let the selector decide).  a_aligned/b_aligned/c_aligned
+ * say whether the base pointer is 16-byte aligned.  On success writes the
+ * chosen path (sgemm_path), the FFMA split-K factor, the tile rows and
+ * columns, and whether 16-byte vector loads are used (1) or the 4-byte
+ * edge path (0).  Any output pointer may be NULL.
+ * Returns SGEMM_OK or a negative argument index as sgemm.
+ */
+int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
+               int64_t lda, int64_t ldb, int64_t ldc,
+               int a_aligned, int b_aligned, int c_aligned,
+               int path, int split, int num_sms,
+               int *out_path, int *out_split, int *out_tile_m, int *out_tile_n,
+               int *out_vector);
+
+/* Static description of a status code (never NULL). */
+const char *sgemm_status_string(int status);
+
+/*
+ * sgemm_device_error - synchronises `stream`, then returns and clears the
+ * library's sticky device error word on the current device: SGEMM_OK, or
+ * SGEMM_ERR_TIMEOUT when a bounded device-side wait gave up (the kernel
+ * then stopped early and its C is undefined).  SGEMM_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int sgemm_device_error(sgemm_stream_t stream);
+
+/*
+ * sgemm_set_wait_limit - spin limit for the device-side waits of the
+ * tensor-core path, in nanoseconds of %globaltimer (0 restores the default
+ * of 2 s).  A test hook: a tiny limit makes a wait run out on purpose so that
+ * the timeout path can be checked without hanging anything.
+ */
+int sgemm_set_wait_limit(uint64_t nanoseconds);
+
+/* Free the current device's workspace (synchronises the device). */
+int sgemm_release_workspace(void);
+
+/* Library version, 100*major + minor. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

@@ -1,0 +1,124 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds, loads,
+exports every entry point the header declares, validates arguments BLAS-style
+before touching the device, and its selector makes the documented choices."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dense_fp32_gemm_05_gb300 as sg
+from dense_fp32_gemm_05_gb300 import build as sgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sgbuild.build()
+    return sg.load()
+
+
+def header_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(sgemm\w*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = header_functions()
+    assert {"sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sg.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
+    for name in header_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    for name in sg.exported_symbols():
+        assert name in exported
+
+
+def test_version_and_status_strings(lib):
+    assert sg.sgemm_version() >= 100
+    for st in (0, 1, 2, 3, 4, 5):
+        assert sg.sgemm_status_string(st)
+    assert "argument" in sg.sgemm_status_string(-3)
+
+
+FAKE = 1 << 20   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("args,want", [
+    (("X", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -1),
+    (("N", "Z", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -2),
+    (("N", "N", -1, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -3),
+    (("N", "N", 4, -2, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -4),
+    (("N", "N", 4, 4, -5, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -5),
+    (("N", "N", 4, 4, 4, 1.0, 0, 4, FAKE, 4, 0.0, FAKE, 4), -7),
+    (("N", "N", 4, 4, 8, 1.0, FAKE, 7, FAKE, 4, 0.0, FAKE, 4), -8),
+    (("T", "N", 9, 4, 8, 1.0, FAKE, 8, FAKE, 4, 0.0, FAKE, 4), -8),
+    (("N", "N", 4, 4, 4, 1.0, FAKE, 4, 0, 4, 0.0, FAKE, 4), -9),
+    (("N", "N", 4, 6, 4, 1.0, FAKE, 4, FAKE, 5, 0.0, FAKE, 6), -10),
+    (("N", "T", 4, 6, 9, 1.0, FAKE, 9, FAKE, 8, 0.0, FAKE, 6), -10),
+    (("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, 0, 4), -12),
+    (("N", "N", 4, 6, 4, 1.0, FAKE, 4, FAKE, 6, 0.0, FAKE, 5), -13),
+    (("N", "N", 2 ** 31, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -3),
+])
+def test_argument_validation_without_gpu(lib, args, want):
+    assert sg.sgemm(*args) == want
+    assert sg.sgemm_ex(*args, path=sg.PATH_FFMA, split=1) == want
+
+
+def test_quick_return_touches_nothing(lib):
+    # M == 0 / N == 0: nothing to do, valid with null pointers, no CUDA call
+    assert sg.sgemm("N", "N", 0, 5, 7, 1.0, 0, 7, 0, 5, 0.0, 0, 5) == sg.SGEMM_OK
+    assert sg.sgemm("T", "T", 5, 0, 7, 1.0, 0, 5, 0, 7, 1.0, 0, 1) == sg.SGEMM_OK
+
+
+def test_aux_argument_errors(lib):
+    assert sg.sgemm_ex("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4,
+                       path=9) == sg.SGEMM_ERR_ARG
+    assert sg.sgemm_ex("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4,
+                       split=-1) == sg.SGEMM_ERR_ARG
+    st, _ = sg.sgemm_plan("N", "N", 8, 8, 8, 8, 8, 8, num_sms=0)
+    assert st == sg.SGEMM_ERR_ARG
+
+
+def test_plan_vector_and_edge_path(lib):
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096)
+    assert st == 0 and p["vector"] == 1 and p["path"] == sg.PATH_FFMA
+    assert (p["tile_m"], p["tile_n"]) == (128, 128)
+    # odd leading dimensions: 16-byte loads are illegal, the 4-byte path runs
+    st, p = sg.sgemm_plan("N", "T", 4095, 3073, 1537, 1537, 1537, 3073)
+    assert st == 0 and p["vector"] == 0
+    # misaligned base pointer
+    st, p = sg.sgemm_plan("N", "N", 512, 512, 512, 512, 512, 512, a_aligned=False)
+    assert st == 0 and p["vector"] == 0
+
+
+def test_plan_split_k_for_small_grids(lib):
+    # 256^3: 4 tiles for 304 CTA slots -> the K loop is split
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152)
+    assert st == 0 and p["split"] > 1
+    # 16384 x 64 x 8192 skinny: 128 tiles, long K -> split
+    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152)
+    assert st == 0 and p["split"] > 1
+    # forced split is honoured, forced 1 disables it
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=1)
+    assert p["split"] == 1
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=3)
+    assert p["split"] == 3
+
+
+def test_plan_forced_tensor_core_path(lib):
+    st, p = sg.sgemm_plan("N", "N", 1024, 1024, 1024, 1024, 1024, 1024, path=sg.PATH_3XTF32)
+    assert st == 0 and p["path"] == sg.PATH_3XTF32
