@@ -103,9 +103,11 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         }
         if (pl.split == 1) pl.dp_tiles = (int)tiles;
     } else {
+        // tensor-core path: 128-row tiles, N of the MMA from the problem's N
         pl.tile_m = 128;
-        pl.tile_n = 256;
+        pl.tile_n = N > 128 ? 256 : (N > 64 ? 128 : 64);
         pl.split = 1;
+        pl.dp_tiles = (int)(((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n));
     }
     *out = pl;
     return 0;

@@ -1,15 +1,550 @@
-// Tensor-core path (placeholder until the tcgen05 kernel lands).
+// Tensor-core path for sm_103a: tcgen05 kind::tf32 MMAs into TMEM, operands
+// brought into shared memory by TMA, fp32 accuracy by a 3xTF32 split.
+//
+// Each fp32 operand x is split once, in a pre-pass, into two TF32 numbers:
+// hi = rna_tf32(x), lo = rna_tf32(x - hi) (x - hi is exact in fp32).  Then
+//   a*b = a_hi*b_hi + a_hi*b_lo + a_lo*b_hi + a_lo*b_lo
+// and the last term (~2^-22 |ab|) is dropped: the three TF32 products are
+// accumulated in fp32 in TMEM.  Single-pass TF32 keeps only a_hi*b_hi (the
+// tensor-core mode of "Optimising fp32 GEMM on A100", kernels 1-7, which
+// trade accuracy for speed).
+//
+// Kernel layout (one CTA per 128 x BN tile of C, 192 threads):
+//   warp 0, one lane : TMA producer - per k-block of 32 (128 bytes, the
+//                      128-byte swizzle span) loads A_hi/A_lo (128 x 32) and
+//                      B_hi/B_lo (BN x 32) into a ring of shared stages,
+//                      completing on the stage's "full" mbarrier;
+//   warp 1           : allocates BN TMEM columns; one lane issues the MMAs
+//                      (M = 128, N = BN, K = 8) for each k-block and commits
+//                      them to the stage's "empty" mbarrier, then to the
+//                      "accumulator ready" mbarrier after the last block;
+//   warps 2..5       : epilogue - tcgen05.ld of the 128 x BN accumulator
+//                      (warp w reads TMEM lanes 32*(w%4)..+31 = its rows),
+//                      C = alpha*acc + beta*C, stores.
+// The multi-stage ring is the asynchronous copy pipeline of "CuTe-ly
+// writing an SM86 SGEMM" (section "mainloop") and "Matmul II" (section 7)
+// rebuilt on TMA + mbarriers; the operand and accumulator placement is
+// Blackwell's (shared-memory descriptors, TMEM) and has no counterpart on
+// the pages.
+// Every mbarrier wait is bounded (%globaltimer): on expiry the thread sets
+// the library's device error word, stops its role, drains what it issued
+// (also bounded) and the CTA frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "ptx_util.cuh"
 #include "tc_gemm.h"
 
 namespace sgemm_gb300 {
+namespace tc {
 
-int run_tc(const Plan &, char, char, int64_t, int64_t, int64_t, float, const float *, int64_t,
-           const float *, int64_t, float, float *, int64_t, cudaStream_t, int) {
-    return SGEMM_ERR_UNSUPPORTED;
+constexpr int BM = 128;
+constexpr int BK = 32;                 // fp32 per k-block = 128 bytes
+constexpr int THREADS = 192;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
+// Limit of the teardown waits (copies and MMAs already issued must retire
+// before the CTA frees TMEM and exits); independent of the test hook so that
+// a tiny role-wait limit never cuts a drain short.
+constexpr uint64_t kDrainNs = 1000000000ull;         // 1 s
+
+__device__ unsigned int g_error;        // sticky device error word (per device)
+
+template <int BN, bool THREE>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 4;
+    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int PARTS = THREE ? 2 : 1;
+    static constexpr int STAGE_BYTES = PARTS * (A_BYTES + B_BYTES);
+    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = BN;            // power of two >= 32
+    static_assert(STAGES >= 2, "need at least two stages");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "N of the MMA");
+};
+
+struct Params {
+    float *C;
+    int64_t ldc;
+    int M, N, K;
+    float alpha, beta;
+    int tiles_m, tiles_n, group_m;
+    int num_kb;                 // k-blocks of 32
+    int c_vec;                  // C 16-byte aligned, ldc % 4 == 0
+    unsigned long long wait_ns; // bounded-wait limit
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
 }
 
-int tc_take_device_error() { return SGEMM_OK; }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
 
-void tc_set_wait_limit(uint64_t) {}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Returns false (and
+// raises the device error word) when the limit passes first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicExch(&g_error, (unsigned)SGEMM_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), descriptor
+// version 1, base offset 0 (every tile is 1024-byte aligned).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+    d |= (uint64_t)1 << 46;                           // version
+    d |= (uint64_t)2 << 61;                           // swizzle: 128B
+    return d;
+}
+
+// Instruction descriptor of kind::tf32: D fp32, A and B tf32, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+template <int BN>
+__device__ __forceinline__ constexpr uint32_t idesc_tf32() {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit accumulators -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- kernel
+__device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group_m, int &tm,
+                                       int &tn) {
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int gm = min(tiles_m - first_m, group_m);
+    const int r = t - g * per_group;
+    tm = first_m + r % gm;
+    tn = r / gm;
+}
+
+template <int BN, bool THREE>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi,
+                   const __grid_constant__ CUtensorMap tm_alo,
+                   const __grid_constant__ CUtensorMap tm_bhi,
+                   const __grid_constant__ CUtensorMap tm_blo, const Params p) {
+    using K_ = Cfg<BN, THREE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_::STAGES * K_::STAGE_BYTES);
+    // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * K_::STAGES + 1);
+    const uint32_t smem0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (K_::STAGES + s); };
+    const uint32_t acc_bar = bar0 + 8u * (2 * K_::STAGES);
+    auto a_hi = [&](int s) { return smem0 + s * K_::STAGE_BYTES; };
+    auto b_hi = [&](int s) { return a_hi(s) + K_::A_BYTES; };
+    auto a_lo = [&](int s) { return b_hi(s) + K_::B_BYTES; };
+    auto b_lo = [&](int s) { return a_lo(s) + K_::A_BYTES; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < K_::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_map(&tm_ahi);
+        prefetch_map(&tm_bhi);
+        if (THREE) {
+            prefetch_map(&tm_alo);
+            prefetch_map(&tm_blo);
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(tmem_slot)), "r"(K_::TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int tm, tn;
+    raster(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int nkb = p.num_kb;
+    const uint64_t lim = p.wait_ns;
+
+    // Roles are dispatched per WARP: the epilogue's tcgen05.ld is warp-collective,
+    // so no lane of the producer or MMA warp may fall into it.
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % K_::STAGES;
+                const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) break;
+                mbar_expect_tx(full_bar(s), K_::STAGE_BYTES);
+                const int kc = kb * BK;
+                tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, m0);
+                tma_load_2d(b_hi(s), &tm_bhi, full_bar(s), kc, n0);
+                if (THREE) {
+                    tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
+                    tma_load_2d(b_lo(s), &tm_blo, full_bar(s), kc, n0);
+                }
+                ++issued;
+            }
+            // drain: the last arming of each stage must have landed before exit
+            for (int kb = (issued > K_::STAGES ? issued - K_::STAGES : 0); kb < issued; ++kb)
+                mbar_wait(full_bar(kb % K_::STAGES), (uint32_t)(kb / K_::STAGES) & 1u, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_tf32<BN>();
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % K_::STAGES;
+                const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
+                if (!mbar_wait(full_bar(s), ph, lim)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    const uint32_t off = kk * 32;            // 8 tf32 = 32 bytes
+                    const uint64_t ah = smem_desc_sw128(a_hi(s) + off);
+                    const uint64_t bh = smem_desc_sw128(b_hi(s) + off);
+                    const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                    if (THREE) {
+                        const uint64_t al = smem_desc_sw128(a_lo(s) + off);
+                        const uint64_t bl = smem_desc_sw128(b_lo(s) + off);
+                        umma_tf32(tmem, al, bh, idesc, first);
+                        umma_tf32(tmem, ah, bl, idesc, 1u);
+                        umma_tf32(tmem, ah, bh, idesc, 1u);
+                    } else {
+                        umma_tf32(tmem, ah, bh, idesc, first);
+                    }
+                }
+                umma_commit(empty_bar(s));
+            }
+            umma_commit(acc_bar);
+            // all MMAs of this CTA retired before TMEM can be freed
+            mbar_wait(acc_bar, 0u, kDrainNs);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                       // TMEM lane quarter
+        const bool ready = mbar_wait(acc_bar, 0u, lim);
+        tc_fence_after();
+        if (ready) {
+            const int row = m0 + q * 32 + lane;
+            const float alpha = p.alpha, beta = p.beta;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                const int col0 = n0 + c * 32;
+                if (row < p.M && col0 < p.N) {
+                    float *dst = p.C + (int64_t)row * p.ldc + col0;
+                    if (p.c_vec && col0 + 31 < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 o;
+                            const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
+                            const float v2 = __uint_as_float(r[j + 2]), v3 = __uint_as_float(r[j + 3]);
+                            if (beta == 0.0f) {
+                                o = make_float4(__fmul_rn(alpha, v0), __fmul_rn(alpha, v1),
+                                                __fmul_rn(alpha, v2), __fmul_rn(alpha, v3));
+                            } else {
+                                const float4 ci = *reinterpret_cast<const float4 *>(dst + j);
+                                o = make_float4(__fmaf_rn(alpha, v0, __fmul_rn(beta, ci.x)),
+                                                __fmaf_rn(alpha, v1, __fmul_rn(beta, ci.y)),
+                                                __fmaf_rn(alpha, v2, __fmul_rn(beta, ci.z)),
+                                                __fmaf_rn(alpha, v3, __fmul_rn(beta, ci.w)));
+                            }
+                            *reinterpret_cast<float4 *>(dst + j) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (col0 + j < p.N) {
+                                const float v = __uint_as_float(r[j]);
+                                dst[j] = (beta == 0.0f) ? __fmul_rn(alpha, v)
+                                                        : __fmaf_rn(alpha, v, __fmul_rn(beta, dst[j]));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(K_::TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- split pre-pass
+__device__ __forceinline__ float rna_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// out[r][k] (r < rows, k < Kp, row stride Kp) = op value at (r, k) for k < K,
+// 0 for K <= k < Kp; hi = rna_tf32(x), lo = rna_tf32(x - hi).
+// TRANS: the source is stored k-major (src[k*ld + r]), else src[r*ld + k].
+// 32 x 32 tiles through shared memory so reads and writes are both coalesced.
+template <bool TRANS, bool THREE>
+__global__ void __launch_bounds__(256)
+    split_kernel(const float *__restrict__ src, int64_t ld, int rows, int K, int Kp,
+                 float *__restrict__ hi, float *__restrict__ lo) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    const int k0 = blockIdx.x * 32;
+    const int r0 = blockIdx.y * 32;
+    if (TRANS) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + ty + 8 * i, r = r0 + tx;
+            tile[ty + 8 * i][tx] = (k < K && r < rows) ? src[(int64_t)k * ld + r] : 0.0f;
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + ty + 8 * i, k = k0 + tx;
+        if (r >= rows) continue;
+        float x;
+        if (TRANS) x = tile[tx][ty + 8 * i];
+        else x = (k < K) ? src[(int64_t)r * ld + k] : 0.0f;
+        const float h = rna_tf32(x);
+        const int64_t o = (int64_t)r * Kp + k;
+        hi[o] = h;
+        if (THREE) lo[o] = rna_tf32(__fsub_rn(x, h));
+    }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a [rows][Kp] fp32 array: box 32 (k) x box_rows, 128-byte swizzle,
+// rows past `rows` read as zeros.
+static bool make_map(CUtensorMap *m, const float *base, int rows, int Kp, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)Kp * sizeof(float)};
+    cuuint32_t box[2] = {(cuuint32_t)tc::BK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static std::mutex g_tc_mu;
+static uint64_t g_wait_ns = tc::kDefaultWaitNs;
+
+void tc_set_wait_limit(uint64_t ns) {
+    std::lock_guard<std::mutex> lk(g_tc_mu);
+    g_wait_ns = ns ? ns : tc::kDefaultWaitNs;
+}
+
+int tc_take_device_error() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, tc::g_error, sizeof(v)) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(tc::g_error, &zero, sizeof(zero)) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return v == 0 ? SGEMM_OK : (int)v;
+}
+
+static int last_status() {
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return SGEMM_OK;
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+        return SGEMM_ERR_UNSUPPORTED;
+    return SGEMM_ERR_CUDA;
+}
+
+template <bool THREE>
+static void launch_split(const float *src, int64_t ld, bool trans, int rows, int K, int Kp,
+                         float *hi, float *lo, cudaStream_t s) {
+    dim3 grid(Kp / 32, (rows + 31) / 32);
+    if (trans) tc::split_kernel<true, THREE><<<grid, 256, 0, s>>>(src, ld, rows, K, Kp, hi, lo);
+    else tc::split_kernel<false, THREE><<<grid, 256, 0, s>>>(src, ld, rows, K, Kp, hi, lo);
+}
+
+template <int BN, bool THREE>
+static int launch_main(const CUtensorMap *maps, const tc::Params &p, cudaStream_t s) {
+    using K_ = tc::Cfg<BN, THREE>;
+    // the shared-memory opt-in is a per-device function attribute
+    static uint64_t attr_done = 0;   // bit d: set on device d
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(tc::tc_gemm_kernel<BN, THREE>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM) !=
+            cudaSuccess)
+            return last_status();
+        __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
+    }
+    tc::tc_gemm_kernel<BN, THREE><<<p.tiles_m * p.tiles_n, tc::THREADS, K_::SMEM, s>>>(
+        maps[0], maps[1], maps[2], maps[3], p);
+    return last_status();
+}
+
+int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
+           const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+           int64_t ldc, cudaStream_t s, int sms) {
+    (void)sms;
+    const bool three = pl.path == SGEMM_PATH_3XTF32;
+    const int BN = pl.tile_n;
+    const int Kp = (int)((K + tc::BK - 1) / tc::BK) * tc::BK;
+    auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
+    const size_t a_elems = up((size_t)M * Kp * 4) / 4;
+    const size_t b_elems = up((size_t)N * Kp * 4) / 4;
+    const int parts = three ? 2 : 1;
+    void *ws = nullptr;
+    int st = workspace(s, (size_t)parts * (a_elems + b_elems) * 4, &ws);
+    if (st != SGEMM_OK) return st;
+    float *a_hi = static_cast<float *>(ws);
+    float *b_hi = a_hi + a_elems;
+    float *a_lo = three ? b_hi + b_elems : a_hi;
+    float *b_lo = three ? a_lo + a_elems : b_hi;
+
+    // canonical K-major operands: A as [M][Kp], B as [N][Kp]
+    const bool a_trans = !is_notrans(ta);   // A stored K x M
+    const bool b_trans = is_notrans(tb);    // B stored K x N
+    if (three) {
+        launch_split<true>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, a_lo, s);
+        launch_split<true>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, b_lo, s);
+    } else {
+        launch_split<false>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, nullptr, s);
+        launch_split<false>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, nullptr, s);
+    }
+    st = last_status();
+    if (st != SGEMM_OK) return st;
+
+    CUtensorMap maps[4];
+    if (!make_map(&maps[0], a_hi, (int)M, Kp, tc::BM) || !make_map(&maps[1], a_lo, (int)M, Kp, tc::BM) ||
+        !make_map(&maps[2], b_hi, (int)N, Kp, BN) || !make_map(&maps[3], b_lo, (int)N, Kp, BN))
+        return SGEMM_ERR_UNSUPPORTED;
+
+    tc::Params p{};
+    p.C = C; p.ldc = ldc; p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.alpha = alpha; p.beta = beta;
+    p.tiles_m = (int)((M + tc::BM - 1) / tc::BM);
+    p.tiles_n = (int)((N + BN - 1) / BN);
+    p.group_m = 16;
+    p.num_kb = Kp / tc::BK;
+    p.c_vec = pl.c_vector;
+    {
+        std::lock_guard<std::mutex> lk(g_tc_mu);
+        p.wait_ns = g_wait_ns;
+    }
+    if (BN == 256) return three ? launch_main<256, true>(maps, p, s) : launch_main<256, false>(maps, p, s);
+    if (BN == 128) return three ? launch_main<128, true>(maps, p, s) : launch_main<128, false>(maps, p, s);
+    return three ? launch_main<64, true>(maps, p, s) : launch_main<64, false>(maps, p, s);
+}
 
 }  // namespace sgemm_gb300

@@ -20,7 +20,7 @@ from tests import gpu_harness as gh
 pytestmark = pytest.mark.gpu
 
 LAYOUTS = [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")]
-ACCURATE_PATHS = [sg.PATH_FFMA]
+ACCURATE_PATHS = [sg.PATH_FFMA, sg.PATH_3XTF32]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -69,6 +69,14 @@ def test_all_ones_exact(path, ta, tb):
     assert st == 0 and np.all(out == np.float32(2 * K - 1.5))
 
 
+def same_or_split_exact(out, want, path):
+    """FFMA: bit-exact.  3xTF32: x*1 is computed as hi(x) + lo(x), which drops
+    the part of x below the 22nd significant bit: |out - x| <= 2^-22 |x|."""
+    if path == sg.PATH_FFMA:
+        return np.array_equal(out, want)
+    return bool(np.all(np.abs(out.astype(np.float64) - want) <= 2.0 ** -22 * np.abs(want)))
+
+
 @pytest.mark.parametrize("path", ACCURATE_PATHS)
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_identity_and_permutation_exact(path, ta, tb):
@@ -78,19 +86,19 @@ def test_identity_and_permutation_exact(path, ta, tb):
     eye = np.eye(M, dtype=np.float32)
     st, out = gh.run(ta, tb, M, N, M, 1.0, stored(eye, ta), M, stored(X, tb), ld_of(stored(X, tb)),
                      0.0, None, N, path=path)
-    assert st == 0 and np.array_equal(out, X)
+    assert st == 0 and same_or_split_exact(out, X, path)
     perm = rng.permutation(M)
     P = np.zeros((M, M), np.float32)
     P[np.arange(M), perm] = 1.0
     st, out = gh.run(ta, tb, M, N, M, 1.0, stored(P, ta), M, stored(X, tb), ld_of(stored(X, tb)),
                      0.0, None, N, path=path)
-    assert st == 0 and np.array_equal(out, X[perm])
+    assert st == 0 and same_or_split_exact(out, X[perm], path)
     sigma = rng.permutation(N)
     Q = np.zeros((N, N), np.float32)
     Q[sigma, np.arange(N)] = 1.0
     st, out = gh.run(ta, tb, M, N, N, 1.0, stored(X, ta), ld_of(stored(X, ta)), stored(Q, tb), N,
                      0.0, None, N, path=path)
-    assert st == 0 and np.array_equal(out, X[:, sigma])
+    assert st == 0 and same_or_split_exact(out, X[:, sigma], path)
 
 
 @pytest.mark.parametrize("path", ACCURATE_PATHS)
@@ -182,8 +190,16 @@ def test_brute_force_tiny_shapes(oracle_mod, path, ta, tb):
         st, out = gh.run(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C if beta else None, ldc,
                          path=path, offsets=(t % 2, 0, (t // 2) % 2))
         assert st == 0, (M, N, K)
-        oracle_check(oracle_mod, ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta, C,
-                     out)
+        if path == sg.PATH_3XTF32 and K < 16:
+            # the dropped lo*lo and residual terms (~3*2^-22 |ab| per product)
+            # can exceed 4*K*2^-24 for K < 3; the selector never sends K < 16
+            # here, a forced call is held to 4*16*2^-24 instead
+            ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, alpha, A, A.shape[1], B,
+                                             B.shape[1], beta, C, N)
+            assert np.all(np.abs(out - ref) <= bound * 16.0 / K), (M, N, K)
+        else:
+            oracle_check(oracle_mod, ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta,
+                         C, out)
 
 
 # ------------------------------------------------------------ BLAS special cases

@@ -1,0 +1,109 @@
+"""Tensor-core specific GPU checks: the single-pass TF32 mode against its own
+error bound, the 3xTF32 error budget at full size, and the bounded-wait
+timeout path (a wait made to run out on purpose through the test hook)."""
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_05_gb300 as sg
+import gemm_inputs as gi
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from dense_fp32_gemm_05_gb300 import build
+    build.build()
+    sg.load()
+
+
+def stored(op_mat, trans):
+    return np.ascontiguousarray(op_mat if trans == "N" else op_mat.T)
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_tf32_exact_on_small_integers(ta, tb):
+    """Integers up to 2^11 are exact in TF32, so single-pass TF32 is exact."""
+    M, N, K = 257, 300, 100
+    opA, opB = gi.small_ints(1, (M, K)), gi.small_ints(2, (K, N))
+    A, B = stored(opA, ta), stored(opB, tb)
+    st, out = gh.run(ta, tb, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, None, N,
+                     path=sg.PATH_TF32)
+    assert st == 0
+    assert np.array_equal(out.astype(np.int64), opA.astype(np.int64) @ opB.astype(np.int64))
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_tf32_within_its_own_bound(oracle_mod, ta, tb):
+    """Single-pass TF32 rounds each operand to 11 significant bits, so each
+    product is off by at most ~2^-10 |a||b|; the sum adds the fp32 term.  The
+    measured error is reported; it is expected to exceed the fp32 bound."""
+    M, N, K = 300, 260, 700
+    opA = gi.random_matrix(5, M, K)
+    opB = gi.random_matrix(6, K, N)
+    C = gi.random_matrix(7, M, N)
+    A, B = stored(opA, ta), stored(opB, tb)
+    st, out = gh.run(ta, tb, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.5, C, N,
+                     path=sg.PATH_TF32)
+    assert st == 0
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.5, C, N)
+    mag = bound / (4 * K * 2.0 ** -24)            # |alpha||A||B| + |beta||C|
+    tf32_bound = (2.0 ** -10 + 4 * K * 2.0 ** -24) * mag
+    err = np.abs(out - ref)
+    assert np.all(err <= tf32_bound)
+    rep = oracle_mod.compare(out, ref, bound, K, 1.0)
+    print(f"tf32 {ta}{tb}: max rel {rep['max_rel']:.3g}, normwise {rep['normwise_rel']:.3g}, "
+          f"max err / fp32 bound {rep['max_err_over_bound']:.3g}")
+    assert rep["normwise_rel"] < 1e-3
+
+
+def test_3xtf32_headline_size_error_budget(oracle_mod):
+    """3xTF32 at 4096^3 (the measured workload): every sampled entry within
+    the fp32 bound, with room to spare."""
+    import torch
+    w = gi.WORKLOADS["sq4096_nn"]
+    A, B, _ = gi.make_inputs(w)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.empty((w.M, w.N), device="cuda")
+    st = sg.sgemm_ex("N", "N", w.M, w.N, w.K, 1.0, dA.data_ptr(), w.K, dB.data_ptr(), w.N, 0.0,
+                     dC.data_ptr(), w.N, torch.cuda.current_stream(), sg.PATH_3XTF32, 0)
+    assert st == 0 and sg.sgemm_device_error(torch.cuda.current_stream()) == 0
+    rows, cols = gi.sample_points(w.M, w.N, 3000, seed=11)
+    ref, bound = oracle_mod.gemm_f64("N", "N", w.M, w.N, w.K, 1.0, A, w.K, B, w.N, 0.0, None,
+                                     w.N, points=(rows, cols))
+    rep = oracle_mod.compare(dC.cpu().numpy()[rows, cols], ref, bound, w.K, 1.0)
+    assert rep["pass"] and rep["max_err_over_bound"] < 0.25, rep
+
+
+@pytest.mark.parametrize("path", [sg.PATH_3XTF32, sg.PATH_TF32])
+def test_bounded_wait_timeout_reports_and_recovers(oracle_mod, path):
+    """A 1 ns wait limit makes the kernel's mbarrier waits run out: the
+    kernel must give up, raise SGEMM_ERR_TIMEOUT through the device error
+    word, free its resources and leave the context usable."""
+    import torch
+    M, N, K = 512, 512, 2048
+    A = gi.random_matrix(1, M, K)
+    B = gi.random_matrix(2, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), device="cuda")
+    s = torch.cuda.current_stream()
+    assert sg.sgemm_device_error(s) == 0
+    assert sg.sgemm_set_wait_limit(1) == 0
+    try:
+        st = sg.sgemm_ex("N", "N", M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                         dC.data_ptr(), N, s, path, 0)
+        assert st == 0
+        assert sg.sgemm_device_error(s) == sg.SGEMM_ERR_TIMEOUT
+        assert sg.sgemm_device_error(s) == 0          # read-and-clear
+    finally:
+        sg.sgemm_set_wait_limit(0)
+    st = sg.sgemm_ex("N", "N", M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                     dC.data_ptr(), N, s, sg.PATH_3XTF32, 0)
+    assert st == 0 and sg.sgemm_device_error(s) == 0
+    ref, bound = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    assert oracle_mod.compare(dC.cpu().numpy(), ref, bound, K, 1.0)["pass"]
