@@ -126,29 +126,35 @@ def measured_peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(files):
+    """Short sha of a kernel's own source files (as profiles/traffic.json keys them)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_gemm_05_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode())
-                h.update(f.read())
+    for fn in files:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel_key: str, units_per_launch: float):
-    """DRAM bytes per launch of `kernel_key` from profiles/traffic.json, if
-    that capture was taken on the current kernel sources; else None."""
+def traffic_from_profiles(kernel_key: str):
+    """DRAM bytes (read + write) per launch of `kernel_key` from
+    profiles/traffic.json, if that ncu capture was taken on the kernel's
+    current source files; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         tab = json.load(f)
     ent = tab.get(kernel_key)
-    if not ent or ent.get("source_sha") != kernel_source_sha():
+    if not ent:
         return None
-    return ent["dram_bytes_per_unit"] * units_per_launch
+    try:
+        if ent.get("source_sha") != kernel_source_sha(ent["files"]):
+            return None
+    except OSError:
+        return None
+    return ent["dram_bytes_per_launch"]
 
 
 def oracle_sample(w, A, B, C, seconds_target=12.0, max_rows=None):
@@ -372,7 +378,7 @@ def gpu_arm(args):
                     "peak_basis": f"{peak_src} bf16 {peaks['bf16_tflops']} TFLOP/s x 1.1/2.25 "
                                   "(nominal tf32/bf16 ratio)",
                     "kernel": "tc_gemm_kernel"}
-    roofline["traffic"] = traffic_from_profiles(roofline["kernel"] + ":" + w.name, 1.0)
+    roofline["traffic"] = traffic_from_profiles(roofline["kernel"] + ":" + w.name)
 
     # ---- end to end: pinned host buffers, copies inside the timed region
     hA = torch.from_numpy(A).pin_memory()
