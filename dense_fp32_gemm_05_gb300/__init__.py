@@ -14,11 +14,11 @@ import threading
 
 __all__ = [
     "SGEMM_OK", "SGEMM_ERR_CUDA", "SGEMM_ERR_TIMEOUT", "SGEMM_ERR_NOMEM",
-    "SGEMM_ERR_UNSUPPORTED", "SGEMM_ERR_ARG", "PATH_AUTO", "PATH_FFMA",
+    "SGEMM_ERR_UNSUPPORTED", "SGEMM_ERR_ARG", "SGEMM_ERR_SCRATCH", "PATH_AUTO", "PATH_FFMA",
     "PATH_3XTF32", "PATH_TF32", "SgemmError", "library_path", "load",
     "sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
-    "sgemm_version", "gemm", "exported_symbols",
+    "sgemm_version", "sgemm_ffma_static_scratch", "gemm", "exported_symbols",
 ]
 
 SGEMM_OK = 0
@@ -27,6 +27,7 @@ SGEMM_ERR_TIMEOUT = 2
 SGEMM_ERR_NOMEM = 3
 SGEMM_ERR_UNSUPPORTED = 4
 SGEMM_ERR_ARG = 5
+SGEMM_ERR_SCRATCH = 6
 
 PATH_AUTO = 0
 PATH_FFMA = 1
@@ -72,6 +73,8 @@ def _declare(lib):
     lib.sgemm_release_workspace.restype = i32
     lib.sgemm_version.argtypes = []
     lib.sgemm_version.restype = i32
+    lib.sgemm_ffma_static_scratch.argtypes = gemm_args + [i32]
+    lib.sgemm_ffma_static_scratch.restype = i32
 
 
 def load():
@@ -93,7 +96,8 @@ def load():
 def exported_symbols(lib=None):
     """Names of the entry points this binding declares, for export checks."""
     return ["sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
-            "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version"]
+            "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
+            "sgemm_ffma_static_scratch"]
 
 
 def _b(t: str) -> bytes:
@@ -150,6 +154,15 @@ def sgemm_release_workspace() -> int:
 
 def sgemm_version() -> int:
     return load().sgemm_version()
+
+
+def sgemm_ffma_static_scratch(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              stream=None, split=0) -> int:
+    """The FFMA path with its split-K scratch in the library's static device
+    array: allocates nothing (for callers that may not allocate device
+    memory).  Overlapping calls on one device race on that array."""
+    return load().sgemm_ffma_static_scratch(_b(transA), _b(transB), M, N, K, alpha, A, lda, B,
+                                            ldb, beta, C, ldc, _stream(stream), split)
 
 
 def gemm(A, B, C, transA="N", transB="N", alpha=1.0, beta=0.0, path=PATH_AUTO, split=0,

@@ -210,6 +210,7 @@ extern "C" const char *sgemm_status_string(int status) {
     case SGEMM_ERR_NOMEM: return "workspace allocation failed";
     case SGEMM_ERR_UNSUPPORTED: return "path or device not supported for this problem";
     case SGEMM_ERR_ARG: return "invalid argument to an auxiliary entry point";
+    case SGEMM_ERR_SCRATCH: return "problem needs more than the static scratch array holds";
     default: return "unknown status";
     }
 }
@@ -242,3 +243,107 @@ extern "C" int sgemm_release_workspace(void) {
 }
 
 extern "C" int sgemm_version(void) { return 100; }
+
+// ------------------------------------------------------------------------
+// sgemm_ffma_static_scratch: the FFMA split-K launch with its partial sums in
+// a fixed-size static device array instead of the allocated workspace, for
+// callers that cannot allocate device memory (see include/sgemm_gb300.h).
+namespace sgemm_gb300 {
+
+constexpr int kStaticPartialTiles = 256;                       // 16 MiB
+constexpr size_t kStaticPartialFloats =
+    (size_t)kStaticPartialTiles * ffma::BM * ffma::BN;
+
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) float g_static_partials[kStaticPartialFloats];
+
+// Device address of g_static_partials per device, looked up once with that
+// device current.  (In host code the symbol's name is only a host-side
+// stand-in; passing it to a kernel would be wrong.)
+static std::mutex g_static_mu;
+static std::map<int, float *> g_static_addr;
+
+static int static_partials(float **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    auto it = g_static_addr.find(dev);
+    if (it == g_static_addr.end()) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_partials) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
+        it = g_static_addr.emplace(dev, static_cast<float *>(p)).first;
+    }
+    *out = it->second;
+    return SGEMM_OK;
+}
+
+}  // namespace sgemm_gb300
+
+extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, int64_t N,
+                                         int64_t K, float alpha, const float *A, int64_t lda,
+                                         const float *B, int64_t ldb, float beta, float *C,
+                                         int64_t ldc, sgemm_stream_t stream, int split) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (st != SGEMM_OK) return st;
+    if (split < 0) return SGEMM_ERR_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    DeviceState *d = nullptr;
+    st = device_state(&d);
+    if (st != SGEMM_OK) return st;
+    if (!(d->cc_major == 10 && d->cc_minor == 3)) return SGEMM_ERR_UNSUPPORTED;
+    if (K == 0 || alpha == 0.0f) {
+        if (beta == 1.0f) return SGEMM_OK;
+        ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc);
+        return launch_status();
+    }
+    Plan pl;
+    st = make_plan(transA, transB, M, N, K, lda, ldb, ldc, aligned16(A), aligned16(B),
+                   aligned16(C), SGEMM_PATH_FFMA, split, d->sms, &pl);
+    if (st != SGEMM_OK) return st;
+
+    ffma::Params p{};
+    p.A = A; p.B = B; p.C = C; p.partial = nullptr;
+    p.lda = lda; p.ldb = ldb; p.ldc = ldc;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.alpha = alpha; p.beta = beta;
+    p.tiles_m = (int)((M + ffma::BM - 1) / ffma::BM);
+    p.tiles_n = (int)((N + ffma::BN - 1) / ffma::BN);
+    p.group_m = pl.group_m;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int total_kt = (int)((K + ffma::BK - 1) / ffma::BK);
+    int sp = std::max(1, std::min(pl.split, total_kt));
+    const int kt_per = (total_kt + sp - 1) / sp;
+    sp = (total_kt + kt_per - 1) / kt_per;
+    p.dp_tiles = sp == 1 ? tiles : std::min(pl.dp_tiles, tiles);
+    p.split = sp;
+    p.kt_per_split = kt_per;
+    p.c_vec = pl.c_vector;
+    const int tail = tiles - p.dp_tiles;
+    if ((int64_t)tail * sp > kStaticPartialTiles) return SGEMM_ERR_SCRATCH;
+    if (tail > 0) {
+        st = static_partials(&p.partial);
+        if (st != SGEMM_OK) return st;
+    }
+    const int grid = p.dp_tiles + tail * sp;
+    const bool ak = is_notrans(transA), bk = !is_notrans(transB);
+    const bool v = pl.vector != 0;
+    if (ak && !bk && v) launch_ffma_t<true, false, true>(p, grid, s);
+    else if (ak && !bk && !v) launch_ffma_t<true, false, false>(p, grid, s);
+    else if (ak && bk && v) launch_ffma_t<true, true, true>(p, grid, s);
+    else if (ak && bk && !v) launch_ffma_t<true, true, false>(p, grid, s);
+    else if (!ak && !bk && v) launch_ffma_t<false, false, true>(p, grid, s);
+    else if (!ak && !bk && !v) launch_ffma_t<false, false, false>(p, grid, s);
+    else if (!ak && bk && v) launch_ffma_t<false, true, true>(p, grid, s);
+    else launch_ffma_t<false, true, false>(p, grid, s);
+    st = launch_status();
+    if (st != SGEMM_OK) return st;
+    if (tail > 0) {
+        ffma::splitk_reduce_kernel<<<tail, 256, 0, s>>>(p);
+        st = launch_status();
+    }
+    return st;
+}

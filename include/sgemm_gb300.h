@@ -60,7 +60,10 @@ typedef enum {
     SGEMM_ERR_NOMEM = 3,       /* the workspace could not be allocated        */
     SGEMM_ERR_UNSUPPORTED = 4, /* the forced path cannot run this problem or
                                   this device (e.g. not compute capability 10.3) */
-    SGEMM_ERR_ARG = 5          /* an argument of an auxiliary entry point     */
+    SGEMM_ERR_ARG = 5,         /* an argument of an auxiliary entry point     */
+    SGEMM_ERR_SCRATCH = 6      /* the problem needs more scratch than the
+                                  fixed-size static array of
+                                  sgemm_ffma_static_scratch holds            */
 } sgemm_status;
 
 /* Arithmetic path.  AUTO lets the per-shape selector choose among the
@@ -147,6 +150,40 @@ int sgemm_set_wait_limit(uint64_t nanoseconds);
 
 /* Free the current device's workspace (synchronises the device). */
 int sgemm_release_workspace(void);
+
+/*
+ * sgemm_ffma_static_scratch - the FFMA path (SGEMM_PATH_FFMA) for callers
+ * that cannot allocate device memory.  The paper has no counterpart: this
+ * entry point exists only for the library's users.
+ *
+ * Who needs it: code that runs where cudaMalloc/cudaMallocAsync must not be
+ * called - a host framework that owns the whole device memory pool and
+ * forbids allocations behind its back, or a latency-critical loop that may
+ * not take the allocator's locks or risk an allocation failure mid-run.
+ * sgemm and sgemm_ex may allocate their workspace on first use; this call
+ * never does: it calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Same arguments and result as sgemm_ex(..., SGEMM_PATH_FFMA, split), with
+ * `split` = 0 letting the selector choose.  The split-K partial sums go to a
+ * file-scope static __device__ array of 16 MiB (256 partial tiles of
+ * 128 x 128 floats) that every GPU which loads the library holds until the
+ * process exits.  A problem whose plan needs more partial tiles than that
+ * returns SGEMM_ERR_SCRATCH and launches nothing (force a smaller split, or
+ * split = 1, which needs no scratch).
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array:
+ * calls whose kernels overlap on the GPU (different streams, or different
+ * host threads without ordering) race on it and give undefined results.  The
+ * array keeps the last call's contents; nothing in it needs to start at
+ * zero, because every partial tile is written in full before it is read.
+ */
+int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                              float alpha, const float *A, int64_t lda,
+                              const float *B, int64_t ldb,
+                              float beta, float *C, int64_t ldc, sgemm_stream_t stream,
+                              int split);
 
 /* Library version, 100*major + minor. */
 int sgemm_version(void);
