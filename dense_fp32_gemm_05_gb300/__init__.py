@@ -18,7 +18,8 @@ __all__ = [
     "PATH_3XTF32", "PATH_TF32", "SgemmError", "library_path", "load",
     "sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
-    "sgemm_version", "sgemm_ffma_static_scratch", "gemm", "exported_symbols",
+    "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
+    "sgemm_timing_read", "gemm", "exported_symbols",
 ]
 
 SGEMM_OK = 0
@@ -73,6 +74,10 @@ def _declare(lib):
     lib.sgemm_release_workspace.restype = i32
     lib.sgemm_version.argtypes = []
     lib.sgemm_version.restype = i32
+    lib.sgemm_timing_enable.argtypes = [i32]
+    lib.sgemm_timing_enable.restype = i32
+    lib.sgemm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i32]
+    lib.sgemm_timing_read.restype = i32
     lib.sgemm_ffma_static_scratch.argtypes = gemm_args + [i32]
     lib.sgemm_ffma_static_scratch.restype = i32
 
@@ -97,7 +102,7 @@ def exported_symbols(lib=None):
     """Names of the entry points this binding declares, for export checks."""
     return ["sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
             "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
-            "sgemm_ffma_static_scratch"]
+            "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read"]
 
 
 def _b(t: str) -> bytes:
@@ -154,6 +159,20 @@ def sgemm_release_workspace() -> int:
 
 def sgemm_version() -> int:
     return load().sgemm_version()
+
+
+def sgemm_timing_enable(n: int) -> int:
+    """Record event pairs around the main kernel of the next n launches."""
+    return load().sgemm_timing_enable(n)
+
+
+def sgemm_timing_read(capacity: int = 4096):
+    """Durations (ms) of the recorded main-kernel launches, oldest first."""
+    buf = (ctypes.c_float * max(capacity, 1))()
+    n = load().sgemm_timing_read(buf, capacity)
+    if n < 0:
+        raise SgemmError(-n, "sgemm_timing_read")
+    return [float(buf[i]) for i in range(n)]
 
 
 def sgemm_ffma_static_scratch(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,

@@ -48,6 +48,7 @@ struct Plan {
     int vector = 1;     // 16-byte operand loads (else 4-byte edge path)
     int c_vector = 1;   // 16-byte C accesses
     int group_m = 8;    // rasterisation group height (tiles)
+    int tail_nsplit = 1;  // tensor cores: column slices of the last-wave tiles
 };
 
 // Cost model of the FFMA path in units of one k-tile step of one CTA
@@ -71,7 +72,17 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
                      int split, int sms, Plan *out) {
     (void)ta; (void)tb;
     Plan pl;
-    pl.path = (path == SGEMM_PATH_AUTO) ? SGEMM_PATH_FFMA : path;
+    if (path == SGEMM_PATH_AUTO) {
+        // 3xTF32 runs the tensor cores at 3 MMAs per product and beats the
+        // CUDA-core path by 1.5x (1024^3) to 5x (8192^3) on GB300, but it
+        // carries a split pre-pass and a launch more: small problems stay on
+        // FFMA, and so does K < 32, where the dropped split terms are not
+        // small against the fp32 bound 4*K*2^-24.
+        const bool big = (double)M * (double)N * (double)K >= (double)(1 << 27);
+        pl.path = (big && K >= 32) ? SGEMM_PATH_3XTF32 : SGEMM_PATH_FFMA;
+    } else {
+        pl.path = path;
+    }
     pl.vector = (a_al && lda % 4 == 0 && b_al && ldb % 4 == 0) ? 1 : 0;
     pl.c_vector = (c_al && ldc % 4 == 0) ? 1 : 0;
     if (pl.path == SGEMM_PATH_FFMA) {
@@ -103,11 +114,31 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         }
         if (pl.split == 1) pl.dp_tiles = (int)tiles;
     } else {
-        // tensor-core path: 128-row tiles, N of the MMA from the problem's N
+        // tensor-core path: 128-row tiles, N of the MMA from the problem's N,
+        // one CTA per SM.  Tiles after the last full wave may run as 2 or 4
+        // narrower CTAs (MMA N = tile_n / slices, at least 64) so the last
+        // wave is short; a narrower tile is charged ~5 % per halving for its
+        // higher shared-memory traffic per flop.
         pl.tile_m = 128;
         pl.tile_n = N > 128 ? 256 : (N > 64 ? 128 : 64);
         pl.split = 1;
-        pl.dp_tiles = (int)(((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n));
+        const int64_t tiles = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
+        const int64_t slots = sms;
+        const int64_t full = (tiles / slots) * slots;
+        const int64_t tail = tiles - full;
+        double best = (double)((tiles + slots - 1) / slots);
+        pl.dp_tiles = (int)tiles;
+        pl.tail_nsplit = 1;
+        for (int ns = 2; ns <= 4 && pl.tile_n / ns >= 64; ns *= 2) {
+            if (tail == 0) break;
+            const double waves = (double)((tail * ns + slots - 1) / slots);
+            const double c = (double)(full / slots) + waves / ns * (ns == 2 ? 1.05 : 1.10);
+            if (c < best * 0.97) {
+                best = c;
+                pl.dp_tiles = (int)full;
+                pl.tail_nsplit = ns;
+            }
+        }
     }
     *out = pl;
     return 0;

@@ -9,6 +9,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/sgemm_gb300.h"
 #include "ffma_kernel.cuh"
@@ -67,6 +68,34 @@ int workspace(cudaStream_t stream, size_t bytes, void **out) {
     return SGEMM_OK;
 }
 
+// ------------------------------------------------------------ timing hook
+// A ring of event pairs recorded around main-kernel launches (see
+// sgemm_timing_enable in the header).  Guarded by g_mu.
+struct TimingRing {
+    int dev = -1;
+    std::vector<cudaEvent_t> ev;   // 2 per slot
+    int slots = 0, next = 0, count = 0;
+    bool open = false;             // a begin without its end yet
+};
+static TimingRing g_timing;
+
+void timing_mark(cudaStream_t s, bool begin) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    TimingRing &t = g_timing;
+    if (t.slots == 0) return;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != t.dev) return;
+    if (begin) {
+        cudaEventRecord(t.ev[2 * t.next], s);
+        t.open = true;
+    } else if (t.open) {
+        cudaEventRecord(t.ev[2 * t.next + 1], s);
+        t.open = false;
+        t.next = (t.next + 1) % t.slots;
+        t.count = std::min(t.count + 1, t.slots);
+    }
+}
+
 static int launch_status() {
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) return SGEMM_OK;
@@ -117,6 +146,7 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
     const int grid = p.dp_tiles + tail * split;
     const bool ak = is_notrans(ta), bk = !is_notrans(tb);
     const bool v = pl.vector != 0;
+    timing_mark(s, true);
     if (ak && !bk && v) launch_ffma_t<true, false, true>(p, grid, s);
     else if (ak && !bk && !v) launch_ffma_t<true, false, false>(p, grid, s);
     else if (ak && bk && v) launch_ffma_t<true, true, true>(p, grid, s);
@@ -125,6 +155,7 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
     else if (!ak && !bk && !v) launch_ffma_t<false, false, false>(p, grid, s);
     else if (!ak && bk && v) launch_ffma_t<false, true, true>(p, grid, s);
     else launch_ffma_t<false, true, false>(p, grid, s);
+    timing_mark(s, false);
     int st = launch_status();
     if (st != SGEMM_OK) return st;
     if (tail > 0) {
@@ -224,6 +255,45 @@ extern "C" int sgemm_device_error(sgemm_stream_t stream) {
 extern "C" int sgemm_set_wait_limit(uint64_t nanoseconds) {
     tc_set_wait_limit(nanoseconds);
     return SGEMM_OK;
+}
+
+extern "C" int sgemm_timing_enable(int n) {
+    if (n < 0 || n > 100000) return -1;
+    int dev = 0;
+    if (n > 0 && cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    TimingRing &t = g_timing;
+    for (cudaEvent_t e : t.ev) cudaEventDestroy(e);
+    t = TimingRing{};
+    if (n == 0) return SGEMM_OK;
+    t.ev.resize(2 * (size_t)n, nullptr);
+    for (auto &e : t.ev) {
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            for (cudaEvent_t x : t.ev) if (x) cudaEventDestroy(x);
+            t = TimingRing{};
+            return SGEMM_ERR_CUDA;
+        }
+    }
+    t.dev = dev;
+    t.slots = n;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_timing_read(float *ms, int capacity) {
+    if (ms == nullptr && capacity > 0) return -1;
+    if (capacity < 0) return -2;
+    std::lock_guard<std::mutex> lk(g_mu);
+    TimingRing &t = g_timing;
+    const int n = std::min(t.count, capacity);
+    const int first = (t.next - t.count + t.slots) % std::max(t.slots, 1);
+    for (int i = 0; i < n; ++i) {
+        const int slot = (first + i) % t.slots;
+        if (cudaEventSynchronize(t.ev[2 * slot + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&ms[i], t.ev[2 * slot], t.ev[2 * slot + 1]) != cudaSuccess)
+            return -SGEMM_ERR_CUDA;
+    }
+    t.count = 0;
+    return n;
 }
 
 extern "C" int sgemm_release_workspace(void) {

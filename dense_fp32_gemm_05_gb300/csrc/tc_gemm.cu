@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -42,8 +43,15 @@ namespace sgemm_gb300 {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BK = 32;                 // fp32 per k-block = 128 bytes
+// k-block width in fp32: 3xTF32 uses 16 (64-byte rows, 64-byte swizzle: six
+// MMAs per block and twice the stages); single-pass TF32 uses 32 (128-byte
+// rows and swizzle: four MMAs per block, so the per-block barrier round trip
+// of the MMA thread stays small against the tensor work).
+template <bool THREE> struct KBlock { static constexpr int BK = THREE ? 16 : 32; };
+constexpr int KPAD = 32;               // K padding of the split operands
 constexpr int THREADS = 192;
+constexpr int EPI_LD = 33;             // padded row of the epilogue staging tile
+constexpr int SMEM_LIMIT = 232448;     // opt-in dynamic shared memory per block
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
 // Limit of the teardown waits (copies and MMAs already issued must retire
 // before the CTA frees TMEM and exits); independent of the test hook so that
@@ -54,27 +62,35 @@ __device__ unsigned int g_error;        // sticky device error word (per device)
 
 template <int BN, bool THREE>
 struct Cfg {
+    static constexpr int BK = KBlock<THREE>::BK;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int PARTS = THREE ? 2 : 1;
     static constexpr int STAGE_BYTES = PARTS * (A_BYTES + B_BYTES);
-    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;   // one 32 x 33 tile per epilogue warp
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int FIXED = EPI_BYTES + BAR_BYTES + 1024;
+    static constexpr int STAGES_RAW = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
     static constexpr uint32_t TMEM_COLS = BN;            // power of two >= 32
     static_assert(STAGES >= 2, "need at least two stages");
     static_assert(BN == 64 || BN == 128 || BN == 256, "N of the MMA");
 };
 
+// Work decomposition: tiles (BM x BN) in grouped raster order.  The first
+// dp_tiles run as whole tiles; each later tile (the last, partly filled
+// wave) runs as tail_nsplit CTAs of BN / tail_nsplit columns each, so the
+// last wave finishes in a fraction of a tile's time.
 struct Params {
     float *C;
     int64_t ldc;
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n, group_m;
-    int num_kb;                 // k-blocks of 32
-    int c_vec;                  // C 16-byte aligned, ldc % 4 == 0
+    int dp_tiles;               // tiles computed at full width
+    int tail_nsplit;            // 1, 2 or 4 column slices for the rest
+    int num_kb;                 // k-blocks of BK
     unsigned long long wait_ns; // bounded-wait limit
 };
 
@@ -131,24 +147,27 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), descriptor
-// version 1, base offset 0 (every tile is 1024-byte aligned).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+// Shared-memory matrix descriptor of a K-major operand whose rows are
+// ROW_BYTES (64 or 128) long and swizzled over that span: 8-row atoms
+// 8*ROW_BYTES apart (stride byte offset), descriptor version 1, base offset 0
+// (every tile is 1024-byte aligned; each +32-byte step to the next K = 8 slice
+// stays inside the row).  Swizzle codes: 4 = 64-byte, 2 = 128-byte.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "swizzle span");
     uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
-    d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
-    d |= (uint64_t)1 << 46;                           // version
-    d |= (uint64_t)2 << 61;                           // swizzle: 128B
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);            // start address
+    d |= (uint64_t)1 << 16;                             // leading byte offset (unused here)
+    d |= (uint64_t)((8 * ROW_BYTES) >> 4) << 32;        // stride byte offset
+    d |= (uint64_t)1 << 46;                             // version
+    d |= (uint64_t)(ROW_BYTES == 64 ? 4 : 2) << 61;     // swizzle mode
     return d;
 }
 
 // Instruction descriptor of kind::tf32: D fp32, A and B tf32, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
-template <int BN>
-__device__ __forceinline__ constexpr uint32_t idesc_tf32() {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+__device__ __forceinline__ uint32_t idesc_tf32(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(BM >> 4) << 24);
 }
 
@@ -198,12 +217,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi,
                    const __grid_constant__ CUtensorMap tm_alo,
                    const __grid_constant__ CUtensorMap tm_bhi,
-                   const __grid_constant__ CUtensorMap tm_blo, const Params p) {
+                   const __grid_constant__ CUtensorMap tm_blo,
+                   const __grid_constant__ CUtensorMap tm_bhi_tail,
+                   const __grid_constant__ CUtensorMap tm_blo_tail, const Params p) {
     using K_ = Cfg<BN, THREE>;
+    constexpr int BK = K_::BK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_::STAGES * K_::STAGE_BYTES);
+    float *epi = reinterpret_cast<float *>(smem + K_::STAGES * K_::STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_::STAGES * K_::STAGE_BYTES +
+                                                  K_::EPI_BYTES);
     // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * K_::STAGES + 1);
     const uint32_t smem0 = smem_u32(smem);
@@ -219,6 +243,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // ---- this CTA's unit of work
+    int tile, sub = 0, nsub = 1;
+    if ((int)blockIdx.x < p.dp_tiles) {
+        tile = blockIdx.x;
+    } else {
+        const int u = blockIdx.x - p.dp_tiles;
+        nsub = p.tail_nsplit;
+        tile = p.dp_tiles + u / nsub;
+        sub = u % nsub;
+    }
+    int tm, tn;
+    raster(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int bn = BN / nsub;                          // columns of this unit
+    const int m0 = tm * BM, n0 = tn * BN + sub * bn;
+    const CUtensorMap *mb_hi = nsub == 1 ? &tm_bhi : &tm_bhi_tail;
+    const CUtensorMap *mb_lo = nsub == 1 ? &tm_blo : &tm_blo_tail;
+    const uint32_t stage_tx = (uint32_t)(K_::PARTS * (K_::A_BYTES + bn * BK * 4));
+
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < K_::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -227,10 +269,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(acc_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tm_ahi);
-        prefetch_map(&tm_bhi);
+        prefetch_map(mb_hi);
         if (THREE) {
             prefetch_map(&tm_alo);
-            prefetch_map(&tm_blo);
+            prefetch_map(mb_lo);
         }
     }
     if (warp == 1) {
@@ -243,9 +285,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    int tm, tn;
-    raster(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
     const int nkb = p.num_kb;
     const uint64_t lim = p.wait_ns;
 
@@ -259,13 +298,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int s = kb % K_::STAGES;
                 const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) break;
-                mbar_expect_tx(full_bar(s), K_::STAGE_BYTES);
+                mbar_expect_tx(full_bar(s), stage_tx);
                 const int kc = kb * BK;
                 tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, m0);
-                tma_load_2d(b_hi(s), &tm_bhi, full_bar(s), kc, n0);
+                tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, n0);
                 if (THREE) {
                     tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
-                    tma_load_2d(b_lo(s), &tm_blo, full_bar(s), kc, n0);
+                    tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, n0);
                 }
                 ++issued;
             }
@@ -277,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_tf32<BN>();
+            const uint32_t idesc = idesc_tf32(bn);
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % K_::STAGES;
                 const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
@@ -286,12 +325,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 8; ++kk) {
                     const uint32_t off = kk * 32;            // 8 tf32 = 32 bytes
-                    const uint64_t ah = smem_desc_sw128(a_hi(s) + off);
-                    const uint64_t bh = smem_desc_sw128(b_hi(s) + off);
+                    const uint64_t ah = smem_desc<BK * 4>(a_hi(s) + off);
+                    const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
                     const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
                     if (THREE) {
-                        const uint64_t al = smem_desc_sw128(a_lo(s) + off);
-                        const uint64_t bl = smem_desc_sw128(b_lo(s) + off);
+                        const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
+                        const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
                         umma_tf32(tmem, al, bh, idesc, first);
                         umma_tf32(tmem, ah, bl, idesc, 1u);
                         umma_tf32(tmem, ah, bh, idesc, 1u);
@@ -308,48 +347,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
-        const int q = warp & 3;                       // TMEM lane quarter
+        // Warp w owns TMEM lanes (= tile rows) 32*(w%4) .. +31.  Each 32 x 32
+        // block is read with tcgen05.ld (lane = row), turned around through a
+        // padded shared tile, then written row by row: every store
+        // instruction of the warp covers 32 consecutive columns of one row.
+        const int q = warp & 3;
+        float *stg = epi + q * 32 * EPI_LD;
         const bool ready = mbar_wait(acc_bar, 0u, lim);
         tc_fence_after();
         if (ready) {
-            const int row = m0 + q * 32 + lane;
             const float alpha = p.alpha, beta = p.beta;
+            const int rows_here = min(32, p.M - (m0 + q * 32));
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < bn / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-                const int col0 = n0 + c * 32;
-                if (row < p.M && col0 < p.N) {
-                    float *dst = p.C + (int64_t)row * p.ldc + col0;
-                    if (p.c_vec && col0 + 31 < p.N) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 o;
-                            const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
-                            const float v2 = __uint_as_float(r[j + 2]), v3 = __uint_as_float(r[j + 3]);
-                            if (beta == 0.0f) {
-                                o = make_float4(__fmul_rn(alpha, v0), __fmul_rn(alpha, v1),
-                                                __fmul_rn(alpha, v2), __fmul_rn(alpha, v3));
-                            } else {
-                                const float4 ci = *reinterpret_cast<const float4 *>(dst + j);
-                                o = make_float4(__fmaf_rn(alpha, v0, __fmul_rn(beta, ci.x)),
-                                                __fmaf_rn(alpha, v1, __fmul_rn(beta, ci.y)),
-                                                __fmaf_rn(alpha, v2, __fmul_rn(beta, ci.z)),
-                                                __fmaf_rn(alpha, v3, __fmul_rn(beta, ci.w)));
-                            }
-                            *reinterpret_cast<float4 *>(dst + j) = o;
-                        }
+                for (int j = 0; j < 32; ++j) stg[lane * EPI_LD + j] = __uint_as_float(r[j]);
+                __syncwarp();
+                const int col = n0 + c * 32 + lane;
+                if (col < p.N) {
+                    float *__restrict__ dst = p.C + (int64_t)(m0 + q * 32) * p.ldc + col;
+                    if (beta == 0.0f) {
+#pragma unroll 8
+                        for (int rr = 0; rr < rows_here; ++rr)
+                            dst[(int64_t)rr * p.ldc] = __fmul_rn(alpha, stg[rr * EPI_LD + lane]);
                     } else {
+                        // issue all 32 loads of C before the first store
+                        float cin[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < p.N) {
-                                const float v = __uint_as_float(r[j]);
-                                dst[j] = (beta == 0.0f) ? __fmul_rn(alpha, v)
-                                                        : __fmaf_rn(alpha, v, __fmul_rn(beta, dst[j]));
-                            }
-                        }
+                        for (int rr = 0; rr < 32; ++rr)
+                            cin[rr] = rr < rows_here ? dst[(int64_t)rr * p.ldc] : 0.0f;
+#pragma unroll
+                        for (int rr = 0; rr < 32; ++rr)
+                            if (rr < rows_here)
+                                dst[(int64_t)rr * p.ldc] =
+                                    __fmaf_rn(alpha, stg[rr * EPI_LD + lane], __fmul_rn(beta, cin[rr]));
                     }
                 }
+                __syncwarp();
             }
         }
     }
@@ -426,17 +462,18 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D map over a [rows][Kp] fp32 array: box 32 (k) x box_rows, 128-byte swizzle,
-// rows past `rows` read as zeros.
-static bool make_map(CUtensorMap *m, const float *base, int rows, int Kp, int box_rows) {
+// 2-D map over a [rows][Kp] fp32 array: box bk (k) x box_rows, swizzled over
+// the bk*4-byte row (64 or 128 bytes); rows past `rows` read as zeros.
+static bool make_map(CUtensorMap *m, const float *base, int rows, int Kp, int box_rows, int bk) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)Kp * sizeof(float)};
-    cuuint32_t box[2] = {(cuuint32_t)tc::BK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               bk == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -488,8 +525,12 @@ static int launch_main(const CUtensorMap *maps, const tc::Params &p, cudaStream_
             return last_status();
         __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
     }
-    tc::tc_gemm_kernel<BN, THREE><<<p.tiles_m * p.tiles_n, tc::THREADS, K_::SMEM, s>>>(
-        maps[0], maps[1], maps[2], maps[3], p);
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int grid = p.dp_tiles + (tiles - p.dp_tiles) * p.tail_nsplit;
+    timing_mark(s, true);
+    tc::tc_gemm_kernel<BN, THREE><<<grid, tc::THREADS, K_::SMEM, s>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    timing_mark(s, false);
     return last_status();
 }
 
@@ -499,7 +540,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     (void)sms;
     const bool three = pl.path == SGEMM_PATH_3XTF32;
     const int BN = pl.tile_n;
-    const int Kp = (int)((K + tc::BK - 1) / tc::BK) * tc::BK;
+    const int Kp = (int)((K + tc::KPAD - 1) / tc::KPAD) * tc::KPAD;
     auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
     const size_t a_elems = up((size_t)M * Kp * 4) / 4;
     const size_t b_elems = up((size_t)N * Kp * 4) / 4;
@@ -525,9 +566,14 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     st = last_status();
     if (st != SGEMM_OK) return st;
 
-    CUtensorMap maps[4];
-    if (!make_map(&maps[0], a_hi, (int)M, Kp, tc::BM) || !make_map(&maps[1], a_lo, (int)M, Kp, tc::BM) ||
-        !make_map(&maps[2], b_hi, (int)N, Kp, BN) || !make_map(&maps[3], b_lo, (int)N, Kp, BN))
+    const int nsplit = std::max(1, pl.tail_nsplit);
+    const int bk = three ? tc::KBlock<true>::BK : tc::KBlock<false>::BK;
+    CUtensorMap maps[6];
+    if (!make_map(&maps[0], a_hi, (int)M, Kp, tc::BM, bk) ||
+        !make_map(&maps[1], a_lo, (int)M, Kp, tc::BM, bk) ||
+        !make_map(&maps[2], b_hi, (int)N, Kp, BN, bk) || !make_map(&maps[3], b_lo, (int)N, Kp, BN, bk) ||
+        !make_map(&maps[4], b_hi, (int)N, Kp, BN / nsplit, bk) ||
+        !make_map(&maps[5], b_lo, (int)N, Kp, BN / nsplit, bk))
         return SGEMM_ERR_UNSUPPORTED;
 
     tc::Params p{};
@@ -536,8 +582,9 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.tiles_m = (int)((M + tc::BM - 1) / tc::BM);
     p.tiles_n = (int)((N + BN - 1) / BN);
     p.group_m = 16;
-    p.num_kb = Kp / tc::BK;
-    p.c_vec = pl.c_vector;
+    p.dp_tiles = std::min(pl.dp_tiles, p.tiles_m * p.tiles_n);
+    p.tail_nsplit = nsplit;
+    p.num_kb = Kp / bk;
     {
         std::lock_guard<std::mutex> lk(g_tc_mu);
         p.wait_ns = g_wait_ns;

@@ -20,6 +20,10 @@ int tc_take_device_error();
 // Sets the bounded-wait limit (ns; 0 = default).
 void tc_set_wait_limit(uint64_t ns);
 
+// Measurement hook: records an event before (begin = true) or after the main
+// kernel launch on `s` when timing is enabled (no-op otherwise).
+void timing_mark(cudaStream_t s, bool begin);
+
 // Library-owned per-(device, stream) workspace, grown on demand.
 int workspace(cudaStream_t stream, size_t bytes, void **out);
 

@@ -148,6 +148,20 @@ int sgemm_device_error(sgemm_stream_t stream);
  */
 int sgemm_set_wait_limit(uint64_t nanoseconds);
 
+/*
+ * Measurement hook.  sgemm_timing_enable(n), n > 0, makes the library record
+ * a CUDA event pair around the main GEMM kernel (the FFMA or tensor-core
+ * kernel, not the split pre-pass or the split-K reduction) of each of its
+ * next n launches on the current device, on the caller's stream; n = 0 turns
+ * recording off.  sgemm_timing_read(ms, capacity) waits for the recorded
+ * launches, writes their durations in milliseconds (oldest first, at most
+ * capacity) and clears the record; it returns the count written or a
+ * negative argument index / sgemm_status (as a negative number) on error.
+ * Recording costs two event records per call; it is off by default.
+ */
+int sgemm_timing_enable(int n);
+int sgemm_timing_read(float *ms, int capacity);
+
 /* Free the current device's workspace (synchronises the device). */
 int sgemm_release_workspace(void);
 

@@ -94,23 +94,45 @@ def test_aux_argument_errors(lib):
 
 
 def test_plan_vector_and_edge_path(lib):
-    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096)
-    assert st == 0 and p["vector"] == 1 and p["path"] == sg.PATH_FFMA
+    F = sg.PATH_FFMA
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, path=F)
+    assert st == 0 and p["vector"] == 1 and p["path"] == F
     assert (p["tile_m"], p["tile_n"]) == (128, 128)
     # odd leading dimensions: 16-byte loads are illegal, the 4-byte path runs
-    st, p = sg.sgemm_plan("N", "T", 4095, 3073, 1537, 1537, 1537, 3073)
+    st, p = sg.sgemm_plan("N", "T", 4095, 3073, 1537, 1537, 1537, 3073, path=F)
     assert st == 0 and p["vector"] == 0
     # misaligned base pointer
-    st, p = sg.sgemm_plan("N", "N", 512, 512, 512, 512, 512, 512, a_aligned=False)
+    st, p = sg.sgemm_plan("N", "N", 512, 512, 512, 512, 512, 512, a_aligned=False, path=F)
     assert st == 0 and p["vector"] == 0
+
+
+def test_plan_auto_path_choice(lib):
+    # large problems go to the tensor cores (3xTF32), with N-sized MMA tiles
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096)
+    assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["tile_n"] == 256
+    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64)
+    assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["tile_n"] == 64
+    # odd leading dimensions do not matter to the tensor-core path (pre-pass)
+    st, p = sg.sgemm_plan("T", "T", 4095, 3073, 1537, 4095, 1537, 3073)
+    assert st == 0 and p["path"] == sg.PATH_3XTF32
+    # small problems and short K stay on the CUDA cores
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256)
+    assert st == 0 and p["path"] == sg.PATH_FFMA
+    st, p = sg.sgemm_plan("N", "N", 8192, 8192, 16, 16, 8192, 8192)
+    assert st == 0 and p["path"] == sg.PATH_FFMA
+    # TF32 is never chosen automatically
+    for shp in [(4096, 4096, 4096), (1024, 1024, 1024), (300, 300, 40)]:
+        st, p = sg.sgemm_plan("N", "N", *shp, shp[2], shp[1], shp[1])
+        assert p["path"] != sg.PATH_TF32
 
 
 def test_plan_split_k_for_small_grids(lib):
     # 256^3: 4 tiles for 304 CTA slots -> the K loop is split
     st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152)
     assert st == 0 and p["split"] > 1
-    # 16384 x 64 x 8192 skinny: 128 tiles, long K -> split
-    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152)
+    # 16384 x 64 x 8192 skinny on the FFMA path: 128 tiles, long K -> split
+    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152,
+                          path=sg.PATH_FFMA)
     assert st == 0 and p["split"] > 1
     # forced split is honoured, forced 1 disables it
     st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=1)
