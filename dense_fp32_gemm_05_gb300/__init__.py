@@ -62,7 +62,7 @@ def _declare(lib):
     lib.sgemm_ex.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
     lib.sgemm_plan.argtypes = [c, c, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, i32, i32,
-                               ip, ip, ip, ip, ip]
+                               ip, ip, ip, ip, ip, ip]
     lib.sgemm_plan.restype = i32
     lib.sgemm_status_string.argtypes = [i32]
     lib.sgemm_status_string.restype = ctypes.c_char_p
@@ -133,11 +133,11 @@ def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, strea
 def sgemm_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned=True, b_aligned=True,
                c_aligned=True, path=PATH_AUTO, split=0, num_sms=152):
     """The selector's decision, without a GPU: (status, dict)."""
-    outs = [ctypes.c_int(0) for _ in range(5)]
+    outs = [ctypes.c_int(0) for _ in range(6)]
     st = load().sgemm_plan(_b(transA), _b(transB), M, N, K, lda, ldb, ldc, int(a_aligned),
                            int(b_aligned), int(c_aligned), path, split, num_sms,
                            *[ctypes.byref(o) for o in outs])
-    keys = ("path", "split", "tile_m", "tile_n", "vector")
+    keys = ("path", "split", "tile_m", "tile_n", "vector", "ctas")
     return st, {k: o.value for k, o in zip(keys, outs)}
 
 

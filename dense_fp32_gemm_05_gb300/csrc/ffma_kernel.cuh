@@ -2,20 +2,24 @@
 //
 // Structure (the nest of tiles of "Matmul II: register blocking, warp tiling,
 // tensor cores", sections 1-5, re-derived for this GPU):
-//   * block tile 128 x 128 of C per CTA, 256 threads, k-tiles of BK = 16;
-//   * warp tile 32 (rows) x 64 (cols): 8 warps as 4 x 2, square enough that
-//     a warp's shared-memory reads per k are its perimeter, not its area
-//     (section 5, "v7: warp tiling");
-//   * thread tile 8 x 8 as a 2 x 2 grid of 4 x 4 blocks (rows tr*4 + {0..3}
-//     and 16 + tr*4 + {0..3}, columns tc*4 + {0..3} and 32 + tc*4 + {0..3}),
-//     so that one k-step is four 16-byte shared loads feeding 64 FMAs
-//     (section 4, "v6: wider loads and a transposed tile"), issued as 32
-//     packed fma.rn.f32x2 (two independent round-to-nearest FMAs each);
-//   * both operand tiles sit in shared memory k-major ([k][m] and [k][n]), so
-//     an operand whose rows run along K in global memory (A with 'N', B with
-//     'T') is transposed on the way in through registers, and one whose rows
-//     run along M or N is copied with cp.async as-is ("CuTe-ly writing an
-//     SM86 SGEMM", section "host-side setup": 16-byte cp.async.cg);
+//   * block tile 128 x 128 of C per CTA, 128 threads, k-tiles of BK = 16;
+//   * warp tile 64 x 64: 4 warps as 2 x 2, a square warp tile so that a
+//     warp's shared-memory reads per k are its perimeter, not its area
+//     (section 5, "v7: warp tiling", whose 64 x 64 warp tile this is);
+//   * thread tile 8 x 16: a lane owns rows am + {0..3}, am + 32 + {0..3} and
+//     columns bn + 16 g + {0..3}, g = 0..3.  One k-step is 6 sixteen-byte
+//     shared loads (2 of A, 4 of B) feeding 128 FMAs, issued as 64 packed
+//     fma.rn.f32x2 (two independent round-to-nearest FMAs each).  The 8 x 16
+//     tile is what keeps shared-memory delivery (128 bytes per clock per SM)
+//     below the FMA rate: 24 loaded floats per 128 FMAs instead of the 16 per
+//     64 of an 8 x 8 tile (section 4 counts the same ratio at one level less);
+//   * both operand tiles sit in shared memory k-major ([k][m] and [k][n]).
+//     An operand whose rows run along K in global memory (A with 'N', B with
+//     'T') is loaded as float4 along K into registers and stored transposed
+//     (section 4, "transposed tile"), in two halves per k-tile so that only
+//     8 staging registers are live; one whose rows run along M or N is copied
+//     with cp.async as-is ("CuTe-ly writing an SM86 SGEMM", section
+//     "host-side setup": 16-byte cp.async.cg);
 //   * an XOR swizzle of each shared row (bits 3-4 of the column flipped by
 //     bits 2-3 of k) keeps the transposing stores and the 16-byte loads free
 //     of bank conflicts ("CuTe-ly writing an SM86 SGEMM", section "swizzles &
@@ -23,15 +27,30 @@
 //   * two shared-memory stages: the copy of k-tile t+1 is in flight while
 //     k-tile t is multiplied ("Matmul II", section 7, t3's double buffer);
 //   * fused alpha/beta epilogue with 16-byte stores where C allows.
+//
+// Work decomposition (data-parallel tiles + "stream-K" remainder): tiles are
+// numbered in grouped raster order.  The first dp_tiles are computed whole,
+// one CTA each, wave after wave (neighbouring CTAs share A and B panels in
+// L2).  The k-tile iterations of the remaining tiles are cut into sk_ctas
+// contiguous, equal shares, one per further CTA: a share that covers a whole
+// tile writes C; a share that starts or ends inside a tile leaves a partial
+// sum in the workspace, and sk_fixup_kernel adds a shared tile's partials in
+// ascending k order (deterministic) and writes C.  So the last, partly
+// filled wave of whole tiles becomes one short wave that keeps every SM busy,
+// and a grid with fewer tiles than CTA slots is spread over all of them;
+// with dp_tiles = 0 and sk_ctas = s * tiles every tile is cut into s
+// contiguous K slices (split-K, "Matmul II", section 8).
+//
 // Every output is summed in ascending k with one fused multiply-add per
 // term, starting from +0; a k-tile past K is zero-filled and adds exactly 0.
-// So with one K slice the result equals, bit for bit, the naive loop
+// So a tile computed whole equals, bit for bit, the naive loop
 // acc = fmaf(a, b, acc) followed by alpha*acc or fmaf(alpha, acc, beta*c)
 // ("How to get a matmul kernel into the top percentile (worklog)",
 // "Optimization 1": same ascending order, identical fp32 result).
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "ptx_util.cuh"
@@ -42,35 +61,46 @@ namespace ffma {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 16;
-constexpr int THREADS = 256;
+constexpr int THREADS = 128;
+constexpr int CHUNKS = (BM * BK / 4) / THREADS;    // float4 chunks per thread per operand tile
 
-// Work decomposition: tiles are numbered in rasterised order.  The first
-// dp_tiles tiles are computed whole by one CTA each (blockIdx.x < dp_tiles);
-// every later tile is cut into `split` contiguous K slices, one CTA each,
-// whose raw partial sums go to a 128 x 128 block of `partial` and are added
-// by splitk_reduce_kernel in ascending slice order.  This evens out the last,
-// partly filled wave of CTAs and fills the GPU for problems with few tiles
-// ("Matmul II", section 8: split-K when M*N is too small to fill the SMs).
 struct Params {
     const float *A;
     const float *B;
     float *C;
-    float *partial;        // [(tile - dp_tiles) * split + slice][BM * BN]
+    float *partial;        // [2 * sk_ctas][BM * BN]: slot 2c = share c's first tile, 2c+1 its last
     int64_t lda, ldb, ldc;
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n;
     int group_m;           // CTA rasterisation: tile rows per group
-    int dp_tiles;          // tiles computed whole
-    int split;             // K slices of each remaining tile
-    int kt_per_split;      // BK-tiles per K slice
+    int kt;                // k-tiles per tile, ceil(K / BK)
+    int dp_tiles;          // tiles computed whole (CTAs 0 .. dp_tiles-1)
+    int sk_ctas;           // CTAs sharing the remaining tiles' iterations
+    int64_t sk_iters;      // (tiles - dp_tiles) * kt, counted from tile dp_tiles
     int c_vec;             // C base 16-byte aligned and ldc % 4 == 0
 };
 
+// First remaining-tile iteration of share c.
+__host__ __device__ __forceinline__ int64_t share_begin(int64_t iters, int ctas, int c) {
+    return iters * c / ctas;
+}
+
+// The share containing remaining-tile iteration x (largest c with begin <= x).
+__host__ __device__ __forceinline__ int share_owner(int64_t iters, int ctas, int64_t x) {
+    return (int)(((x + 1) * ctas - 1) / iters);
+}
+
+// Workspace slot of share c's partial sum of remaining tile u: its first tile or its last.
+__host__ __device__ __forceinline__ int partial_slot(const Params &p, int c, int u) {
+    return (share_begin(p.sk_iters, p.sk_ctas, c) / p.kt == u) ? 2 * c : 2 * c + 1;
+}
+
 // Tile index -> (tile row, tile column), grouped rasterisation: consecutive
 // tiles walk down a group of group_m tile rows before moving one tile column
-// right, so co-resident CTAs share the group's A panels and a few B panels in
-// L2 ("Optimising fp32 GEMM on A100", "Kernel 5 (grid swizzling)").
+// right, so CTAs working on neighbouring tiles share the group's A panels and
+// a few B panels in L2 ("Optimising fp32 GEMM on A100", "Kernel 5 (grid
+// swizzling)").
 __host__ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group_m,
                                                 int &tm, int &tn) {
     const int per_group = group_m * tiles_n;
@@ -87,43 +117,45 @@ __host__ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n,
 __device__ __forceinline__ int swz(int k, int col) { return col ^ (((k >> 2) & 3) << 3); }
 
 // Register staging for an operand whose global rows run along K: the 128 x 16
-// tile is 512 float4 chunks, two per thread; chunk c covers row c / 4 and
-// k = 4*(c % 4) .. +3.  A warp covers 8 whole 64-byte row pieces.
-template <bool VEC>
+// tile is 512 float4 chunks, CHUNKS per thread; chunk c covers row c / 4 and
+// k = 4*(c % 4) .. +3.  A warp covers 8 whole 64-byte row pieces.  Chunks
+// H0 and H0 + 1 of this thread are loaded into r.
+template <bool VEC, int H0>
 __device__ __forceinline__ void kmajor_load(const float *__restrict__ X, int64_t ldx,
                                             int rows_total, int K, int row0, int k0,
                                             int tid, float (&r)[2][4]) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int c = tid + h * THREADS;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int c = tid + (H0 + hh) * THREADS;
         const int gr = row0 + (c >> 2);
         const int gk = k0 + (c & 3) * 4;
         const float *src = X + (int64_t)gr * ldx + gk;
         if (VEC && gr < rows_total && gk + 3 < K) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-            r[h][0] = v.x; r[h][1] = v.y; r[h][2] = v.z; r[h][3] = v.w;
+            r[hh][0] = v.x; r[hh][1] = v.y; r[hh][2] = v.z; r[hh][3] = v.w;
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                r[h][j] = (gr < rows_total && gk + j < K) ? __ldg(src + j) : 0.0f;
+                r[hh][j] = (gr < rows_total && gk + j < K) ? __ldg(src + j) : 0.0f;
         }
     }
 }
 
-// Transposing store of the staged chunks into the k-major shared tile.
+// Transposing store of the staged chunks H0, H0 + 1 into the k-major tile.
 // For a fixed j the 32 lanes of a warp hit 32 different banks: the low three
 // bits of the row come from the lane, bits 3-4 from (warp ^ k-quad).
+template <int H0>
 __device__ __forceinline__ void kmajor_store(float *__restrict__ s, int tid,
                                              const float (&r)[2][4]) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int c = tid + h * THREADS;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int c = tid + (H0 + hh) * THREADS;
         const int row = c >> 2;
         const int kq = c & 3;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int k = kq * 4 + j;
-            s[k * BM + swz(k, row)] = r[h][j];
+            s[k * BM + swz(k, row)] = r[hh][j];
         }
     }
 }
@@ -136,7 +168,7 @@ __device__ __forceinline__ void mnmajor_async(const float *__restrict__ X, int64
                                               int cols_total, int K, int col0, int k0,
                                               int tid, float *__restrict__ s) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < CHUNKS; ++h) {
         const int c = tid + h * THREADS;
         const int k = c >> 5;
         const int cc = (c & 31) * 4;
@@ -162,12 +194,13 @@ __device__ __forceinline__ void mnmajor_async(const float *__restrict__ X, int64
     }
 }
 
-// One output quad (4 consecutive columns of one row): alpha/beta epilogue.
+// alpha/beta epilogue of one element (beta == 0 is handled by the caller:
+// C is then not read).
 __device__ __forceinline__ float axpby(float alpha, float acc, float beta, float c) {
-    // beta == 0 is handled by the caller (C is then not read)
     return __fmaf_rn(alpha, acc, __fmul_rn(beta, c));
 }
 
+// One output quad (4 consecutive columns of one row) into C.
 __device__ __forceinline__ void store_quad(const Params &p, int row, int col, float4 v) {
     if (row >= p.M || col >= p.N) return;
     float *dst = p.C + (int64_t)row * p.ldc + col;
@@ -195,6 +228,132 @@ __device__ __forceinline__ void store_quad(const Params &p, int row, int col, fl
     }
 }
 
+// k-tiles [j0, j1) of tile t; a whole tile goes to C, a part to partial[slot].
+template <bool A_KMAJOR, bool B_KMAJOR, bool VEC>
+__device__ __forceinline__ void run_share(const Params &p, float (*sA)[BK * BM],
+                                          float (*sB)[BK * BN], int t, int j0, int j1, int slot) {
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    int tm, tn;
+    raster(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * BM;
+    const int n0 = tn * BN;
+    const int nkt = j1 - j0;
+
+    // thread -> outputs: 4 warps as 2 x 2 of 64 x 64
+    const int wm = warp & 1;
+    const int wn = warp >> 1;
+    const int lr = lane >> 2;           // 0..7
+    const int lc = lane & 3;            // 0..3
+    const int am = wm * 64 + lr * 4;    // rows am + {0..3}, am + 32 + {0..3}
+    const int bn = wn * 64 + lc * 4;    // columns bn + 16 g + {0..3}
+
+    float2 acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+
+    float ra[2][4], rb[2][4];
+    using H_0 = std::integral_constant<int, 0>;
+    using H_2 = std::integral_constant<int, 2>;
+    // K-contiguous operands are staged through registers in two halves:
+    // chunks 0-1 are loaded at the start of a k-tile and parked in shared
+    // memory half way through it, chunks 2-3 are loaded then and parked at its
+    // end; MN-contiguous operands are copied with cp.async.
+    auto issue_async = [&](int kt, int stage) {
+        const int k0 = kt * BK;
+        if (!A_KMAJOR) mnmajor_async<VEC>(p.A, p.lda, p.M, p.K, m0, k0, tid, sA[stage]);
+        if (!B_KMAJOR) mnmajor_async<VEC>(p.B, p.ldb, p.N, p.K, n0, k0, tid, sB[stage]);
+        cp_async_commit();
+    };
+    auto load_half = [&](int kt, auto h0) {
+        constexpr int H0 = decltype(h0)::value;
+        const int k0 = kt * BK;
+        if (A_KMAJOR) kmajor_load<VEC, H0>(p.A, p.lda, p.M, p.K, m0, k0, tid, ra);
+        if (B_KMAJOR) kmajor_load<VEC, H0>(p.B, p.ldb, p.N, p.K, n0, k0, tid, rb);
+    };
+    auto park_half = [&](int stage, auto h0) {
+        constexpr int H0 = decltype(h0)::value;
+        if (A_KMAJOR) kmajor_store<H0>(sA[stage], tid, ra);
+        if (B_KMAJOR) kmajor_store<H0>(sB[stage], tid, rb);
+    };
+
+    issue_async(j0, 0);
+    load_half(j0, H_0{});
+    park_half(0, H_0{});
+    load_half(j0, H_2{});
+    park_half(0, H_2{});
+    cp_async_wait_all();
+    __syncthreads();
+
+    for (int it = 0; it < nkt; ++it) {
+        const int stage = it & 1;
+        const bool has_next = it + 1 < nkt;
+        if (has_next) {
+            issue_async(j0 + it + 1, stage ^ 1);
+            load_half(j0 + it + 1, H_0{});
+        }
+        const float *As = sA[stage];
+        const float *Bs = sB[stage];
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            if (k == BK / 2 && has_next) {
+                park_half(stage ^ 1, H_0{});
+                load_half(j0 + it + 1, H_2{});
+            }
+            const int s = ((k >> 2) & 3) << 3;
+            const float4 a0 = *reinterpret_cast<const float4 *>(As + k * BM + (am ^ s));
+            const float4 a1 = *reinterpret_cast<const float4 *>(As + k * BM + ((am + 32) ^ s));
+            float2 b[8];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 bg =
+                    *reinterpret_cast<const float4 *>(Bs + k * BN + ((bn + 16 * g) ^ s));
+                b[2 * g] = make_float2(bg.x, bg.y);
+                b[2 * g + 1] = make_float2(bg.z, bg.w);
+            }
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
+            }
+        }
+        if (has_next) {
+            park_half(stage ^ 1, H_2{});
+            cp_async_wait_all();
+        }
+        __syncthreads();
+    }
+
+    if (nkt != p.kt) {
+        // raw partial sums into this share's dense 128 x 128 block
+        float *blk = p.partial + (int64_t)slot * (BM * BN);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = am + (i & 3) + (i >> 2) * 32;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<float4 *>(blk + r * BN + bn + 16 * g) =
+                    make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                                acc[i][2 * g + 1].y);
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + am + (i & 3) + (i >> 2) * 32;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            store_quad(p, row, n0 + bn + 16 * g,
+                       make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                                   acc[i][2 * g + 1].y));
+    }
+}
+
 // A_KMAJOR: op(A) rows run along K in memory (transA 'N').
 // B_KMAJOR: op(B) columns run along K in memory (transB 'T').
 // VEC: A and B base pointers are 16-byte aligned and their leading
@@ -203,138 +362,73 @@ template <bool A_KMAJOR, bool B_KMAJOR, bool VEC>
 __global__ void __launch_bounds__(THREADS, 2) ffma_gemm_kernel(const Params p) {
     __shared__ __align__(16) float sA[2][BK * BM];
     __shared__ __align__(16) float sB[2][BK * BN];
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-
-    const int total_kt = (p.K + BK - 1) / BK;
-    int tile, unit = -1, kt_begin = 0, kt_end = total_kt;
     if ((int)blockIdx.x < p.dp_tiles) {
-        tile = blockIdx.x;
-    } else {
-        unit = blockIdx.x - p.dp_tiles;                 // partial block index
-        tile = p.dp_tiles + unit / p.split;
-        kt_begin = (unit % p.split) * p.kt_per_split;
-        kt_end = min(kt_begin + p.kt_per_split, total_kt);
-    }
-    int tm, tn;
-    raster(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int m0 = tm * BM;
-    const int n0 = tn * BN;
-    const int nkt = kt_end - kt_begin;
-
-    // thread -> outputs
-    const int wm = warp & 3;            // warp row   (4 x 32 rows)
-    const int wn = warp >> 2;           // warp col   (2 x 64 cols)
-    const int tr = lane >> 3;           // 0..3
-    const int tc = lane & 7;            // 0..7
-    const int am = wm * 32 + tr * 4;    // first of the thread's A rows in the tile
-    const int bn = wn * 64 + tc * 4;    // first of the thread's B cols in the tile
-
-    float2 acc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-
-    float ra[2][4], rb[2][4];
-
-    auto issue = [&](int kt, int stage) {
-        const int k0 = kt * BK;
-        if (A_KMAJOR) kmajor_load<VEC>(p.A, p.lda, p.M, p.K, m0, k0, tid, ra);
-        else mnmajor_async<VEC>(p.A, p.lda, p.M, p.K, m0, k0, tid, sA[stage]);
-        if (B_KMAJOR) kmajor_load<VEC>(p.B, p.ldb, p.N, p.K, n0, k0, tid, rb);
-        else mnmajor_async<VEC>(p.B, p.ldb, p.N, p.K, n0, k0, tid, sB[stage]);
-        cp_async_commit();
-    };
-    auto park = [&](int stage) {
-        if (A_KMAJOR) kmajor_store(sA[stage], tid, ra);
-        if (B_KMAJOR) kmajor_store(sB[stage], tid, rb);
-    };
-
-    if (nkt > 0) {
-        issue(kt_begin, 0);
-        park(0);
-        cp_async_wait_all();
-        __syncthreads();
-    }
-
-    for (int it = 0; it < nkt; ++it) {
-        const int stage = it & 1;
-        const bool has_next = it + 1 < nkt;
-        if (has_next) issue(kt_begin + it + 1, stage ^ 1);
-
-        const float *As = sA[stage];
-        const float *Bs = sB[stage];
-#pragma unroll
-        for (int k = 0; k < BK; ++k) {
-            const int s = ((k >> 2) & 3) << 3;
-            const float4 a0 = *reinterpret_cast<const float4 *>(As + k * BM + (am ^ s));
-            const float4 a1 = *reinterpret_cast<const float4 *>(As + k * BM + ((am + 16) ^ s));
-            const float4 b0 = *reinterpret_cast<const float4 *>(Bs + k * BN + (bn ^ s));
-            const float4 b1 = *reinterpret_cast<const float4 *>(Bs + k * BN + ((bn + 32) ^ s));
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float2 b[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                 make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 ai = make_float2(a[i], a[i]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
-            }
-        }
-
-        if (has_next) {
-            park(stage ^ 1);
-            cp_async_wait_all();
-        }
-        __syncthreads();
-    }
-
-    if (unit >= 0) {
-        // raw partial sums into this unit's dense 128 x 128 block
-        float *blk = p.partial + (int64_t)unit * (BM * BN);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = am + (i & 3) + (i >> 2) * 16;
-            *reinterpret_cast<float4 *>(blk + r * BN + bn) =
-                make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
-            *reinterpret_cast<float4 *>(blk + r * BN + bn + 32) =
-                make_float4(acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y);
-        }
+        run_share<A_KMAJOR, B_KMAJOR, VEC>(p, sA, sB, blockIdx.x, 0, p.kt, 0);
         return;
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = m0 + am + (i & 3) + (i >> 2) * 16;
-        store_quad(p, row, n0 + bn,
-                   make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y));
-        store_quad(p, row, n0 + bn + 32,
-                   make_float4(acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y));
+    const int c = blockIdx.x - p.dp_tiles;
+    const int64_t end = share_begin(p.sk_iters, p.sk_ctas, c + 1);
+    int64_t it = share_begin(p.sk_iters, p.sk_ctas, c);
+    bool first = true;
+    while (it < end) {
+        const int u = (int)(it / p.kt);
+        const int j0 = (int)(it - (int64_t)u * p.kt);
+        const int j1 = (int)((int64_t)j0 + (end - it) < (int64_t)p.kt ? j0 + (end - it) : p.kt);
+        // the shared tiles are free again: the share's last k-tile ended in a barrier
+        run_share<A_KMAJOR, B_KMAJOR, VEC>(p, sA, sB, p.dp_tiles + u, j0, j1,
+                                           first ? 2 * c : 2 * c + 1);
+        it += j1 - j0;
+        first = false;
     }
 }
 
-// For each split tile (one CTA per tile): C = alpha * (sum of its K-slice
-// partial blocks, added in ascending slice order) + beta * C.  Threads walk
-// the 128 x 128 tile row by row, four columns each, so reads of the partial
-// blocks and of C are coalesced.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const Params p) {
-    const int tile = p.dp_tiles + blockIdx.x;
-    int tm, tn;
-    raster(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
-    const float *base = p.partial + (int64_t)blockIdx.x * p.split * (BM * BN);
-    for (int e = threadIdx.x * 4; e < BM * BN; e += blockDim.x * 4) {
-        const int r = e / BN, c = e % BN;
-        if (m0 + r >= p.M || n0 + c >= p.N) continue;
-        float4 s = *reinterpret_cast<const float4 *>(base + e);
-        for (int q = 1; q < p.split; ++q) {
-            const float4 t = *reinterpret_cast<const float4 *>(base + q * (BM * BN) + e);
-            s.x = __fadd_rn(s.x, t.x); s.y = __fadd_rn(s.y, t.y);
-            s.z = __fadd_rn(s.z, t.z); s.w = __fadd_rn(s.w, t.w);
+// Grid (remaining tiles, FIX_PARTS): block (u, part) handles rows
+// 16*part .. +15 of remaining tile u.  A tile cut between several shares gets
+// C = alpha * (sum of its partial blocks, added in ascending k order) + beta*C;
+// a tile inside one share was written by it and is skipped.  The shares'
+// workspace slots are looked up once per block; threads then walk the rows
+// four columns each (coalesced).
+constexpr int FIX_PARTS = 8;
+constexpr int FIX_MAX_SHARES = 64;
+
+__global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
+    __shared__ int slots[FIX_MAX_SHARES];
+    __shared__ int nslots;
+    const int u = blockIdx.x;
+    const int64_t x0 = (int64_t)u * p.kt;
+    const int c_lo = share_owner(p.sk_iters, p.sk_ctas, x0);
+    const int c_hi = share_owner(p.sk_iters, p.sk_ctas, x0 + p.kt - 1);
+    if (c_lo == c_hi) return;
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int c = c_lo; c <= c_hi; ++c) {
+            if (share_begin(p.sk_iters, p.sk_ctas, c) == share_begin(p.sk_iters, p.sk_ctas, c + 1))
+                continue;                                       // empty share
+            if (n < FIX_MAX_SHARES) slots[n] = partial_slot(p, c, u);
+            ++n;
         }
-        store_quad(p, m0 + r, n0 + c, s);
+        nslots = n;
+    }
+    __syncthreads();
+    // the selector keeps shares per tile <= 32; more would not fit the table
+    if (nslots > FIX_MAX_SHARES) return;
+    int tm, tn;
+    raster(p.dp_tiles + u, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int rows = BM / FIX_PARTS;
+    const int n = nslots;
+    for (int e = blockIdx.y * rows * BN + threadIdx.x * 4; e < (blockIdx.y + 1) * rows * BN;
+         e += blockDim.x * 4) {
+        const int r = e / BN, col = e % BN;
+        if (m0 + r >= p.M || n0 + col >= p.N) continue;
+        float4 s = *reinterpret_cast<const float4 *>(p.partial + (int64_t)slots[0] * (BM * BN) + e);
+        for (int q = 1; q < n; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(
+                p.partial + (int64_t)slots[q] * (BM * BN) + e);
+            s.x = __fadd_rn(s.x, v.x); s.y = __fadd_rn(s.y, v.y);
+            s.z = __fadd_rn(s.z, v.z); s.w = __fadd_rn(s.w, v.w);
+        }
+        store_quad(p, m0 + r, n0 + col, s);
     }
 }
 

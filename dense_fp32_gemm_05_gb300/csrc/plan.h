@@ -42,29 +42,15 @@ inline int check_args(char ta, char tb, int64_t M, int64_t N, int64_t K, float a
 
 struct Plan {
     int path = SGEMM_PATH_FFMA;
-    int split = 1;      // FFMA: K slices of the tail tiles (1 = none)
-    int dp_tiles = 0;   // FFMA: tiles computed whole
+    int split = 1;      // FFMA: CTAs per shared tile, rounded up (1 = every tile whole)
+    int ctas = 0;       // FFMA: CTAs sharing the iterations of the tiles after dp_tiles
+    int dp_tiles = 0;   // tiles computed whole (tensor cores: at full width)
     int tile_m = 128, tile_n = 128;
     int vector = 1;     // 16-byte operand loads (else 4-byte edge path)
     int c_vector = 1;   // 16-byte C accesses
     int group_m = 8;    // rasterisation group height (tiles)
     int tail_nsplit = 1;  // tensor cores: column slices of the last-wave tiles
 };
-
-// Cost model of the FFMA path in units of one k-tile step of one CTA
-// (about 2 us at 2 CTAs per SM).  CTAs run in waves of `slots`; a whole
-// tile takes kt steps, a slice ceil(kt / split).  `dp` (0 or a multiple of
-// `slots`) whole tiles run first, then the sliced tail units.  Each partial
-// block costs ~0.01 step of HBM traffic in the reduction, which also adds a
-// fixed ~2 steps (a second launch).
-inline double ffma_cost(int64_t tiles, int64_t kt, int64_t dp, int64_t split, int64_t slots) {
-    if (split == 1) return (double)((tiles + slots - 1) / slots) * (double)kt;
-    const int64_t units = (tiles - dp) * split;
-    const int64_t slice = (kt + split - 1) / split;
-    const int64_t slice_waves = (units + slots - 1) / slots;
-    return (double)(dp / slots) * (double)kt + (double)slice_waves * (double)slice +
-           0.01 * (double)units + 2.0;
-}
 
 // Chooses path, tile, split and vectorisation.  `path`/`split` 0 = auto.
 inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -86,33 +72,37 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
     pl.vector = (a_al && lda % 4 == 0 && b_al && ldb % 4 == 0) ? 1 : 0;
     pl.c_vector = (c_al && ldc % 4 == 0) ? 1 : 0;
     if (pl.path == SGEMM_PATH_FFMA) {
+        // A grid of at least one full wave (2 CTAs per SM) runs whole tiles:
+        // measured on GB300, sharing the last partial wave ("stream-K") or
+        // cutting every tile in two K slices gains no more than the run-to-run
+        // spread (~2 %), while whole tiles keep the result bit-identical to the
+        // naive loop.  A grid smaller than one wave has its k-tile iterations
+        // shared equally by up to a wave of CTAs (at least 8 k-tiles, 128 of K,
+        // each, at most 32 CTAs per tile): 1024^3 runs 1.7x faster that way.
+        // Forced split s: every tile cut into s K slices; s = 1 keeps every
+        // tile whole.
         const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
-        const int64_t kt = (K + 15) / 16;
-        const int64_t slots = 2LL * sms;        // two 256-thread CTAs per SM
-        if (split > 0) {
-            pl.split = (int)std::min<int64_t>(split, std::max<int64_t>(kt, 1));
-            pl.dp_tiles = pl.split == 1 ? (int)tiles : 0;
+        const int64_t kt = std::max<int64_t>((K + 15) / 16, 1);
+        const int64_t slots = 2LL * sms;
+        int64_t dp, sk;
+        if (split == 1) {
+            dp = tiles;
+            sk = 0;
+        } else if (split > 1) {
+            dp = 0;
+            sk = tiles * std::min<int64_t>(split, kt);
+        } else if (tiles >= slots) {
+            dp = tiles;
+            sk = 0;
         } else {
-            // try "all tiles whole" and, for each split s, "whole waves of
-            // whole tiles + the rest sliced in s"; keep the cheapest
-            double best = ffma_cost(tiles, kt, tiles, 1, slots);
-            pl.split = 1;
-            pl.dp_tiles = (int)tiles;
-            const int64_t max_split = std::min<int64_t>(16, kt / 4);   // slices >= 64 of K
-            for (int64_t s = 2; s <= max_split; ++s) {
-                const int64_t dp = (tiles / slots) * slots;            // whole waves
-                for (int64_t d : {dp, (int64_t)0}) {
-                    if (d == tiles) continue;
-                    const double c = ffma_cost(tiles, kt, d, s, slots);
-                    if (c < best * 0.97) {                              // must win clearly
-                        best = c;
-                        pl.split = (int)s;
-                        pl.dp_tiles = (int)d;
-                    }
-                }
-            }
+            dp = 0;
+            sk = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(slots, (tiles * kt + 7) / 8),
+                                                        32 * tiles));
         }
-        if (pl.split == 1) pl.dp_tiles = (int)tiles;
+        pl.dp_tiles = (int)dp;
+        pl.ctas = (int)std::min<int64_t>(sk, INT32_MAX);
+        const int64_t rem = tiles - dp;
+        pl.split = (sk == 0 || rem == 0) ? 1 : (int)((sk + rem - 1) / rem);
     } else {
         // tensor-core path: 128-row tiles, N of the MMA from the problem's N,
         // one CTA per SM.  Tiles after the last full wave may run as 2 or 4

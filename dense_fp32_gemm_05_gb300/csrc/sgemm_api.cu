@@ -115,9 +115,11 @@ static void launch_ffma_t(const ffma::Params &p, int grid, cudaStream_t s) {
     ffma::ffma_gemm_kernel<AK, BK_, V><<<grid, ffma::THREADS, 0, s>>>(p);
 }
 
-static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K,
-                    float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
-                    float beta, float *C, int64_t ldc, cudaStream_t s) {
+// Fills the FFMA kernel parameters of a plan (shared by sgemm_ex and the
+// static-scratch entry point).
+static ffma::Params ffma_params(const Plan &pl, int64_t M, int64_t N, int64_t K, float alpha,
+                                const float *A, int64_t lda, const float *B, int64_t ldb,
+                                float beta, float *C, int64_t ldc) {
     ffma::Params p{};
     p.A = A; p.B = B; p.C = C; p.partial = nullptr;
     p.lda = lda; p.ldb = ldb; p.ldc = ldc;
@@ -126,40 +128,58 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
     p.tiles_m = (int)((M + ffma::BM - 1) / ffma::BM);
     p.tiles_n = (int)((N + ffma::BN - 1) / ffma::BN);
     p.group_m = pl.group_m;
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int total_kt = (int)((K + ffma::BK - 1) / ffma::BK);
-    int split = std::max(1, std::min(pl.split, total_kt));
-    int kt_per = (total_kt + split - 1) / split;
-    split = (total_kt + kt_per - 1) / kt_per;          // every slice owns >= 1 k-tile
-    p.dp_tiles = split == 1 ? tiles : std::min(pl.dp_tiles, tiles);
-    p.split = split;
-    p.kt_per_split = kt_per;
+    p.kt = (int)((K + ffma::BK - 1) / ffma::BK);
+    const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+    p.dp_tiles = (int)std::min<int64_t>(pl.dp_tiles, tiles);
+    p.sk_iters = (tiles - p.dp_tiles) * p.kt;
+    p.sk_ctas = p.sk_iters == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(pl.ctas, p.sk_iters));
     p.c_vec = pl.c_vector;
-    const int tail = tiles - p.dp_tiles;
-    if (tail > 0) {
+    return p;
+}
+
+// True when some share starts or ends inside a tile (partials + fixup needed).
+static bool ffma_has_partials(const ffma::Params &p) {
+    if (p.sk_ctas == 0) return false;
+    return !(p.sk_iters % p.sk_ctas == 0 && (p.sk_iters / p.sk_ctas) % p.kt == 0);
+}
+
+static int ffma_grid(const ffma::Params &p) { return p.dp_tiles + p.sk_ctas; }
+static int ffma_fix_tiles(const ffma::Params &p) {
+    return p.tiles_m * p.tiles_n - p.dp_tiles;
+}
+
+static int launch_ffma(const ffma::Params &p, char ta, char tb, bool vec, cudaStream_t s) {
+    const bool ak = is_notrans(ta), bk = !is_notrans(tb);
+    const int grid = ffma_grid(p);
+    if (ak && !bk && vec) launch_ffma_t<true, false, true>(p, grid, s);
+    else if (ak && !bk && !vec) launch_ffma_t<true, false, false>(p, grid, s);
+    else if (ak && bk && vec) launch_ffma_t<true, true, true>(p, grid, s);
+    else if (ak && bk && !vec) launch_ffma_t<true, true, false>(p, grid, s);
+    else if (!ak && !bk && vec) launch_ffma_t<false, false, true>(p, grid, s);
+    else if (!ak && !bk && !vec) launch_ffma_t<false, false, false>(p, grid, s);
+    else if (!ak && bk && vec) launch_ffma_t<false, true, true>(p, grid, s);
+    else launch_ffma_t<false, true, false>(p, grid, s);
+    return launch_status();
+}
+
+static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K,
+                    float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                    float beta, float *C, int64_t ldc, cudaStream_t s) {
+    ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    const bool partials = ffma_has_partials(p);
+    if (partials) {
         void *ws = nullptr;
-        const size_t bytes = (size_t)tail * split * ffma::BM * ffma::BN * sizeof(float);
+        const size_t bytes = (size_t)2 * p.sk_ctas * ffma::BM * ffma::BN * sizeof(float);
         int st = workspace(s, bytes, &ws);
         if (st != SGEMM_OK) return st;
         p.partial = static_cast<float *>(ws);
     }
-    const int grid = p.dp_tiles + tail * split;
-    const bool ak = is_notrans(ta), bk = !is_notrans(tb);
-    const bool v = pl.vector != 0;
     timing_mark(s, true);
-    if (ak && !bk && v) launch_ffma_t<true, false, true>(p, grid, s);
-    else if (ak && !bk && !v) launch_ffma_t<true, false, false>(p, grid, s);
-    else if (ak && bk && v) launch_ffma_t<true, true, true>(p, grid, s);
-    else if (ak && bk && !v) launch_ffma_t<true, true, false>(p, grid, s);
-    else if (!ak && !bk && v) launch_ffma_t<false, false, true>(p, grid, s);
-    else if (!ak && !bk && !v) launch_ffma_t<false, false, false>(p, grid, s);
-    else if (!ak && bk && v) launch_ffma_t<false, true, true>(p, grid, s);
-    else launch_ffma_t<false, true, false>(p, grid, s);
+    int st = launch_ffma(p, ta, tb, pl.vector != 0, s);
     timing_mark(s, false);
-    int st = launch_status();
     if (st != SGEMM_OK) return st;
-    if (tail > 0) {
-        ffma::splitk_reduce_kernel<<<tail, 256, 0, s>>>(p);
+    if (partials) {
+        ffma::sk_fixup_kernel<<<dim3(ffma_fix_tiles(p), ffma::FIX_PARTS), 256, 0, s>>>(p);
         st = launch_status();
     }
     return st;
@@ -214,7 +234,8 @@ extern "C" int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t 
 extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldb, int64_t ldc, int a_aligned, int b_aligned,
                           int c_aligned, int path, int split, int num_sms, int *out_path,
-                          int *out_split, int *out_tile_m, int *out_tile_n, int *out_vector) {
+                          int *out_split, int *out_tile_m, int *out_tile_n, int *out_vector,
+                          int *out_ctas) {
     int st = check_args(transA, transB, M, N, K, 1.0f, nullptr, lda, nullptr, ldb, 0.0f,
                         nullptr, ldc, /*pointers_checked=*/false);
     if (st != SGEMM_OK) return st;
@@ -229,6 +250,14 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
     if (out_tile_m) *out_tile_m = pl.tile_m;
     if (out_tile_n) *out_tile_n = pl.tile_n;
     if (out_vector) *out_vector = pl.vector;
+    if (out_ctas) {
+        if (pl.path == SGEMM_PATH_FFMA) {
+            *out_ctas = pl.dp_tiles + pl.ctas;
+        } else {
+            const int64_t tiles = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
+            *out_ctas = (int)(pl.dp_tiles + (tiles - pl.dp_tiles) * pl.tail_nsplit);
+        }
+    }
     return SGEMM_OK;
 }
 
@@ -325,6 +354,8 @@ constexpr size_t kStaticPartialFloats =
     (size_t)kStaticPartialTiles * ffma::BM * ffma::BN;
 
 // Every GPU that loads the library holds this array until the process exits.
+// It holds 2 slots per CTA of the stream-K decomposition (a CTA's first and
+// last partial tile), so plans with up to 128 CTAs fit.
 static __device__ __align__(256) float g_static_partials[kStaticPartialFloats];
 
 // Device address of g_static_partials per device, looked up once with that
@@ -374,45 +405,24 @@ extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, in
     st = make_plan(transA, transB, M, N, K, lda, ldb, ldc, aligned16(A), aligned16(B),
                    aligned16(C), SGEMM_PATH_FFMA, split, d->sms, &pl);
     if (st != SGEMM_OK) return st;
-
-    ffma::Params p{};
-    p.A = A; p.B = B; p.C = C; p.partial = nullptr;
-    p.lda = lda; p.ldb = ldb; p.ldc = ldc;
-    p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.alpha = alpha; p.beta = beta;
-    p.tiles_m = (int)((M + ffma::BM - 1) / ffma::BM);
-    p.tiles_n = (int)((N + ffma::BN - 1) / ffma::BN);
-    p.group_m = pl.group_m;
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int total_kt = (int)((K + ffma::BK - 1) / ffma::BK);
-    int sp = std::max(1, std::min(pl.split, total_kt));
-    const int kt_per = (total_kt + sp - 1) / sp;
-    sp = (total_kt + kt_per - 1) / kt_per;
-    p.dp_tiles = sp == 1 ? tiles : std::min(pl.dp_tiles, tiles);
-    p.split = sp;
-    p.kt_per_split = kt_per;
-    p.c_vec = pl.c_vector;
-    const int tail = tiles - p.dp_tiles;
-    if ((int64_t)tail * sp > kStaticPartialTiles) return SGEMM_ERR_SCRATCH;
-    if (tail > 0) {
+    ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    bool partials = ffma_has_partials(p);
+    if (partials && 2LL * p.sk_ctas > kStaticPartialTiles) {
+        if (split != 0) return SGEMM_ERR_SCRATCH;    // the caller's split does not fit
+        // the selector's choice does not fit: every tile whole needs no scratch
+        p.dp_tiles = p.tiles_m * p.tiles_n;
+        p.sk_ctas = 0;
+        p.sk_iters = 0;
+        partials = false;
+    }
+    if (partials) {
         st = static_partials(&p.partial);
         if (st != SGEMM_OK) return st;
     }
-    const int grid = p.dp_tiles + tail * sp;
-    const bool ak = is_notrans(transA), bk = !is_notrans(transB);
-    const bool v = pl.vector != 0;
-    if (ak && !bk && v) launch_ffma_t<true, false, true>(p, grid, s);
-    else if (ak && !bk && !v) launch_ffma_t<true, false, false>(p, grid, s);
-    else if (ak && bk && v) launch_ffma_t<true, true, true>(p, grid, s);
-    else if (ak && bk && !v) launch_ffma_t<true, true, false>(p, grid, s);
-    else if (!ak && !bk && v) launch_ffma_t<false, false, true>(p, grid, s);
-    else if (!ak && !bk && !v) launch_ffma_t<false, false, false>(p, grid, s);
-    else if (!ak && bk && v) launch_ffma_t<false, true, true>(p, grid, s);
-    else launch_ffma_t<false, true, false>(p, grid, s);
-    st = launch_status();
+    st = launch_ffma(p, transA, transB, pl.vector != 0, s);
     if (st != SGEMM_OK) return st;
-    if (tail > 0) {
-        ffma::splitk_reduce_kernel<<<tail, 256, 0, s>>>(p);
+    if (partials) {
+        ffma::sk_fixup_kernel<<<dim3(ffma_fix_tiles(p), ffma::FIX_PARTS), 256, 0, s>>>(p);
         st = launch_status();
     }
     return st;

@@ -100,9 +100,12 @@ int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
 /*
  * sgemm_ex - as sgemm, with the path forced (sgemm_path) and the split-K
  * factor forced (split >= 1, or 0 to let the selector decide).  The split
- * applies to the FFMA path: split > 1 sums K in `split` contiguous slices
- * whose partial results are added in a fixed order (deterministic, but no
- * longer bit-identical to the naive loop).
+ * applies to the FFMA path: split = 1 computes every output tile whole
+ * (bit-identical to the naive ascending-k FMA loop); split > 1 sums K in
+ * `split` contiguous slices per tile whose partial results are added in a
+ * fixed order; 0 lets the selector share all tiles x k-tiles iterations
+ * equally among two CTAs per SM ("stream-K": deterministic, not
+ * bit-identical to the naive loop where a tile is shared).
  * Returns SGEMM_ERR_UNSUPPORTED when the forced path cannot run the problem.
  */
 int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
@@ -114,19 +117,20 @@ int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
 /*
  * sgemm_plan - the selector's decision for a problem, without launching
  * anything and without touching the GPU.  `path` and `split` as in
- * sgemm_ex (0 = let the selector decide).  a_aligned/b_aligned/c_aligned
- * say whether the base pointer is 16-byte aligned.  On success writes the
- * chosen path (sgemm_path), the FFMA split-K factor, the tile rows and
- * columns, and whether 16-byte vector loads are used (1) or the 4-byte
- * edge path (0).  Any output pointer may be NULL.
- * Returns SGEMM_OK or a negative argument index as sgemm.
+ * sgemm_ex (0 = let the selector decide); num_sms is the GPU's SM count.
+ * a_aligned/b_aligned/c_aligned say whether the base pointer is 16-byte
+ * aligned.  On success writes the chosen path (sgemm_path), the FFMA CTAs
+ * per output tile rounded up (1 = every tile whole), the tile rows and
+ * columns, whether the FFMA path uses 16-byte loads (1) or the 4-byte edge
+ * path (0), and the number of CTAs of the main kernel.  Any output pointer
+ * may be NULL.  Returns SGEMM_OK or a negative argument index as sgemm.
  */
 int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
                int64_t lda, int64_t ldb, int64_t ldc,
                int a_aligned, int b_aligned, int c_aligned,
                int path, int split, int num_sms,
                int *out_path, int *out_split, int *out_tile_m, int *out_tile_n,
-               int *out_vector);
+               int *out_vector, int *out_ctas);
 
 /* Static description of a status code (never NULL). */
 const char *sgemm_status_string(int status);
@@ -178,12 +182,13 @@ int sgemm_release_workspace(void);
  * never does: it calls no cudaMalloc, cudaFree or allocating library routine.
  *
  * Same arguments and result as sgemm_ex(..., SGEMM_PATH_FFMA, split), with
- * `split` = 0 letting the selector choose.  The split-K partial sums go to a
- * file-scope static __device__ array of 16 MiB (256 partial tiles of
- * 128 x 128 floats) that every GPU which loads the library holds until the
- * process exits.  A problem whose plan needs more partial tiles than that
- * returns SGEMM_ERR_SCRATCH and launches nothing (force a smaller split, or
- * split = 1, which needs no scratch).
+ * `split` = 0 letting the selector choose.  The partial sums of tiles shared
+ * by several CTAs go to a file-scope static __device__ array of 16 MiB (256
+ * partial tiles of 128 x 128 floats, two per CTA) that every GPU which loads
+ * the library holds until the process exits.  With split = 0 a plan that
+ * would need more falls back to computing every tile whole (no scratch);
+ * a forced split that needs more returns SGEMM_ERR_SCRATCH and launches
+ * nothing (split = 1 never needs scratch).
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call

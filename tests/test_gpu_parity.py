@@ -255,3 +255,35 @@ def test_workload_full_size_sampled(oracle_mod, name):
     rep = oracle_mod.compare(out[rows, cols], ref, bound, w.K, w.alpha)
     assert rep["pass"], rep
     assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("name", ["sq4096_nn", "ragged_tn", "skinny_nt", "sq1024_nn"])
+def test_ffma_full_size_sampled(oracle_mod, name):
+    """The FFMA path at full size with the selector's stream-K decomposition
+    (shares crossing tile boundaries, fixup of shared tiles), sampled against
+    the fp64 oracle within the bound; and forced whole tiles (split = 1)
+    bit-identical to the oracle's ascending-k FMA evaluation on the samples."""
+    import torch
+
+    w = gi.WORKLOADS[name]
+    A, B, C = gi.make_inputs(w)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    rows, cols = gi.sample_points(w.M, w.N, 2048, seed=w.seed + 7)
+    ref, bound = oracle_mod.gemm_f64(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A, A.shape[1],
+                                     B, B.shape[1], w.beta, C, w.N, points=(rows, cols))
+    seq = oracle_mod.gemm_f32_seq(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A, A.shape[1],
+                                  B, B.shape[1], w.beta, C, w.N, points=(rows, cols))
+    for split in (0, 1):
+        dC = (torch.from_numpy(C).cuda() if C is not None
+              else torch.full((w.M, w.N), float("nan"), device="cuda"))
+        st = sg.sgemm_ex(w.transA, w.transB, w.M, w.N, w.K, w.alpha, dA.data_ptr(), A.shape[1],
+                         dB.data_ptr(), B.shape[1], w.beta, dC.data_ptr(), w.N,
+                         torch.cuda.current_stream(), sg.PATH_FFMA, split)
+        torch.cuda.synchronize()
+        assert st == 0
+        out = dC.cpu().numpy()[rows, cols]
+        rep = oracle_mod.compare(out, ref, bound, w.K, w.alpha)
+        assert rep["pass"], (split, rep)
+        if split == 1:
+            assert np.array_equal(out.view(np.uint32), seq.view(np.uint32))
