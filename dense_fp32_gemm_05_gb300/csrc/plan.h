@@ -50,6 +50,8 @@ struct Plan {
     int c_vector = 1;   // 16-byte C accesses
     int group_m = 8;    // rasterisation group height (tiles)
     int tail_nsplit = 1;  // tensor cores: column slices of the last-wave tiles
+    int fuse_a = 1;       // tensor cores: split A in shared memory when its layout allows
+    int fuse_b = 1;       // tensor cores: same for B
 };
 
 // Chooses path, tile, split and vectorisation.  `path`/`split` 0 = auto.
@@ -112,6 +114,14 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         pl.tile_m = 128;
         pl.tile_n = N > 128 ? 256 : (N > 64 ? 128 : 64);
         pl.split = 1;
+        // Splitting an operand in shared memory saves its pre-pass (12 bytes
+        // of HBM traffic per element) but slows the main loop by ~10 %; the
+        // pre-pass of A costs ~285/N of the tensor work (at the measured HBM
+        // and TF32 rates), so A is split in the kernel when N <= 2048, B when
+        // M <= 2048 (and only when the operand is K-contiguous, which
+        // run_tc checks).
+        pl.fuse_a = N <= 2048;
+        pl.fuse_b = M <= 2048;
         const int64_t tiles = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
         const int64_t slots = sms;
         const int64_t full = (tiles / slots) * slots;

@@ -9,7 +9,7 @@
 // tensor-core mode of "Optimising fp32 GEMM on A100", kernels 1-7, which
 // trade accuracy for speed).
 //
-// Kernel layout (one CTA per 128 x BN tile of C, 192 threads):
+// Kernel layout (one CTA per 128 x BN tile of C, 320 threads):
 //   warp 0, one lane : TMA producer - per k-block of 32 (128 bytes, the
 //                      128-byte swizzle span) loads A_hi/A_lo (128 x 32) and
 //                      B_hi/B_lo (BN x 32) into a ring of shared stages,
@@ -18,9 +18,11 @@
 //                      (M = 128, N = BN, K = 8) for each k-block and commits
 //                      them to the stage's "empty" mbarrier, then to the
 //                      "accumulator ready" mbarrier after the last block;
-//   warps 2..5       : epilogue - tcgen05.ld of the 128 x BN accumulator
-//                      (warp w reads TMEM lanes 32*(w%4)..+31 = its rows),
-//                      C = alpha*acc + beta*C, stores.
+//   warps 2..9       : while the main loop runs, split the operands that
+//                      were loaded raw (hi over the raw tile, lo beside it);
+//                      then the epilogue - tcgen05.ld of the 128 x BN
+//                      accumulator (warp w reads TMEM lanes 32*(w%4)..+31 =
+//                      its rows), C = alpha*acc + beta*C, stores.
 // The multi-stage ring is the asynchronous copy pipeline of "CuTe-ly
 // writing an SM86 SGEMM" (section "mainloop") and "Matmul II" (section 7)
 // rebuilt on TMA + mbarriers; the operand and accumulator placement is
@@ -49,7 +51,8 @@ constexpr int BM = 128;
 // of the MMA thread stays small against the tensor work).
 template <bool THREE> struct KBlock { static constexpr int BK = THREE ? 16 : 32; };
 constexpr int KPAD = 32;               // K padding of the split operands
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;               // 10 warps: TMA, MMA, 8 split/epilogue
+constexpr int WORKERS = THREADS - 64;      // split/epilogue threads (warps 2..9)
 constexpr int EPI_LD = 33;             // padded row of the epilogue staging tile
 constexpr int SMEM_LIMIT = 232448;     // opt-in dynamic shared memory per block
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
@@ -67,7 +70,7 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int PARTS = THREE ? 2 : 1;
     static constexpr int STAGE_BYTES = PARTS * (A_BYTES + B_BYTES);
-    static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;   // one 32 x 33 tile per epilogue warp
+    static constexpr int EPI_BYTES = (WORKERS / 32) * 32 * EPI_LD * 4;   // a 32 x 33 tile per epilogue warp
     static constexpr int BAR_BYTES = 256;
     static constexpr int FIXED = EPI_BYTES + BAR_BYTES + 1024;
     static constexpr int STAGES_RAW = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
@@ -91,6 +94,7 @@ struct Params {
     int dp_tiles;               // tiles computed at full width
     int tail_nsplit;            // 1, 2 or 4 column slices for the rest
     int num_kb;                 // k-blocks of BK
+    int fuse_a, fuse_b;         // operand loaded raw (fp32) and split in shared memory
     unsigned long long wait_ns; // bounded-wait limit
 };
 
@@ -102,6 +106,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
@@ -200,6 +208,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Round-to-nearest, ties away from zero, of an fp32 value to TF32 (10 stored
+// mantissa bits, the low 13 bits cleared), by the conversion instruction.
+__device__ __forceinline__ float tf32_round(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// In-place split of `n16` 16-byte groups of a shared tile: hi = round(x)
+// written over x, lo = round(x - hi) written to the twin tile (THREE only).
+// The WORKERS split threads stride through the tile together.
+template <bool THREE>
+__device__ __forceinline__ void split_tile(uint32_t hi, uint32_t lo, int n16, int ct) {
+    for (int i = ct; i < n16; i += WORKERS) {
+        float4 v;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(hi + 16u * i));
+        const float4 h = make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z),
+                                     tf32_round(v.w));
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(hi + 16u * i), "f"(h.x), "f"(h.y), "f"(h.z), "f"(h.w) : "memory");
+        if (THREE) {
+            const float4 l = make_float4(tf32_round(__fsub_rn(v.x, h.x)),
+                                         tf32_round(__fsub_rn(v.y, h.y)),
+                                         tf32_round(__fsub_rn(v.z, h.z)),
+                                         tf32_round(__fsub_rn(v.w, h.w)));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(lo + 16u * i), "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w) : "memory");
+        }
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group_m, int &tm,
                                        int &tn) {
@@ -228,13 +268,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     float *epi = reinterpret_cast<float *>(smem + K_::STAGES * K_::STAGE_BYTES);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_::STAGES * K_::STAGE_BYTES +
                                                   K_::EPI_BYTES);
-    // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * K_::STAGES + 1);
+    // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready,
+    // bars[2S+1 .. 3S+1) split done (operands loaded raw)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * K_::STAGES + 1);
     const uint32_t smem0 = smem_u32(smem);
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (K_::STAGES + s); };
     const uint32_t acc_bar = bar0 + 8u * (2 * K_::STAGES);
+    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * K_::STAGES + 1 + s); };
+    const bool fused = p.fuse_a || p.fuse_b;
     auto a_hi = [&](int s) { return smem0 + s * K_::STAGE_BYTES; };
     auto b_hi = [&](int s) { return a_hi(s) + K_::A_BYTES; };
     auto a_lo = [&](int s) { return b_hi(s) + K_::B_BYTES; };
@@ -259,12 +302,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int m0 = tm * BM, n0 = tn * BN + sub * bn;
     const CUtensorMap *mb_hi = nsub == 1 ? &tm_bhi : &tm_bhi_tail;
     const CUtensorMap *mb_lo = nsub == 1 ? &tm_blo : &tm_blo_tail;
-    const uint32_t stage_tx = (uint32_t)(K_::PARTS * (K_::A_BYTES + bn * BK * 4));
+    const uint32_t a_bytes = (uint32_t)K_::A_BYTES, b_bytes = (uint32_t)(bn * BK * 4);
+    const uint32_t stage_tx = (p.fuse_a ? a_bytes : K_::PARTS * a_bytes) +
+                              (p.fuse_b ? b_bytes : K_::PARTS * b_bytes);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < K_::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+            mbar_init(conv_bar(s), WORKERS / 32);      // one arrival per split warp
         }
         mbar_init(acc_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -300,12 +346,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) break;
                 mbar_expect_tx(full_bar(s), stage_tx);
                 const int kc = kb * BK;
+                // a fused operand arrives raw in its hi tile and is split there
                 tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, m0);
                 tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, n0);
-                if (THREE) {
-                    tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
-                    tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, n0);
-                }
+                if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
+                if (THREE && !p.fuse_b) tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, n0);
                 ++issued;
             }
             // drain: the last arming of each stage must have landed before exit
@@ -320,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % K_::STAGES;
                 const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
-                if (!mbar_wait(full_bar(s), ph, lim)) break;
+                if (!mbar_wait(fused ? conv_bar(s) : full_bar(s), ph, lim)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BK / 8; ++kk) {
@@ -346,20 +391,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        // Warp w owns TMEM lanes (= tile rows) 32*(w%4) .. +31.  Each 32 x 32
-        // block is read with tcgen05.ld (lane = row), turned around through a
-        // padded shared tile, then written row by row: every store
+        // ------------------------------------------------ epilogue (warps 2..9)
+        // Warp w owns TMEM lanes (= tile rows) 32*(w%4) .. +31, and of them
+        // every other 32-column block (two warps per lane quarter).  Each
+        // 32 x 32 block is read with tcgen05.ld (lane = row), turned around
+        // through a padded shared tile, then written row by row: every store
         // instruction of the warp covers 32 consecutive columns of one row.
         const int q = warp & 3;
-        float *stg = epi + q * 32 * EPI_LD;
+        const int half = (warp - 2) >> 2;
+        float *stg = epi + (warp - 2) * 32 * EPI_LD;
+        if (fused) {
+            // during the main loop these warps split the raw operand tiles
+            const int ct = threadIdx.x - 64;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % K_::STAGES;
+                const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
+                if (!mbar_wait(full_bar(s), ph, lim)) break;
+                if (p.fuse_a) split_tile<THREE>(a_hi(s), a_lo(s), K_::A_BYTES / 16, ct);
+                if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s), bn * BK * 4 / 16, ct);
+                // generic-proxy stores must be visible to the tensor core's reads
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(conv_bar(s));
+            }
+        }
         const bool ready = mbar_wait(acc_bar, 0u, lim);
         tc_fence_after();
         if (ready) {
             const float alpha = p.alpha, beta = p.beta;
             const int rows_here = min(32, p.M - (m0 + q * 32));
 #pragma unroll 1
-            for (int c = 0; c < bn / 32; ++c) {
+            for (int c = half; c < bn / 32; c += 2) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
 #pragma unroll
@@ -534,6 +596,24 @@ static int launch_main(const CUtensorMap *maps, const tc::Params &p, cudaStream_
     return last_status();
 }
 
+// 2-D map over a caller's K-contiguous fp32 operand (`rows` rows of K values,
+// row stride ld): box bk (k) x box_rows, swizzled like the split operands;
+// k past K and rows past `rows` read as zeros.
+static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int64_t ld,
+                         int box_rows, int bk) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+    cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               bk == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
            const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
            int64_t ldc, cudaStream_t s, int sms) {
@@ -541,40 +621,64 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     const bool three = pl.path == SGEMM_PATH_3XTF32;
     const int BN = pl.tile_n;
     const int Kp = (int)((K + tc::KPAD - 1) / tc::KPAD) * tc::KPAD;
+    // An operand whose rows already run along K in memory, 16-byte aligned
+    // with a leading dimension that is a multiple of 4, is read raw by TMA and
+    // split in shared memory; any other goes through the split pre-pass into
+    // the canonical K-contiguous workspace layout.
+    const bool fuse_a = pl.fuse_a && is_notrans(ta) && aligned16(A) && lda % 4 == 0;
+    const bool fuse_b = pl.fuse_b && !is_notrans(tb) && aligned16(B) && ldb % 4 == 0;
     auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
-    const size_t a_elems = up((size_t)M * Kp * 4) / 4;
-    const size_t b_elems = up((size_t)N * Kp * 4) / 4;
+    const size_t a_elems = fuse_a ? 0 : up((size_t)M * Kp * 4) / 4;
+    const size_t b_elems = fuse_b ? 0 : up((size_t)N * Kp * 4) / 4;
     const int parts = three ? 2 : 1;
-    void *ws = nullptr;
-    int st = workspace(s, (size_t)parts * (a_elems + b_elems) * 4, &ws);
-    if (st != SGEMM_OK) return st;
-    float *a_hi = static_cast<float *>(ws);
-    float *b_hi = a_hi + a_elems;
-    float *a_lo = three ? b_hi + b_elems : a_hi;
-    float *b_lo = three ? a_lo + a_elems : b_hi;
+    float *a_hi = nullptr, *b_hi = nullptr, *a_lo = nullptr, *b_lo = nullptr;
+    if (a_elems + b_elems > 0) {
+        void *ws = nullptr;
+        int st = workspace(s, (size_t)parts * (a_elems + b_elems) * 4, &ws);
+        if (st != SGEMM_OK) return st;
+        a_hi = static_cast<float *>(ws);
+        b_hi = a_hi + a_elems;
+        a_lo = three ? b_hi + b_elems : a_hi;
+        b_lo = three ? a_lo + a_elems : b_hi;
+    }
 
     // canonical K-major operands: A as [M][Kp], B as [N][Kp]
     const bool a_trans = !is_notrans(ta);   // A stored K x M
     const bool b_trans = is_notrans(tb);    // B stored K x N
-    if (three) {
-        launch_split<true>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, a_lo, s);
-        launch_split<true>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, b_lo, s);
-    } else {
-        launch_split<false>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, nullptr, s);
-        launch_split<false>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, nullptr, s);
+    if (!fuse_a) {
+        if (three) launch_split<true>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, a_lo, s);
+        else launch_split<false>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, nullptr, s);
     }
-    st = last_status();
+    if (!fuse_b) {
+        if (three) launch_split<true>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, b_lo, s);
+        else launch_split<false>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, nullptr, s);
+    }
+    int st = last_status();
     if (st != SGEMM_OK) return st;
 
     const int nsplit = std::max(1, pl.tail_nsplit);
     const int bk = three ? tc::KBlock<true>::BK : tc::KBlock<false>::BK;
     CUtensorMap maps[6];
-    if (!make_map(&maps[0], a_hi, (int)M, Kp, tc::BM, bk) ||
-        !make_map(&maps[1], a_lo, (int)M, Kp, tc::BM, bk) ||
-        !make_map(&maps[2], b_hi, (int)N, Kp, BN, bk) || !make_map(&maps[3], b_lo, (int)N, Kp, BN, bk) ||
-        !make_map(&maps[4], b_hi, (int)N, Kp, BN / nsplit, bk) ||
-        !make_map(&maps[5], b_lo, (int)N, Kp, BN / nsplit, bk))
-        return SGEMM_ERR_UNSUPPORTED;
+    bool ok;
+    if (fuse_a) {
+        ok = make_raw_map(&maps[0], A, (int)M, (int)K, lda, tc::BM, bk);
+        maps[1] = maps[0];
+    } else {
+        ok = make_map(&maps[0], a_hi, (int)M, Kp, tc::BM, bk) &&
+             make_map(&maps[1], a_lo, (int)M, Kp, tc::BM, bk);
+    }
+    if (fuse_b) {
+        ok = ok && make_raw_map(&maps[2], B, (int)N, (int)K, ldb, BN, bk) &&
+             make_raw_map(&maps[4], B, (int)N, (int)K, ldb, BN / nsplit, bk);
+        maps[3] = maps[2];
+        maps[5] = maps[4];
+    } else {
+        ok = ok && make_map(&maps[2], b_hi, (int)N, Kp, BN, bk) &&
+             make_map(&maps[3], b_lo, (int)N, Kp, BN, bk) &&
+             make_map(&maps[4], b_hi, (int)N, Kp, BN / nsplit, bk) &&
+             make_map(&maps[5], b_lo, (int)N, Kp, BN / nsplit, bk);
+    }
+    if (!ok) return SGEMM_ERR_UNSUPPORTED;
 
     tc::Params p{};
     p.C = C; p.ldc = ldc; p.M = (int)M; p.N = (int)N; p.K = (int)K;
@@ -585,6 +689,8 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.dp_tiles = std::min(pl.dp_tiles, p.tiles_m * p.tiles_n);
     p.tail_nsplit = nsplit;
     p.num_kb = Kp / bk;
+    p.fuse_a = fuse_a;
+    p.fuse_b = fuse_b;
     {
         std::lock_guard<std::mutex> lk(g_tc_mu);
         p.wait_ns = g_wait_ns;
