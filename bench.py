@@ -444,6 +444,39 @@ def gpu_arm(args):
     return 0
 
 
+def only_path(args):
+    """Profiling mode: W + K calls of one path on the workload, nothing else."""
+    import torch
+    import dense_fp32_gemm_05_gb300 as sg
+    from dense_fp32_gemm_05_gb300 import build as sgbuild
+
+    sgbuild.build()
+    sg.load()
+    w = gi.WORKLOADS[WORKLOAD]
+    A, B, _ = gi.make_inputs(w)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    pid = {"ffma": sg.PATH_FFMA, "3xtf32": sg.PATH_3XTF32, "tf32": sg.PATH_TF32}[args.only_path]
+    s = torch.cuda.current_stream()
+    ev = []
+    for i in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        st = sg.sgemm_ex(w.transA, w.transB, w.M, w.N, w.K, w.alpha, dA.data_ptr(), A.shape[1],
+                         dB.data_ptr(), B.shape[1], w.beta, dC.data_ptr(), w.N, s, pid, 0)
+        e1.record(s)
+        if st != 0:
+            raise sg.SgemmError(st)
+        if i >= args.warmup:
+            ev.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev) if ev else None
+    print(json.dumps({"mode": "only-path", "path": args.only_path, "workload": w.name,
+                      "calls": args.warmup + args.steps, "median_ms": ms,
+                      "tflops": (w.flops / ms / 1e9) if ms else None}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -455,10 +488,15 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--paths", default="ffma,3xtf32,tf32",
                     help="comma list of paths to time beside the main call")
+    ap.add_argument("--only-path", default=None, choices=["ffma", "3xtf32", "tf32"],
+                    help="profiling mode: run only W + K calls of this path on the "
+                         "workload (no baseline, e2e or oracle) and print their timing")
     ap.add_argument("--no-check", action="store_true", help="skip the oracle sample check")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.only_path:
+        return only_path(args)
     return gpu_arm(args)
 
 
