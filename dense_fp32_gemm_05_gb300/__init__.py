@@ -16,7 +16,7 @@ __all__ = [
     "SGEMM_OK", "SGEMM_ERR_CUDA", "SGEMM_ERR_TIMEOUT", "SGEMM_ERR_NOMEM",
     "SGEMM_ERR_UNSUPPORTED", "SGEMM_ERR_ARG", "SGEMM_ERR_SCRATCH", "PATH_AUTO", "PATH_FFMA",
     "PATH_3XTF32", "PATH_TF32", "SgemmError", "library_path", "load",
-    "sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string",
+    "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
     "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
     "sgemm_timing_read", "gemm", "exported_symbols",
@@ -60,6 +60,8 @@ def _declare(lib):
     lib.sgemm.restype = i32
     lib.sgemm_ex.argtypes = gemm_args + [i32, i32]
     lib.sgemm_ex.restype = i32
+    lib.sgemm_host.argtypes = gemm_args
+    lib.sgemm_host.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
     lib.sgemm_plan.argtypes = [c, c, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, i32, i32,
                                ip, ip, ip, ip, ip, ip]
@@ -100,7 +102,7 @@ def load():
 
 def exported_symbols(lib=None):
     """Names of the entry points this binding declares, for export checks."""
-    return ["sgemm", "sgemm_ex", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
+    return ["sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
             "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
             "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read"]
 
@@ -128,6 +130,13 @@ def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, strea
     """sgemm with the path and the FFMA split-K factor forced."""
     return load().sgemm_ex(_b(transA), _b(transB), M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                            _stream(stream), path, split)
+
+
+def sgemm_host(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """sgemm on HOST buffers (addresses as int), copies pipelined with the
+    computation; asynchronous on `stream` (page-locked buffers overlap)."""
+    return load().sgemm_host(_b(transA), _b(transB), M, N, K, alpha, A, lda, B, ldb, beta, C,
+                             ldc, _stream(stream))
 
 
 def sgemm_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned=True, b_aligned=True,

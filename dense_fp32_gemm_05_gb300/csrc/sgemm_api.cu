@@ -27,8 +27,19 @@ struct DeviceState {
 
 static std::mutex g_mu;
 static std::map<int, DeviceState> g_dev;
-// per (device, stream) workspace so that concurrent streams never share one
-static std::map<std::pair<int, cudaStream_t>, std::pair<void *, size_t>> g_ws;
+// per (device, stream, slot) workspace so that concurrent streams never share
+// one; slot 0 is the kernels' scratch, slot 1 the staging buffers of sgemm_host
+struct WsKey {
+    int dev;
+    cudaStream_t stream;
+    int slot;
+    bool operator<(const WsKey &o) const {
+        if (dev != o.dev) return dev < o.dev;
+        if (stream != o.stream) return stream < o.stream;
+        return slot < o.slot;
+    }
+};
+static std::map<WsKey, std::pair<void *, size_t>> g_ws;
 
 static int device_state(DeviceState **out) {
     int dev = 0;
@@ -46,13 +57,13 @@ static int device_state(DeviceState **out) {
     return SGEMM_OK;
 }
 
-// Returns a workspace of at least `bytes` private to (device, stream).  It is
-// allocated and, when it must grow, freed in stream order on `stream`.
-int workspace(cudaStream_t stream, size_t bytes, void **out) {
+// Returns a workspace of at least `bytes` private to (device, stream, slot).
+// It is allocated and, when it must grow, freed in stream order on `stream`.
+int workspace(cudaStream_t stream, size_t bytes, void **out, int which) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    auto &slot = g_ws[{dev, stream}];
+    auto &slot = g_ws[WsKey{dev, stream, which}];
     if (slot.second < bytes) {
         if (slot.first) cudaFreeAsync(slot.first, stream);
         slot = {nullptr, 0};
@@ -185,7 +196,7 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
     return st;
 }
 
-static int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
+int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
                      const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                      float *C, int64_t ldc, cudaStream_t s, int path, int split) {
     int st = check_args(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
@@ -331,7 +342,7 @@ extern "C" int sgemm_release_workspace(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto it = g_ws.begin(); it != g_ws.end();) {
-        if (it->first.first == dev) {
+        if (it->first.dev == dev) {
             if (it->second.first) cudaFree(it->second.first);
             it = g_ws.erase(it);
         } else {

@@ -24,7 +24,12 @@ void tc_set_wait_limit(uint64_t ns);
 // kernel launch on `s` when timing is enabled (no-op otherwise).
 void timing_mark(cudaStream_t s, bool begin);
 
-// Library-owned per-(device, stream) workspace, grown on demand.
-int workspace(cudaStream_t stream, size_t bytes, void **out);
+// Library-owned per-(device, stream, slot) workspace, grown on demand.
+int workspace(cudaStream_t stream, size_t bytes, void **out, int which = 0);
+
+// The whole device-pointer GEMM call (checks, quick returns, selector, launch).
+int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+              int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+              cudaStream_t s, int path, int split);
 
 }  // namespace sgemm_gb300

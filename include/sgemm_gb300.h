@@ -115,6 +115,26 @@ int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
              int path, int split);
 
 /*
+ * sgemm_host - the same operation on HOST buffers (same arguments and
+ * conventions as sgemm, but A, B and C point to host memory).  The library
+ * cuts K into up to 4 chunks, uploads each chunk's slices of A and B (after
+ * C when beta != 0) on an internal stream while the previous chunks'
+ * GEMMs run, accumulates the chunks into C on the device (one extra fp32
+ * rounding of C per chunk), runs the last chunk in row blocks and downloads
+ * each block of C on a second internal stream as soon as it is final.
+ * Asynchronous on `stream`: C is complete once `stream` has synchronised.
+ * For the copies to overlap and to run at full speed A, B and C must be
+ * page-locked (cudaHostAlloc / cudaHostRegister); pageable buffers work but
+ * their copies serialise.  Device staging buffers (4*(M*K + K*N + M*N)
+ * bytes) are library-owned per (device, stream) like the workspace.
+ * Returns as sgemm.
+ */
+int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
+               float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc, sgemm_stream_t stream);
+
+/*
  * sgemm_plan - the selector's decision for a problem, without launching
  * anything and without touching the GPU.  `path` and `split` as in
  * sgemm_ex (0 = let the selector decide); num_sms is the GPU's SM count.
