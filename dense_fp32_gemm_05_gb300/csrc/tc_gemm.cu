@@ -76,7 +76,9 @@ struct Cfg {
     static constexpr int STAGES_RAW = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
-    static constexpr uint32_t TMEM_COLS = BN;            // power of two >= 32
+    // two accumulators (double-buffered TMEM) when they fit in the 512 columns
+    static constexpr int NBUF = 2;
+    static constexpr uint32_t TMEM_COLS = NBUF * BN;     // power of two <= 512
     static_assert(STAGES >= 2, "need at least two stages");
     static_assert(BN == 64 || BN == 128 || BN == 256, "N of the MMA");
 };
@@ -95,6 +97,7 @@ struct Params {
     int tail_nsplit;            // 1, 2 or 4 column slices for the rest
     int num_kb;                 // k-blocks of BK
     int fuse_a, fuse_b;         // operand loaded raw (fp32) and split in shared memory
+    int units;                  // dp_tiles + (tiles - dp_tiles) * tail_nsplit
     unsigned long long wait_ns; // bounded-wait limit
 };
 
@@ -252,6 +255,31 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
     tn = r / gm;
 }
 
+// Decodes unit u: whole tiles first, then the last-wave tiles' column slices.
+__device__ __forceinline__ void unit_of(const Params &p, int BN_, int u, int &m0, int &n0,
+                                        int &bn, int &nsub) {
+    int tile, sub = 0;
+    nsub = 1;
+    if (u < p.dp_tiles) {
+        tile = u;
+    } else {
+        const int v = u - p.dp_tiles;
+        nsub = p.tail_nsplit;
+        tile = p.dp_tiles + v / nsub;
+        sub = v % nsub;
+    }
+    int tm, tn;
+    raster(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    bn = BN_ / nsub;
+    m0 = tm * BM;
+    n0 = tn * BN_ + sub * bn;
+}
+
+// Persistent over units: CTA c handles units c, c + gridDim.x, ...  The
+// k-block stream of the TMA producer and of the MMA issuer runs on across
+// units (stage and phase from a per-CTA k-block counter), and the two TMEM
+// accumulators alternate between units, so the epilogue of one unit overlaps
+// the main loop of the next.
 template <int BN, bool THREE>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi,
@@ -262,63 +290,50 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_blo_tail, const Params p) {
     using K_ = Cfg<BN, THREE>;
     constexpr int BK = K_::BK;
+    constexpr int NW = WORKERS / 32;                   // split / epilogue warps
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *epi = reinterpret_cast<float *>(smem + K_::STAGES * K_::STAGE_BYTES);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_::STAGES * K_::STAGE_BYTES +
                                                   K_::EPI_BYTES);
-    // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready,
-    // bars[2S+1 .. 3S+1) split done (operands loaded raw)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * K_::STAGES + 1);
+    // bars[0..S) full, [S..2S) empty, [2S..3S) split done, [3S, 3S+2) accumulator
+    // full, [3S+2, 3S+4) accumulator empty
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * K_::STAGES + 4);
     const uint32_t smem0 = smem_u32(smem);
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (K_::STAGES + s); };
-    const uint32_t acc_bar = bar0 + 8u * (2 * K_::STAGES);
-    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * K_::STAGES + 1 + s); };
-    const bool fused = p.fuse_a || p.fuse_b;
+    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * K_::STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * K_::STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * K_::STAGES + 2 + b); };
     auto a_hi = [&](int s) { return smem0 + s * K_::STAGE_BYTES; };
     auto b_hi = [&](int s) { return a_hi(s) + K_::A_BYTES; };
     auto a_lo = [&](int s) { return b_hi(s) + K_::B_BYTES; };
     auto b_lo = [&](int s) { return a_lo(s) + K_::A_BYTES; };
+    const bool fused = p.fuse_a || p.fuse_b;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- this CTA's unit of work
-    int tile, sub = 0, nsub = 1;
-    if ((int)blockIdx.x < p.dp_tiles) {
-        tile = blockIdx.x;
-    } else {
-        const int u = blockIdx.x - p.dp_tiles;
-        nsub = p.tail_nsplit;
-        tile = p.dp_tiles + u / nsub;
-        sub = u % nsub;
-    }
-    int tm, tn;
-    raster(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int bn = BN / nsub;                          // columns of this unit
-    const int m0 = tm * BM, n0 = tn * BN + sub * bn;
-    const CUtensorMap *mb_hi = nsub == 1 ? &tm_bhi : &tm_bhi_tail;
-    const CUtensorMap *mb_lo = nsub == 1 ? &tm_blo : &tm_blo_tail;
-    const uint32_t a_bytes = (uint32_t)K_::A_BYTES, b_bytes = (uint32_t)(bn * BK * 4);
-    const uint32_t stage_tx = (p.fuse_a ? a_bytes : K_::PARTS * a_bytes) +
-                              (p.fuse_b ? b_bytes : K_::PARTS * b_bytes);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < K_::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(conv_bar(s), WORKERS / 32);      // one arrival per split warp
+            mbar_init(conv_bar(s), NW);                // one arrival per split warp
         }
-        mbar_init(acc_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);                 // tcgen05.commit
+            mbar_init(acce_bar(b), NW);                // one arrival per epilogue warp
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tm_ahi);
-        prefetch_map(mb_hi);
+        prefetch_map(&tm_bhi);
+        prefetch_map(&tm_bhi_tail);
         if (THREE) {
             prefetch_map(&tm_alo);
-            prefetch_map(mb_lo);
+            prefetch_map(&tm_blo);
+            prefetch_map(&tm_blo_tail);
         }
     }
     if (warp == 1) {
@@ -339,59 +354,84 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % K_::STAGES;
-                const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) break;
-                mbar_expect_tx(full_bar(s), stage_tx);
-                const int kc = kb * BK;
-                // a fused operand arrives raw in its hi tile and is split there
-                tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, m0);
-                tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, n0);
-                if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
-                if (THREE && !p.fuse_b) tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, n0);
-                ++issued;
+            int64_t g = 0;                             // k-blocks issued by this CTA
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                int m0, n0, bn, nsub;
+                unit_of(p, BN, u, m0, n0, bn, nsub);
+                const CUtensorMap *mb_hi = nsub == 1 ? &tm_bhi : &tm_bhi_tail;
+                const CUtensorMap *mb_lo = nsub == 1 ? &tm_blo : &tm_blo_tail;
+                const uint32_t a_bytes = (uint32_t)K_::A_BYTES, b_bytes = (uint32_t)(bn * BK * 4);
+                const uint32_t tx = (p.fuse_a ? a_bytes : K_::PARTS * a_bytes) +
+                                    (p.fuse_b ? b_bytes : K_::PARTS * b_bytes);
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const int s = (int)(g % K_::STAGES);
+                    const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) { ok = false; break; }
+                    mbar_expect_tx(full_bar(s), tx);
+                    const int kc = kb * BK;
+                    // a fused operand arrives raw in its hi tile and is split there
+                    tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, m0);
+                    tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, n0);
+                    if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
+                    if (THREE && !p.fuse_b) tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, n0);
+                }
             }
             // drain: the last arming of each stage must have landed before exit
-            for (int kb = (issued > K_::STAGES ? issued - K_::STAGES : 0); kb < issued; ++kb)
-                mbar_wait(full_bar(kb % K_::STAGES), (uint32_t)(kb / K_::STAGES) & 1u, kDrainNs);
+            for (int64_t q = (g > K_::STAGES ? g - K_::STAGES : 0); q < g; ++q)
+                mbar_wait(full_bar((int)(q % K_::STAGES)), (uint32_t)(q / K_::STAGES) & 1u,
+                          kDrainNs);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_tf32(bn);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % K_::STAGES;
-                const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
-                if (!mbar_wait(fused ? conv_bar(s) : full_bar(s), ph, lim)) break;
+            int64_t g = 0;
+            int j = 0;                                 // units done by this CTA
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++j) {
+                int m0, n0, bn, nsub;
+                unit_of(p, BN, u, m0, n0, bn, nsub);
+                const int b = j & 1;
+                // the epilogue must have emptied this accumulator (unit j - 2)
+                if (!mbar_wait(acce_bar(b), ((uint32_t)(j >> 1) & 1u) ^ 1u, lim)) break;
                 tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * BN);
+                const uint32_t idesc = idesc_tf32(bn);
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const int s = (int)(g % K_::STAGES);
+                    const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
+                    if (!mbar_wait(fused ? conv_bar(s) : full_bar(s), ph, lim)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BK / 8; ++kk) {
-                    const uint32_t off = kk * 32;            // 8 tf32 = 32 bytes
-                    const uint64_t ah = smem_desc<BK * 4>(a_hi(s) + off);
-                    const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
-                    const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
-                    if (THREE) {
-                        const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
-                        const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
-                        umma_tf32(tmem, al, bh, idesc, first);
-                        umma_tf32(tmem, ah, bl, idesc, 1u);
-                        umma_tf32(tmem, ah, bh, idesc, 1u);
-                    } else {
-                        umma_tf32(tmem, ah, bh, idesc, first);
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        const uint32_t off = kk * 32;            // 8 tf32 = 32 bytes
+                        const uint64_t ah = smem_desc<BK * 4>(a_hi(s) + off);
+                        const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
+                        const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                        if (THREE) {
+                            const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
+                            const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
+                            umma_tf32(d, al, bh, idesc, first);
+                            umma_tf32(d, ah, bl, idesc, 1u);
+                            umma_tf32(d, ah, bh, idesc, 1u);
+                        } else {
+                            umma_tf32(d, ah, bh, idesc, first);
+                        }
                     }
+                    umma_commit(empty_bar(s));
                 }
-                umma_commit(empty_bar(s));
+                umma_commit(accf_bar(b));              // this unit's accumulator is ready
             }
-            umma_commit(acc_bar);
             // all MMAs of this CTA retired before TMEM can be freed
-            mbar_wait(acc_bar, 0u, kDrainNs);
+            if (j > 0) {
+                const int b = (j - 1) & 1;
+                mbar_wait(accf_bar(b), (uint32_t)((j - 1) >> 1) & 1u, kDrainNs);
+            }
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2..9)
+        // ------------------------------------------------ split + epilogue (warps 2..9)
         // Warp w owns TMEM lanes (= tile rows) 32*(w%4) .. +31, and of them
         // every other 32-column block (two warps per lane quarter).  Each
         // 32 x 32 block is read with tcgen05.ld (lane = row), turned around
@@ -400,32 +440,40 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         float *stg = epi + (warp - 2) * 32 * EPI_LD;
-        if (fused) {
-            // during the main loop these warps split the raw operand tiles
-            const int ct = threadIdx.x - 64;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % K_::STAGES;
-                const uint32_t ph = (uint32_t)(kb / K_::STAGES) & 1u;
-                if (!mbar_wait(full_bar(s), ph, lim)) break;
-                if (p.fuse_a) split_tile<THREE>(a_hi(s), a_lo(s), K_::A_BYTES / 16, ct);
-                if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s), bn * BK * 4 / 16, ct);
-                // generic-proxy stores must be visible to the tensor core's reads
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(conv_bar(s));
+        const int ct = threadIdx.x - 64;
+        int64_t g = 0;
+        int j = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++j) {
+            int m0, n0, bn, nsub;
+            unit_of(p, BN, u, m0, n0, bn, nsub);
+            if (fused) {
+                // during the main loop these warps split the raw operand tiles
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const int s = (int)(g % K_::STAGES);
+                    const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, lim)) { ok = false; break; }
+                    if (p.fuse_a) split_tile<THREE>(a_hi(s), a_lo(s), K_::A_BYTES / 16, ct);
+                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s), bn * BK * 4 / 16, ct);
+                    // generic-proxy stores must be visible to the tensor core's reads
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(conv_bar(s));
+                }
+                if (!ok) break;
             }
-        }
-        const bool ready = mbar_wait(acc_bar, 0u, lim);
-        tc_fence_after();
-        if (ready) {
+            const int b = j & 1;
+            const bool ready = mbar_wait(accf_bar(b), (uint32_t)(j >> 1) & 1u, lim);
+            tc_fence_after();
+            if (!ready) break;
             const float alpha = p.alpha, beta = p.beta;
             const int rows_here = min(32, p.M - (m0 + q * 32));
 #pragma unroll 1
             for (int c = half; c < bn / 32; c += 2) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) stg[lane * EPI_LD + j] = __uint_as_float(r[j]);
+                for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = __uint_as_float(r[jj]);
                 __syncwarp();
                 const int col = n0 + c * 32 + lane;
                 if (col < p.N) {
@@ -449,6 +497,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();
             }
+            // this warp has read its part of accumulator b: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(b));
         }
     }
 
@@ -573,7 +625,7 @@ static void launch_split(const float *src, int64_t ld, bool trans, int rows, int
 }
 
 template <int BN, bool THREE>
-static int launch_main(const CUtensorMap *maps, const tc::Params &p, cudaStream_t s) {
+static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, cudaStream_t s) {
     using K_ = tc::Cfg<BN, THREE>;
     // the shared-memory opt-in is a per-device function attribute
     static uint64_t attr_done = 0;   // bit d: set on device d
@@ -587,8 +639,6 @@ static int launch_main(const CUtensorMap *maps, const tc::Params &p, cudaStream_
             return last_status();
         __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
     }
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int grid = p.dp_tiles + (tiles - p.dp_tiles) * p.tail_nsplit;
     timing_mark(s, true);
     tc::tc_gemm_kernel<BN, THREE><<<grid, tc::THREADS, K_::SMEM, s>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
@@ -617,7 +667,6 @@ static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int
 int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
            const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
            int64_t ldc, cudaStream_t s, int sms) {
-    (void)sms;
     const bool three = pl.path == SGEMM_PATH_3XTF32;
     const int BN = pl.tile_n;
     const int Kp = (int)((K + tc::KPAD - 1) / tc::KPAD) * tc::KPAD;
@@ -691,13 +740,19 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.num_kb = Kp / bk;
     p.fuse_a = fuse_a;
     p.fuse_b = fuse_b;
+    p.units = p.dp_tiles + (p.tiles_m * p.tiles_n - p.dp_tiles) * nsplit;
     {
         std::lock_guard<std::mutex> lk(g_tc_mu);
         p.wait_ns = g_wait_ns;
     }
-    if (BN == 256) return three ? launch_main<256, true>(maps, p, s) : launch_main<256, false>(maps, p, s);
-    if (BN == 128) return three ? launch_main<128, true>(maps, p, s) : launch_main<128, false>(maps, p, s);
-    return three ? launch_main<64, true>(maps, p, s) : launch_main<64, false>(maps, p, s);
+    // Persistent (one CTA per SM walking the units, epilogue of one unit
+    // under the main loop of the next) unless an operand is split in the
+    // kernel: the split warps are also the epilogue warps, so those CTAs take
+    // one unit each.
+    const int grid = (fuse_a || fuse_b) ? p.units : std::min(p.units, std::max(sms, 1));
+    if (BN == 256) return three ? launch_main<256, true>(maps, p, grid, s) : launch_main<256, false>(maps, p, grid, s);
+    if (BN == 128) return three ? launch_main<128, true>(maps, p, grid, s) : launch_main<128, false>(maps, p, grid, s);
+    return three ? launch_main<64, true>(maps, p, grid, s) : launch_main<64, false>(maps, p, grid, s);
 }
 
 }  // namespace sgemm_gb300
