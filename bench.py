@@ -118,6 +118,25 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
+def job_throughput(local_ms: float, steps: int, flops_per_step: float, device=None):
+    """(max over ranks of the timed milliseconds, whole-job TFLOP/s).
+
+    Every rank runs an independent replica of the step; the job takes as long
+    as its slowest rank, and it did world * steps steps in that time.  Works
+    with any torch.distributed backend (NCCL on GPUs, gloo in the CPU tests);
+    without an initialised process group it is the single-rank value.
+    """
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    t = float(local_ms)
+    if world > 1:
+        x = torch.tensor([t], dtype=torch.float64, device=device)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        t = float(x.item())
+    return t, world * steps * flops_per_step / (t / 1e3) / 1e12
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -293,29 +312,23 @@ def gpu_arm(args):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sg.sgemm_timing_read(args.steps)
     sg.sgemm_timing_enable(0)
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = job_throughput(sum(step_ms), args.steps, w.flops, device=dev)
     ms_per_step = total_ms / args.steps
-    value = world * args.steps * w.flops / (total_ms / 1e3) / 1e12
     clocks = sampler.summary()
 
     # ---- plan of the timed call: which kernels ran
     st, plan = sg.sgemm_plan(w.transA, w.transB, w.M, w.N, w.K, lda, ldb, ldc, True, True, True,
                              sg.PATH_AUTO, 0, sms)
     # our kernels per timed call: FFMA (+ fixup when tiles are shared); tensor
-    # cores: the main kernel + one split pre-pass per operand not split in it
-    # (A in the kernel when N <= 2048 and A is K-contiguous, B when M <= 2048
-    # and B is K-contiguous; see the selector)
+    # cores: the main kernel + one split pre-pass launch unless both operands
+    # are split in it (A in the kernel when N <= 2048 and A is K-contiguous,
+    # B when M <= 2048 and B is K-contiguous; see the selector)
     if plan["path"] == sg.PATH_FFMA:
         launches_per_step = 1 + (1 if plan["split"] > 1 else 0)
     else:
         fuse_a = w.N <= 2048 and w.transA.upper() == "N"
         fuse_b = w.M <= 2048 and w.transB.upper() == "T"
-        launches_per_step = 1 + (0 if fuse_a else 1) + (0 if fuse_b else 1)
+        launches_per_step = 1 + (0 if (fuse_a and fuse_b) else 1)
 
     # ---- per-path timings on the same workload (outside the timed region)
     peaks, peak_src = measured_peaks()

@@ -520,37 +520,84 @@ __device__ __forceinline__ float rna_tf32(float x) {
     return __uint_as_float(r);
 }
 
-// out[r][k] (r < rows, k < Kp, row stride Kp) = op value at (r, k) for k < K,
-// 0 for K <= k < Kp; hi = rna_tf32(x), lo = rna_tf32(x - hi).
-// TRANS: the source is stored k-major (src[k*ld + r]), else src[r*ld + k].
-// 32 x 32 tiles through shared memory so reads and writes are both coalesced.
-template <bool TRANS, bool THREE>
-__global__ void __launch_bounds__(256)
-    split_kernel(const float *__restrict__ src, int64_t ld, int rows, int K, int Kp,
-                 float *__restrict__ hi, float *__restrict__ lo) {
+// One operand of the split pre-pass: out[r][k] (r < rows, k < Kp, row stride
+// Kp) = op value at (r, k) for k < K, 0 for K <= k < Kp; hi = rna_tf32(x),
+// lo = rna_tf32(x - hi).  trans: the source is stored k-major
+// (src[k*ld + r]), else src[r*ld + k]; vec: the source rows are 16-byte
+// aligned (base aligned, ld % 4 == 0).
+struct SplitJob {
+    const float *src;
+    int64_t ld;
+    int rows, K, Kp;
+    float *hi, *lo;
+    int trans, vec;
+    int blocks;                 // CTAs of this job
+};
+
+__host__ __device__ inline int split_blocks(int rows, int Kp, bool trans) {
+    // transposed: one 32 x 32 tile per CTA; direct: 1024 float4 per CTA
+    return trans ? (Kp / 32) * ((rows + 31) / 32)
+                 : (int)(((int64_t)rows * (Kp / 4) + 1023) / 1024);
+}
+
+template <bool THREE>
+__device__ __forceinline__ void split_store4(const SplitJob &j, int64_t o, float4 x) {
+    const float4 h = make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
+    *reinterpret_cast<float4 *>(j.hi + o) = h;
+    if (THREE)
+        *reinterpret_cast<float4 *>(j.lo + o) =
+            make_float4(rna_tf32(__fsub_rn(x.x, h.x)), rna_tf32(__fsub_rn(x.y, h.y)),
+                        rna_tf32(__fsub_rn(x.z, h.z)), rna_tf32(__fsub_rn(x.w, h.w)));
+}
+
+// Both operands in one launch: CTAs [0, j0.blocks) do j0, the rest j1.
+// The direct case streams float4 groups (16-byte loads where the source
+// allows, always 16-byte stores); the transposed case turns 32 x 32 tiles
+// around through shared memory so that reads and writes are both coalesced.
+template <bool THREE>
+__global__ void __launch_bounds__(256) split_pair_kernel(const SplitJob j0, const SplitJob j1) {
     __shared__ float tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-    const int k0 = blockIdx.x * 32;
-    const int r0 = blockIdx.y * 32;
-    if (TRANS) {
+    const bool second = (int)blockIdx.x >= j0.blocks;
+    const SplitJob &j = second ? j1 : j0;
+    const int b = second ? (int)blockIdx.x - j0.blocks : (int)blockIdx.x;
+    if (j.trans) {
+        const int tiles_k = j.Kp / 32;
+        const int k0 = (b % tiles_k) * 32, r0 = (b / tiles_k) * 32;
+        const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int k = k0 + ty + 8 * i, r = r0 + tx;
-            tile[ty + 8 * i][tx] = (k < K && r < rows) ? src[(int64_t)k * ld + r] : 0.0f;
+            tile[ty + 8 * i][tx] = (k < j.K && r < j.rows) ? j.src[(int64_t)k * j.ld + r] : 0.0f;
         }
         __syncthreads();
+        // each thread then writes a float4 of one output row
+        const int r = r0 + (threadIdx.x >> 3), kq = (threadIdx.x & 7) * 4;
+        if (r < j.rows) {
+            const float4 x = make_float4(tile[kq][r - r0], tile[kq + 1][r - r0],
+                                         tile[kq + 2][r - r0], tile[kq + 3][r - r0]);
+            split_store4<THREE>(j, (int64_t)r * j.Kp + k0 + kq, x);
+        }
+        return;
     }
+    const int64_t per_row = j.Kp / 4;
+    const int64_t total = (int64_t)j.rows * per_row;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int r = r0 + ty + 8 * i, k = k0 + tx;
-        if (r >= rows) continue;
-        float x;
-        if (TRANS) x = tile[tx][ty + 8 * i];
-        else x = (k < K) ? src[(int64_t)r * ld + k] : 0.0f;
-        const float h = rna_tf32(x);
-        const int64_t o = (int64_t)r * Kp + k;
-        hi[o] = h;
-        if (THREE) lo[o] = rna_tf32(__fsub_rn(x, h));
+        const int64_t g = (int64_t)b * 1024 + i * 256 + threadIdx.x;
+        if (g >= total) break;
+        const int64_t r = g / per_row;
+        const int k = (int)(g - r * per_row) * 4;
+        const float *src = j.src + r * j.ld + k;
+        float4 x;
+        if (j.vec && k + 3 < j.K) {
+            x = __ldg(reinterpret_cast<const float4 *>(src));
+        } else {
+            x.x = k < j.K ? __ldg(src) : 0.0f;
+            x.y = k + 1 < j.K ? __ldg(src + 1) : 0.0f;
+            x.z = k + 2 < j.K ? __ldg(src + 2) : 0.0f;
+            x.w = k + 3 < j.K ? __ldg(src + 3) : 0.0f;
+        }
+        split_store4<THREE>(j, r * j.Kp + k, x);
     }
 }
 
@@ -616,12 +663,23 @@ static int last_status() {
     return SGEMM_ERR_CUDA;
 }
 
-template <bool THREE>
-static void launch_split(const float *src, int64_t ld, bool trans, int rows, int K, int Kp,
-                         float *hi, float *lo, cudaStream_t s) {
-    dim3 grid(Kp / 32, (rows + 31) / 32);
-    if (trans) tc::split_kernel<true, THREE><<<grid, 256, 0, s>>>(src, ld, rows, K, Kp, hi, lo);
-    else tc::split_kernel<false, THREE><<<grid, 256, 0, s>>>(src, ld, rows, K, Kp, hi, lo);
+static tc::SplitJob split_job(const float *src, int64_t ld, bool trans, int rows, int K, int Kp,
+                              float *hi, float *lo) {
+    tc::SplitJob j{};
+    j.src = src; j.ld = ld; j.rows = rows; j.K = K; j.Kp = Kp; j.hi = hi; j.lo = lo;
+    j.trans = trans;
+    j.vec = aligned16(src) && ld % 4 == 0;
+    j.blocks = rows > 0 ? tc::split_blocks(rows, Kp, trans) : 0;
+    return j;
+}
+
+// One launch for the operands that need the pre-pass (either may be absent).
+static void launch_split_pair(bool three, const tc::SplitJob &a, const tc::SplitJob &b,
+                              cudaStream_t s) {
+    const int blocks = a.blocks + b.blocks;
+    if (blocks == 0) return;
+    if (three) tc::split_pair_kernel<true><<<blocks, 256, 0, s>>>(a, b);
+    else tc::split_pair_kernel<false><<<blocks, 256, 0, s>>>(a, b);
 }
 
 template <int BN, bool THREE>
@@ -694,14 +752,10 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // canonical K-major operands: A as [M][Kp], B as [N][Kp]
     const bool a_trans = !is_notrans(ta);   // A stored K x M
     const bool b_trans = is_notrans(tb);    // B stored K x N
-    if (!fuse_a) {
-        if (three) launch_split<true>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, a_lo, s);
-        else launch_split<false>(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, nullptr, s);
-    }
-    if (!fuse_b) {
-        if (three) launch_split<true>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, b_lo, s);
-        else launch_split<false>(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, nullptr, s);
-    }
+    tc::SplitJob ja{}, jb{};
+    if (!fuse_a) ja = split_job(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, three ? a_lo : nullptr);
+    if (!fuse_b) jb = split_job(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, three ? b_lo : nullptr);
+    launch_split_pair(three, ja, jb, s);
     int st = last_status();
     if (st != SGEMM_OK) return st;
 
