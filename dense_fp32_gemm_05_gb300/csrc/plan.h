@@ -52,13 +52,13 @@ struct Plan {
     int tail_nsplit = 1;  // tensor cores: column slices of the last-wave tiles
     int fuse_a = 1;       // tensor cores: split A in shared memory when its layout allows
     int fuse_b = 1;       // tensor cores: same for B
+    int pair = 0;         // tensor cores: 256-row tiles on a pair of SMs (cta_group::2)
 };
 
 // Chooses path, tile, split and vectorisation.  `path`/`split` 0 = auto.
 inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda,
                      int64_t ldb, int64_t ldc, bool a_al, bool b_al, bool c_al, int path,
                      int split, int sms, Plan *out) {
-    (void)ta; (void)tb;
     Plan pl;
     if (path == SGEMM_PATH_AUTO) {
         // 3xTF32 runs the tensor cores at 3 MMAs per product and beats the
@@ -118,12 +118,18 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // of HBM traffic per element) but slows the main loop by ~10 %; the
         // pre-pass of A costs ~285/N of the tensor work (at the measured HBM
         // and TF32 rates), so A is split in the kernel when N <= 2048, B when
-        // M <= 2048 (and only when the operand is K-contiguous, which
-        // run_tc checks).
-        pl.fuse_a = N <= 2048;
-        pl.fuse_b = M <= 2048;
-        const int64_t tiles = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
-        const int64_t slots = sms;
+        // M <= 2048, and only when the operand is K-contiguous and 16-byte
+        // aligned (TMA reads it raw).
+        pl.fuse_a = N <= 2048 && is_notrans(ta) && a_al && lda % 4 == 0;
+        pl.fuse_b = M <= 2048 && is_trans(tb) && b_al && ldb % 4 == 0;
+        // 256-row tiles on an SM pair when both operands come pre-split and
+        // M fills them: each SM holds half of B, a third less shared-memory
+        // traffic per flop (+6 % at 4096^3 and 8192^3 on GB300).  With an
+        // operand split in shared memory the pair measured 2-4 % slower.
+        pl.pair = (M > 128 && !pl.fuse_a && !pl.fuse_b) ? 1 : 0;
+        pl.tile_m = pl.pair ? 256 : 128;
+        const int64_t tiles = ((M + pl.tile_m - 1) / pl.tile_m) * ((N + pl.tile_n - 1) / pl.tile_n);
+        const int64_t slots = pl.pair ? std::max(sms / 2, 1) : sms;
         const int64_t full = (tiles / slots) * slots;
         const int64_t tail = tiles - full;
         double best = (double)((tiles + slots - 1) / slots);

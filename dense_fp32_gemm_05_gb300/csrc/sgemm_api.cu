@@ -265,8 +265,15 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
         if (pl.path == SGEMM_PATH_FFMA) {
             *out_ctas = pl.dp_tiles + pl.ctas;
         } else {
-            const int64_t tiles = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
-            *out_ctas = (int)(pl.dp_tiles + (tiles - pl.dp_tiles) * pl.tail_nsplit);
+            // units of work; one CTA each (two for SM pairs), or one CTA (pair)
+            // per SM (pair) walking them when no operand is split in the kernel
+            const int64_t tiles = ((M + pl.tile_m - 1) / pl.tile_m) * ((N + pl.tile_n - 1) / pl.tile_n);
+            const int64_t units = pl.dp_tiles + (tiles - pl.dp_tiles) * pl.tail_nsplit;
+            const bool fa = pl.fuse_a && is_notrans(transA) && a_aligned && lda % 4 == 0;
+            const bool fb = pl.fuse_b && !is_notrans(transB) && b_aligned && ldb % 4 == 0;
+            const int64_t slots = pl.pair ? std::max(num_sms / 2, 1) : num_sms;
+            const int64_t groups = (fa || fb) ? units : std::min<int64_t>(units, slots);
+            *out_ctas = (int)(groups * (pl.pair ? 2 : 1));
         }
     }
     return SGEMM_OK;

@@ -63,15 +63,18 @@ constexpr uint64_t kDrainNs = 1000000000ull;         // 1 s
 
 __device__ unsigned int g_error;        // sticky device error word (per device)
 
-template <int BN, bool THREE>
+// PAIR: a cluster of two CTAs on two SMs computes a 256 x BN tile with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA holds its 128 rows of A and
+// half (BN / 2 columns) of B, and its 128 rows of the accumulator.
+template <int BN, bool THREE, bool PAIR = false>
 struct Cfg {
     static constexpr int BK = KBlock<THREE>::BK;
     static constexpr int A_BYTES = BM * BK * 4;
-    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 4;
     static constexpr int PARTS = THREE ? 2 : 1;
     static constexpr int STAGE_BYTES = PARTS * (A_BYTES + B_BYTES);
     static constexpr int EPI_BYTES = (WORKERS / 32) * 32 * EPI_LD * 4;   // a 32 x 33 tile per epilogue warp
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int FIXED = EPI_BYTES + BAR_BYTES + 1024;
     static constexpr int STAGES_RAW = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -195,6 +198,83 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                  :: "r"(bar) : "memory");
 }
 
+// ---- two-CTA (cluster pair) forms
+__device__ __forceinline__ void umma_tf32_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Arrives on the barrier at the same offset in both CTAs of the pair once
+// this thread's earlier pair MMAs have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" :: "r"(bar), "h"((uint16_t)3) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The address of a local shared variable in the leader CTA (rank 0) of the pair.
+__device__ __forceinline__ uint32_t leader_addr(uint32_t local) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(local));
+    return r;
+}
+
+// Arrive with release at cluster scope: the once-per-tile hand-back of an
+// accumulator, ordering this warp's TMEM reads before the leader's next MMAs.
+// (Such a release stalls the thread for about an L2 round trip, longer than
+// a stage's MMAs, so nothing per stage goes through a thread's arrive: the
+// peer's TMA loads count their bytes on the leader's barrier directly.)
+__device__ __forceinline__ void remote_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion (bytes) is counted
+// on a barrier of the pair given by its cluster address (the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a barrier that the peer CTA also arrives on (cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_cluster(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicExch(&g_error, (unsigned)SGEMM_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit accumulators -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -256,7 +336,8 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
 }
 
 // Decodes unit u: whole tiles first, then the last-wave tiles' column slices.
-__device__ __forceinline__ void unit_of(const Params &p, int BN_, int u, int &m0, int &n0,
+// TM rows per tile (128, or 256 for a CTA pair).
+__device__ __forceinline__ void unit_of(const Params &p, int TM, int BN_, int u, int &m0, int &n0,
                                         int &bn, int &nsub) {
     int tile, sub = 0;
     nsub = 1;
@@ -271,16 +352,27 @@ __device__ __forceinline__ void unit_of(const Params &p, int BN_, int u, int &m0
     int tm, tn;
     raster(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     bn = BN_ / nsub;
-    m0 = tm * BM;
+    m0 = tm * TM;
     n0 = tn * BN_ + sub * bn;
 }
 
-// Persistent over units: CTA c handles units c, c + gridDim.x, ...  The
-// k-block stream of the TMA producer and of the MMA issuer runs on across
+// Persistent over units: CTA (or CTA pair) c handles units c, c + count, ...
+// The k-block stream of the TMA producer and of the MMA issuer runs on across
 // units (stage and phase from a per-CTA k-block counter), and the two TMEM
 // accumulators alternate between units, so the epilogue of one unit overlaps
 // the main loop of the next.
-template <int BN, bool THREE>
+//
+// PAIR: a cluster of two CTAs computes 256-row tiles with cta_group::2 MMAs
+// issued by the leader (rank 0).  Each CTA loads its 128 rows of A and half
+// of the tile's B columns into its own shared memory and keeps its 128 rows
+// of the accumulator in its own TMEM.  Both operands come pre-split (the
+// host never pairs an operand split in shared memory): both CTAs' TMA loads
+// count their bytes on the leader's full barrier, which the leader arms for
+// both.  The leader's commits free the stage and announce the accumulator in
+// both CTAs (multicast); every epilogue warp of both CTAs hands the
+// accumulator back on the leader's acce barrier.  Halving B per SM cuts the
+// shared-memory traffic per flop by a third.
+template <int BN, bool THREE, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi,
                    const __grid_constant__ CUtensorMap tm_alo,
@@ -288,17 +380,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_blo,
                    const __grid_constant__ CUtensorMap tm_bhi_tail,
                    const __grid_constant__ CUtensorMap tm_blo_tail, const Params p) {
-    using K_ = Cfg<BN, THREE>;
+    using K_ = Cfg<BN, THREE, PAIR>;
     constexpr int BK = K_::BK;
     constexpr int NW = WORKERS / 32;                   // split / epilogue warps
+    constexpr int TM = PAIR ? 2 * BM : BM;             // tile rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *epi = reinterpret_cast<float *>(smem + K_::STAGES * K_::STAGE_BYTES);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_::STAGES * K_::STAGE_BYTES +
                                                   K_::EPI_BYTES);
-    // bars[0..S) full, [S..2S) empty, [2S..3S) split done, [3S, 3S+2) accumulator
-    // full, [3S+2, 3S+4) accumulator empty
+    // bars[0..S) full, [S..2S) empty, [2S..3S) split done, [3S, 3S+2)
+    // accumulator full, [3S+2, 3S+4) accumulator empty
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * K_::STAGES + 4);
     const uint32_t smem0 = smem_u32(smem);
     const uint32_t bar0 = smem_u32(bars);
@@ -315,6 +408,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
+    const bool leader = rank == 0;
+    const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // CTA pair index
+    const int groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < K_::STAGES; ++s) {
@@ -324,7 +421,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);                 // tcgen05.commit
-            mbar_init(acce_bar(b), NW);                // one arrival per epilogue warp
+            mbar_init(acce_bar(b), PAIR ? 2 * NW : NW);   // every epilogue warp of the tile
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tm_ahi);
@@ -337,12 +434,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     :: "r"(smem_u32(tmem_slot)), "r"(K_::TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                         :: "r"(smem_u32(tmem_slot)), "r"(K_::TMEM_COLS) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                         :: "r"(smem_u32(tmem_slot)), "r"(K_::TMEM_COLS) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync_all();   // the peer's barriers exist before anything arrives on them
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -356,52 +460,76 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int64_t g = 0;                             // k-blocks issued by this CTA
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            // a pair: the leader's full barrier counts both CTAs' bytes
+            const uint32_t lead_full0 = PAIR ? leader_addr(full_bar(0)) : 0u;
+            for (int u = group; u < p.units && ok; u += groups) {
                 int m0, n0, bn, nsub;
-                unit_of(p, BN, u, m0, n0, bn, nsub);
+                unit_of(p, TM, BN, u, m0, n0, bn, nsub);
                 const CUtensorMap *mb_hi = nsub == 1 ? &tm_bhi : &tm_bhi_tail;
                 const CUtensorMap *mb_lo = nsub == 1 ? &tm_blo : &tm_blo_tail;
-                const uint32_t a_bytes = (uint32_t)K_::A_BYTES, b_bytes = (uint32_t)(bn * BK * 4);
+                const int b_rows = PAIR ? bn / 2 : bn;            // this CTA's B rows
+                const int am = m0 + (int)rank * BM, bnn = n0 + (int)rank * b_rows;
+                const uint32_t a_bytes = (uint32_t)K_::A_BYTES, b_bytes = (uint32_t)(b_rows * BK * 4);
                 const uint32_t tx = (p.fuse_a ? a_bytes : K_::PARTS * a_bytes) +
                                     (p.fuse_b ? b_bytes : K_::PARTS * b_bytes);
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) { ok = false; break; }
-                    mbar_expect_tx(full_bar(s), tx);
                     const int kc = kb * BK;
+                    if (PAIR && !leader) {
+                        // the leader arms its barrier with these bytes too
+                        const uint32_t fb = lead_full0 + 8u * s;
+                        tma_load_2d_pair(a_hi(s), &tm_ahi, fb, kc, am);
+                        tma_load_2d_pair(b_hi(s), mb_hi, fb, kc, bnn);
+                        if (THREE) tma_load_2d_pair(a_lo(s), &tm_alo, fb, kc, am);
+                        if (THREE) tma_load_2d_pair(b_lo(s), mb_lo, fb, kc, bnn);
+                        continue;
+                    }
+                    mbar_expect_tx(full_bar(s), PAIR ? 2u * tx : tx);
                     // a fused operand arrives raw in its hi tile and is split there
-                    tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, m0);
-                    tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, n0);
-                    if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, m0);
-                    if (THREE && !p.fuse_b) tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, n0);
+                    tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, am);
+                    tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, bnn);
+                    if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, am);
+                    if (THREE && !p.fuse_b) tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, bnn);
                 }
             }
-            // drain: the last arming of each stage must have landed before exit
-            for (int64_t q = (g > K_::STAGES ? g - K_::STAGES : 0); q < g; ++q)
-                mbar_wait(full_bar((int)(q % K_::STAGES)), (uint32_t)(q / K_::STAGES) & 1u,
-                          kDrainNs);
+            // drain: the last arming of each stage must have landed before
+            // exit (a pair's peer, whose loads count on the leader's barrier: consumed)
+            for (int64_t q = (g > K_::STAGES ? g - K_::STAGES : 0); q < g; ++q) {
+                const int s = (int)(q % K_::STAGES);
+                const uint32_t ph = (uint32_t)(q / K_::STAGES) & 1u;
+                if (PAIR && !leader) mbar_wait(empty_bar(s), ph, kDrainNs);
+                else mbar_wait(full_bar(s), ph, kDrainNs);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------ MMA issuer
             int64_t g = 0;
             int j = 0;                                 // units done by this CTA
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++j) {
+            for (int u = group; u < p.units && ok; u += groups, ++j) {
                 int m0, n0, bn, nsub;
-                unit_of(p, BN, u, m0, n0, bn, nsub);
+                unit_of(p, TM, BN, u, m0, n0, bn, nsub);
                 const int b = j & 1;
                 // the epilogue must have emptied this accumulator (unit j - 2)
-                if (!mbar_wait(acce_bar(b), ((uint32_t)(j >> 1) & 1u) ^ 1u, lim)) break;
+                const uint32_t eph = ((uint32_t)(j >> 1) & 1u) ^ 1u;
+                if (!(PAIR ? mbar_wait_cluster(acce_bar(b), eph, lim) : mbar_wait(acce_bar(b), eph, lim)))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
-                const uint32_t idesc = idesc_tf32(bn);
+                const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                                       ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
-                    if (!mbar_wait(fused ? conv_bar(s) : full_bar(s), ph, lim)) { ok = false; break; }
+                    const uint32_t ready = fused ? conv_bar(s) : full_bar(s);
+                    if (!(PAIR ? mbar_wait_cluster(ready, ph, lim) : mbar_wait(ready, ph, lim))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
@@ -412,16 +540,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (THREE) {
                             const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
                             const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
-                            umma_tf32(d, al, bh, idesc, first);
-                            umma_tf32(d, ah, bl, idesc, 1u);
-                            umma_tf32(d, ah, bh, idesc, 1u);
+                            if (PAIR) {
+                                umma_tf32_pair(d, al, bh, idesc, first);
+                                umma_tf32_pair(d, ah, bl, idesc, 1u);
+                                umma_tf32_pair(d, ah, bh, idesc, 1u);
+                            } else {
+                                umma_tf32(d, al, bh, idesc, first);
+                                umma_tf32(d, ah, bl, idesc, 1u);
+                                umma_tf32(d, ah, bh, idesc, 1u);
+                            }
                         } else {
-                            umma_tf32(d, ah, bh, idesc, first);
+                            if (PAIR) umma_tf32_pair(d, ah, bh, idesc, first);
+                            else umma_tf32(d, ah, bh, idesc, first);
                         }
                     }
-                    umma_commit(empty_bar(s));
+                    if (PAIR) umma_commit_pair(empty_bar(s));
+                    else umma_commit(empty_bar(s));
                 }
-                umma_commit(accf_bar(b));              // this unit's accumulator is ready
+                // this unit's accumulator is ready
+                if (PAIR) umma_commit_pair(accf_bar(b));
+                else umma_commit(accf_bar(b));
             }
             // all MMAs of this CTA retired before TMEM can be freed
             if (j > 0) {
@@ -432,20 +570,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ split + epilogue (warps 2..9)
-        // Warp w owns TMEM lanes (= tile rows) 32*(w%4) .. +31, and of them
-        // every other 32-column block (two warps per lane quarter).  Each
-        // 32 x 32 block is read with tcgen05.ld (lane = row), turned around
-        // through a padded shared tile, then written row by row: every store
-        // instruction of the warp covers 32 consecutive columns of one row.
+        // Warp w owns TMEM lanes (= rows of this CTA's part of the tile)
+        // 32*(w%4) .. +31, and of them every other 32-column block (two warps
+        // per lane quarter).  Each 32 x 32 block is read with tcgen05.ld
+        // (lane = row), turned around through a padded shared tile, then
+        // written row by row: every store instruction of the warp covers 32
+        // consecutive columns of one row.
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         float *stg = epi + (warp - 2) * 32 * EPI_LD;
         const int ct = threadIdx.x - 64;
         int64_t g = 0;
         int j = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++j) {
+        for (int u = group; u < p.units; u += groups, ++j) {
             int m0, n0, bn, nsub;
-            unit_of(p, BN, u, m0, n0, bn, nsub);
+            unit_of(p, TM, BN, u, m0, n0, bn, nsub);
+            const int b_rows = PAIR ? bn / 2 : bn;
             if (fused) {
                 // during the main loop these warps split the raw operand tiles
                 bool ok = true;
@@ -454,7 +594,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(full_bar(s), ph, lim)) { ok = false; break; }
                     if (p.fuse_a) split_tile<THREE>(a_hi(s), a_lo(s), K_::A_BYTES / 16, ct);
-                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s), bn * BK * 4 / 16, ct);
+                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s), b_rows * BK * 4 / 16, ct);
                     // generic-proxy stores must be visible to the tensor core's reads
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
@@ -467,7 +607,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             if (!ready) break;
             const float alpha = p.alpha, beta = p.beta;
-            const int rows_here = min(32, p.M - (m0 + q * 32));
+            const int row0 = m0 + (int)rank * BM + q * 32;
+            const int rows_here = min(32, p.M - row0);
 #pragma unroll 1
             for (int c = half; c < bn / 32; c += 2) {
                 uint32_t r[32];
@@ -477,7 +618,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 const int col = n0 + c * 32 + lane;
                 if (col < p.N) {
-                    float *__restrict__ dst = p.C + (int64_t)(m0 + q * 32) * p.ldc + col;
+                    float *__restrict__ dst = p.C + (int64_t)row0 * p.ldc + col;
                     if (beta == 0.0f) {
 #pragma unroll 8
                         for (int rr = 0; rr < rows_here; ++rr)
@@ -500,16 +641,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             // this warp has read its part of accumulator b: hand it back
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(b));
+            if (lane == 0) {
+                if (PAIR) remote_arrive_cluster(leader_addr(acce_bar(b)));
+                else mbar_arrive(acce_bar(b));
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync_all();   // no CTA leaves while its peer may still signal it
+    else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-                     :: "r"(tmem), "r"(K_::TMEM_COLS) : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                         :: "r"(tmem), "r"(K_::TMEM_COLS) : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                         :: "r"(tmem), "r"(K_::TMEM_COLS) : "memory");
     }
 }
 
@@ -682,26 +831,50 @@ static void launch_split_pair(bool three, const tc::SplitJob &a, const tc::Split
     else tc::split_pair_kernel<false><<<blocks, 256, 0, s>>>(a, b);
 }
 
-template <int BN, bool THREE>
+template <int BN, bool THREE, bool PAIR>
 static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, cudaStream_t s) {
-    using K_ = tc::Cfg<BN, THREE>;
+    using K_ = tc::Cfg<BN, THREE, PAIR>;
+    auto kern = tc::tc_gemm_kernel<BN, THREE, PAIR>;
     // the shared-memory opt-in is a per-device function attribute
     static uint64_t attr_done = 0;   // bit d: set on device d
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(tc::tc_gemm_kernel<BN, THREE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM) !=
             cudaSuccess)
             return last_status();
         __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
     }
     timing_mark(s, true);
-    tc::tc_gemm_kernel<BN, THREE><<<grid, tc::THREADS, K_::SMEM, s>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    if (PAIR) {
+        // clusters of two CTAs (one per SM of a pair)
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(tc::THREADS);
+        cfg.dynamicSmemBytes = K_::SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    } else {
+        kern<<<grid, tc::THREADS, K_::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                   maps[5], p);
+    }
     timing_mark(s, false);
     return last_status();
+}
+
+template <int BN, bool THREE>
+static int launch_main_any(bool pair, const CUtensorMap *maps, const tc::Params &p, int grid,
+                           cudaStream_t s) {
+    return pair ? launch_main<BN, THREE, true>(maps, p, grid, s)
+                : launch_main<BN, THREE, false>(maps, p, grid, s);
 }
 
 // 2-D map over a caller's K-contiguous fp32 operand (`rows` rows of K values,
@@ -734,6 +907,10 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // the canonical K-contiguous workspace layout.
     const bool fuse_a = pl.fuse_a && is_notrans(ta) && aligned16(A) && lda % 4 == 0;
     const bool fuse_b = pl.fuse_b && !is_notrans(tb) && aligned16(B) && ldb % 4 == 0;
+    // the pair kernel takes pre-split operands only
+    const bool pair = pl.pair != 0 && !fuse_a && !fuse_b;
+    const int TM = pair ? 2 * tc::BM : tc::BM;          // tile rows
+    const int bdiv = pair ? 2 : 1;                      // B rows per CTA = tile columns / bdiv
     auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
     const size_t a_elems = fuse_a ? 0 : up((size_t)M * Kp * 4) / 4;
     const size_t b_elems = fuse_b ? 0 : up((size_t)N * Kp * 4) / 4;
@@ -771,24 +948,24 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
              make_map(&maps[1], a_lo, (int)M, Kp, tc::BM, bk);
     }
     if (fuse_b) {
-        ok = ok && make_raw_map(&maps[2], B, (int)N, (int)K, ldb, BN, bk) &&
-             make_raw_map(&maps[4], B, (int)N, (int)K, ldb, BN / nsplit, bk);
+        ok = ok && make_raw_map(&maps[2], B, (int)N, (int)K, ldb, BN / bdiv, bk) &&
+             make_raw_map(&maps[4], B, (int)N, (int)K, ldb, BN / nsplit / bdiv, bk);
         maps[3] = maps[2];
         maps[5] = maps[4];
     } else {
-        ok = ok && make_map(&maps[2], b_hi, (int)N, Kp, BN, bk) &&
-             make_map(&maps[3], b_lo, (int)N, Kp, BN, bk) &&
-             make_map(&maps[4], b_hi, (int)N, Kp, BN / nsplit, bk) &&
-             make_map(&maps[5], b_lo, (int)N, Kp, BN / nsplit, bk);
+        ok = ok && make_map(&maps[2], b_hi, (int)N, Kp, BN / bdiv, bk) &&
+             make_map(&maps[3], b_lo, (int)N, Kp, BN / bdiv, bk) &&
+             make_map(&maps[4], b_hi, (int)N, Kp, BN / nsplit / bdiv, bk) &&
+             make_map(&maps[5], b_lo, (int)N, Kp, BN / nsplit / bdiv, bk);
     }
     if (!ok) return SGEMM_ERR_UNSUPPORTED;
 
     tc::Params p{};
     p.C = C; p.ldc = ldc; p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.alpha = alpha; p.beta = beta;
-    p.tiles_m = (int)((M + tc::BM - 1) / tc::BM);
+    p.tiles_m = (int)((M + TM - 1) / TM);
     p.tiles_n = (int)((N + BN - 1) / BN);
-    p.group_m = 16;
+    p.group_m = pair ? 8 : 16;
     p.dp_tiles = std::min(pl.dp_tiles, p.tiles_m * p.tiles_n);
     p.tail_nsplit = nsplit;
     p.num_kb = Kp / bk;
@@ -803,10 +980,17 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // under the main loop of the next) unless an operand is split in the
     // kernel: the split warps are also the epilogue warps, so those CTAs take
     // one unit each.
-    const int grid = (fuse_a || fuse_b) ? p.units : std::min(p.units, std::max(sms, 1));
-    if (BN == 256) return three ? launch_main<256, true>(maps, p, grid, s) : launch_main<256, false>(maps, p, grid, s);
-    if (BN == 128) return three ? launch_main<128, true>(maps, p, grid, s) : launch_main<128, false>(maps, p, grid, s);
-    return three ? launch_main<64, true>(maps, p, grid, s) : launch_main<64, false>(maps, p, grid, s);
+    const int slots = pair ? std::max(sms / 2, 1) : std::max(sms, 1);
+    const int groups = (fuse_a || fuse_b) ? p.units : std::min(p.units, slots);
+    const int grid = groups * (pair ? 2 : 1);
+    if (BN == 256)
+        return three ? launch_main_any<256, true>(pair, maps, p, grid, s)
+                     : launch_main_any<256, false>(pair, maps, p, grid, s);
+    if (BN == 128)
+        return three ? launch_main_any<128, true>(pair, maps, p, grid, s)
+                     : launch_main_any<128, false>(pair, maps, p, grid, s);
+    return three ? launch_main_any<64, true>(pair, maps, p, grid, s)
+                 : launch_main_any<64, false>(pair, maps, p, grid, s);
 }
 
 }  // namespace sgemm_gb300

@@ -126,6 +126,22 @@ def test_plan_auto_path_choice(lib):
         assert p["path"] != sg.PATH_TF32
 
 
+def test_plan_sm_pair_tiles(lib):
+    # both operands through the split pre-pass and M > 128: 256-row tiles on SM pairs
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096)
+    assert st == 0 and p["tile_m"] == 256 and p["ctas"] % 2 == 0
+    st, p = sg.sgemm_plan("T", "N", 300, 260, 1000, 300, 260, 260, path=sg.PATH_3XTF32)
+    assert st == 0 and p["tile_m"] == 256
+    # an operand split in shared memory (K-contiguous, small other side): single SMs
+    st, p = sg.sgemm_plan("N", "N", 2048, 2048, 2048, 2048, 2048, 2048)
+    assert st == 0 and p["tile_m"] == 128
+    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64)
+    assert st == 0 and p["tile_m"] == 128
+    # M fits one 128-row tile
+    st, p = sg.sgemm_plan("T", "N", 128, 4096, 4096, 128, 4096, 4096, path=sg.PATH_3XTF32)
+    assert st == 0 and p["tile_m"] == 128
+
+
 def test_plan_split_k_for_small_grids(lib):
     # 256^3: 4 tiles for 304 CTA slots -> the K loop is split
     st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152)
