@@ -12,7 +12,9 @@
 //     fma.rn.f32x2 (two independent round-to-nearest FMAs each).  The 8 x 16
 //     tile is what keeps shared-memory delivery (128 bytes per clock per SM)
 //     below the FMA rate: 24 loaded floats per 128 FMAs instead of the 16 per
-//     64 of an 8 x 8 tile (section 4 counts the same ratio at one level less);
+//     64 of an 8 x 8 tile (section 4 counts the same ratio at one level less).
+//     The lanes of each quad hold a 2 x 2 block of row and column groups, so
+//     every 16-byte shared load costs 2 wavefronts instead of 4;
 //   * both operand tiles sit in shared memory k-major ([k][m] and [k][n]).
 //     An operand whose rows run along K in global memory (A with 'N', B with
 //     'T') is loaded as float4 along K into registers and stored transposed
@@ -241,11 +243,16 @@ __device__ __forceinline__ void run_share(const Params &p, float (*sA)[BK * BM],
     const int n0 = tn * BN;
     const int nkt = j1 - j0;
 
-    // thread -> outputs: 4 warps as 2 x 2 of 64 x 64
+    // thread -> outputs: 4 warps as 2 x 2 of 64 x 64; a lane has row group
+    // lr (8 per warp) and column group lc (4 per warp).  Each quad of lanes
+    // (4i .. 4i+3) is a 2 x 2 block of (lr, lc): a 16-byte shared load is
+    // served per lane quad, so a quad that asks for 2 distinct A (or B) chunks
+    // costs half the wavefronts of one that asks for 4 (measured on GB300:
+    // 12 instead of 20 wavefronts per warp k-step).
     const int wm = warp & 1;
     const int wn = warp >> 1;
-    const int lr = lane >> 2;           // 0..7
-    const int lc = lane & 3;            // 0..3
+    const int lr = ((lane >> 3) << 1) | ((lane >> 1) & 1);   // 0..7
+    const int lc = (((lane >> 2) & 1) << 1) | (lane & 1);    // 0..3
     const int am = wm * 64 + lr * 4;    // rows am + {0..3}, am + 32 + {0..3}
     const int bn = wn * 64 + lc * 4;    // columns bn + 16 g + {0..3}
 
@@ -315,11 +322,23 @@ __device__ __forceinline__ void run_share(const Params &p, float (*sA)[BK * BM],
                 b[2 * g + 1] = make_float2(bg.z, bg.w);
             }
             const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            // Column pair outer (consecutive packed FMAs share their b operand),
+            // except with both operands staged through registers by 16-byte
+            // loads, where that order makes the compiler spill (measured on
+            // GB300: NN 4096^3 +1.6 % for the column order, NT -25 % for it).
+            if constexpr (!(A_KMAJOR && B_KMAJOR && VEC)) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 ai = make_float2(a[i], a[i]);
+                for (int j = 0; j < 8; ++j)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
+                    for (int i = 0; i < 8; ++i)
+                        acc[i][j] = __ffma2_rn(make_float2(a[i], a[i]), b[j], acc[i][j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
+                }
             }
         }
         if (has_next) {
