@@ -70,7 +70,7 @@ typedef enum {
    fp32-accurate paths (FFMA and 3xTF32); TF32 is never chosen by AUTO. */
 typedef enum {
     SGEMM_PATH_AUTO = 0,
-    SGEMM_PATH_FFMA = 1,   /* CUDA-core fp32 FMA, 128x128 block tiles, 8x8
+    SGEMM_PATH_FFMA = 1,   /* CUDA-core fp32 FMA, 128x128 block tiles, 8x16
                               register outer products ("Matmul II: register
                               blocking, warp tiling, tensor cores", sections
                               3-5).  Sums each output in ascending k with

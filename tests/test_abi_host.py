@@ -142,6 +142,21 @@ def test_plan_sm_pair_tiles(lib):
     assert st == 0 and p["tile_m"] == 128
 
 
+def test_plan_ffma_stream_k_tail(lib):
+    # 4096^3: 1024 tiles = 3 full waves of 304 + 112; the 112 are shared by 304 CTAs
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152,
+                          path=sg.PATH_FFMA)
+    assert st == 0 and p["split"] > 1 and p["ctas"] == 912 + 304
+    # exactly 4 waves (4096 x 4864): nothing left over, every tile whole
+    st, p = sg.sgemm_plan("N", "N", 4096, 4864, 4096, 4096, 4864, 4864, num_sms=152,
+                          path=sg.PATH_FFMA)
+    assert st == 0 and p["split"] == 1 and p["ctas"] == 1216
+    # a short K leaves too few k-tiles to share: the tail stays whole
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 64, 64, 4096, 4096, num_sms=152,
+                          path=sg.PATH_FFMA)
+    assert st == 0 and p["split"] == 1
+
+
 def test_plan_split_k_for_small_grids(lib):
     # 256^3: 4 tiles for 304 CTA slots -> the K loop is split
     st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152)
