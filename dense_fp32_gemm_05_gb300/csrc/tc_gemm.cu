@@ -81,7 +81,20 @@ struct Cfg {
     static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
     // two accumulators (double-buffered TMEM) when they fit in the 512 columns
     static constexpr int NBUF = 2;
-    static constexpr uint32_t TMEM_COLS = NBUF * BN;     // power of two <= 512
+    // TMEM: the accumulators from column 0 (two of BN columns when the CTA
+    // walks several tiles); a CTA that splits A in the kernel takes one tile,
+    // so its single accumulator leaves columns 256.. for one slot of A per
+    // stage (hi, then lo: PARTS * BK columns).
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int A_TMEM_COL = 256;
+    static constexpr int A_SLOT_COLS = PARTS * BK;
+    // N = 64 MMAs are short enough that one dependent chain of them into a
+    // single accumulator runs at about half the tensor rate: such tiles keep
+    // independent accumulators (3xTF32: one per product; TF32: even and odd
+    // k-slices), summed by the epilogue.
+    static constexpr int NACC = (BN == 64 && !PAIR) ? (THREE ? 3 : 2) : 1;
+    static_assert(NBUF * NACC * BN <= 512 && NACC * BN <= A_TMEM_COL, "accumulator columns");
+    static_assert(A_TMEM_COL + STAGES * A_SLOT_COLS <= 512, "A slots in TMEM");
     static_assert(STAGES >= 2, "need at least two stages");
     static_assert(BN == 64 || BN == 128 || BN == 256, "N of the MMA");
 };
@@ -275,6 +288,29 @@ __device__ __forceinline__ void cluster_sync_all() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// A operand from tensor memory: M = 128 lanes (rows) x 8 columns (k) of tf32.
+__device__ __forceinline__ void umma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// 32 lanes x 8 columns of 32-bit values from registers into tensor memory.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                    "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+                    "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                    "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit accumulators -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -320,6 +356,43 @@ __device__ __forceinline__ void split_tile(uint32_t hi, uint32_t lo, int n16, in
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                          :: "r"(lo + 16u * i), "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w) : "memory");
         }
+    }
+}
+
+// Split of this thread's row of a raw A tile (TMA-swizzled, rows of BK
+// floats) into tensor memory: row r = 32 q + lane, k = half * BK/2 .. +BK/2;
+// hi = round(x) to columns tslot + k, lo = round(x - hi) to tslot + BK + k
+// (THREE only).  TMA's 64-byte swizzle (BK = 16) flips the 16-byte chunk
+// index by bits 1-2 of the row, its 128-byte swizzle (BK = 32) by bits 0-2.
+// `taddr` is the warp's lane quarter and column tslot of tensor memory.
+template <bool THREE>
+__device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, int q, int half,
+                                                int lane) {
+    constexpr int BK_ = KBlock<THREE>::BK;
+    constexpr int KH = BK_ / 2;                       // k values per thread: 8 or 16
+    const int r = q * 32 + lane;
+    const uint32_t sw = THREE ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
+    const uint32_t row = raw + (uint32_t)(r * BK_ * 4);
+#pragma unroll
+    for (int g = 0; g < KH / 8; ++g) {                // 8 k values per TMEM store
+        float hi[8], lo[8];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const uint32_t chunk = (uint32_t)(half * (KH / 4) + g * 2 + c);
+            float4 v;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(row + ((chunk ^ sw) << 4)));
+            const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                hi[4 * c + e] = tf32_round(x[e]);
+                if (THREE) lo[4 * c + e] = tf32_round(__fsub_rn(x[e], hi[4 * c + e]));
+            }
+        }
+        const uint32_t col = (uint32_t)(half * KH + g * 8);
+        tmem_st8(taddr + col, hi);
+        if (THREE) tmem_st8(taddr + (uint32_t)BK_ + col, lo);
     }
 }
 
@@ -405,6 +478,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto a_lo = [&](int s) { return b_hi(s) + K_::B_BYTES; };
     auto b_lo = [&](int s) { return a_lo(s) + K_::A_BYTES; };
     const bool fused = p.fuse_a || p.fuse_b;
+    // 64-wide 3xTF32 tiles with A split into TMEM issue A_hi x [B_hi | B_lo]
+    // as one N = 128 MMA and A_lo x B_hi: 2 MMAs per k-slice instead of 3
+    constexpr bool BCAT = THREE && !PAIR && K_::NACC == 3;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -491,7 +567,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, am);
                     tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, bnn);
                     if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, am);
-                    if (THREE && !p.fuse_b) tma_load_2d(b_lo(s), mb_lo, full_bar(s), kc, bnn);
+                    // with A in TMEM, A_lo's slot holds B_lo right after B_hi:
+                    // one N = 2 BN operand [B_hi | B_lo] (64-wide 3xTF32 tiles)
+                    if (THREE && !p.fuse_b)
+                        tma_load_2d(BCAT && p.fuse_a ? a_lo(s) : b_lo(s), mb_lo, full_bar(s), kc, bnn);
                 }
             }
             // drain: the last arming of each stage must have landed before
@@ -519,7 +598,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!(PAIR ? mbar_wait_cluster(acce_bar(b), eph, lim) : mbar_wait(acce_bar(b), eph, lim)))
                     break;
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(b * BN);
+                const uint32_t d = tmem + (uint32_t)(b * K_::NACC * BN);
+                constexpr int NA = K_::NACC;
                 const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
                                        ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
@@ -531,6 +611,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (!PAIR && p.fuse_a) {
+                        // A split into this stage's TMEM slot by the split warps
+                        const uint32_t at = tmem + (uint32_t)(K_::A_TMEM_COL + s * K_::A_SLOT_COLS);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 8; ++kk) {
+                            const uint32_t off = kk * 32;
+                            const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
+                            const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                            const uint32_t ah = at + (uint32_t)(kk * 8);
+                            if (BCAT && !p.fuse_b) {
+                                // [B_hi | B_lo] starts at b_hi(s): hi*hi to BN.., hi*lo to 2 BN..
+                                const uint32_t idesc2 = idesc + ((uint32_t)(bn >> 3) << 17);
+                                umma_tf32_ta(d + (uint32_t)BN, ah, bh, idesc2, first);
+                                umma_tf32_ta(d, ah + (uint32_t)BK, bh, idesc, first);
+                            } else if (THREE) {
+                                const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
+                                const uint32_t f2 = NA == 3 ? first : 1u;
+                                umma_tf32_ta(d, ah + (uint32_t)BK, bh, idesc, first);
+                                umma_tf32_ta(d + (NA == 3 ? 2 * BN : 0), ah, bl, idesc, f2);
+                                umma_tf32_ta(d + (NA == 3 ? BN : 0), ah, bh, idesc, f2);
+                            } else {
+                                const int ka = NA == 2 ? (kk & 1) : 0;
+                                const uint32_t fa = (kb == 0 && kk < NA) ? 0u : 1u;
+                                umma_tf32_ta(d + (uint32_t)(ka * BN), ah, bh, idesc, fa);
+                            }
+                        }
+                        umma_commit(empty_bar(s));
+                        continue;
+                    }
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
                         const uint32_t off = kk * 32;            // 8 tf32 = 32 bytes
@@ -545,13 +654,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 umma_tf32_pair(d, ah, bl, idesc, 1u);
                                 umma_tf32_pair(d, ah, bh, idesc, 1u);
                             } else {
+                                const uint32_t f2 = NA == 3 ? first : 1u;
                                 umma_tf32(d, al, bh, idesc, first);
-                                umma_tf32(d, ah, bl, idesc, 1u);
-                                umma_tf32(d, ah, bh, idesc, 1u);
+                                umma_tf32(d + (NA == 3 ? 2 * BN : 0), ah, bl, idesc, f2);
+                                umma_tf32(d + (NA == 3 ? BN : 0), ah, bh, idesc, f2);
                             }
                         } else {
-                            if (PAIR) umma_tf32_pair(d, ah, bh, idesc, first);
-                            else umma_tf32(d, ah, bh, idesc, first);
+                            if (PAIR) {
+                                umma_tf32_pair(d, ah, bh, idesc, first);
+                            } else {
+                                const int ka = NA == 2 ? (kk & 1) : 0;
+                                const uint32_t fa = (kb == 0 && kk < NA) ? 0u : 1u;
+                                umma_tf32(d + (uint32_t)(ka * BN), ah, bh, idesc, fa);
+                            }
                         }
                     }
                     if (PAIR) umma_commit_pair(empty_bar(s));
@@ -593,10 +708,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(full_bar(s), ph, lim)) { ok = false; break; }
-                    if (p.fuse_a) split_tile<THREE>(a_hi(s), a_lo(s), K_::A_BYTES / 16, ct);
-                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s), b_rows * BK * 4 / 16, ct);
-                    // generic-proxy stores must be visible to the tensor core's reads
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    if (p.fuse_a) {
+                        // A's hi and lo go to tensor memory, where the MMA reads
+                        // them: no shared-memory traffic for A in the MMAs
+                        const uint32_t slot = tmem + ((uint32_t)(q * 32) << 16) +
+                                              (uint32_t)(K_::A_TMEM_COL + s * K_::A_SLOT_COLS);
+                        split_a_to_tmem<THREE>(a_hi(s), slot, q, half, lane);
+                        tmem_st_wait();
+                        tc_fence_before();
+                    }
+                    if (p.fuse_b) {
+                        split_tile<THREE>(b_hi(s), b_lo(s), b_rows * BK * 4 / 16, ct);
+                        // generic-proxy stores must be visible to the tensor core's reads
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(conv_bar(s));
                 }
@@ -612,9 +737,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
             for (int c = half; c < bn / 32; c += 2) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) +
+                                    (uint32_t)(b * K_::NACC * BN + c * 32);
+                tmem_ld32(ta, r);
+                if (K_::NACC == 1) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = __uint_as_float(r[jj]);
+                    for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = __uint_as_float(r[jj]);
+                } else {
+                    // 3xTF32 (lo*hi at 0, hi*hi at BN, hi*lo at 2 BN):
+                    // hi*hi + (lo*hi + hi*lo); TF32: even + odd k-slices
+                    float f[32];
+                    uint32_t r2[32];
+                    tmem_ld32(ta + (uint32_t)(K_::NACC == 3 ? 2 * BN : BN), r2);
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        f[jj] = __fadd_rn(__uint_as_float(r[jj]), __uint_as_float(r2[jj]));
+                    if (K_::NACC == 3) {
+                        tmem_ld32(ta + (uint32_t)BN, r2);
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) f[jj] = __fadd_rn(__uint_as_float(r2[jj]), f[jj]);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = f[jj];
+                }
                 __syncwarp();
                 const int col = n0 + c * 32 + lane;
                 if (col < p.N) {
