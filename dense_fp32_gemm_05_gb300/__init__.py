@@ -15,7 +15,7 @@ import threading
 __all__ = [
     "SGEMM_OK", "SGEMM_ERR_CUDA", "SGEMM_ERR_TIMEOUT", "SGEMM_ERR_NOMEM",
     "SGEMM_ERR_UNSUPPORTED", "SGEMM_ERR_ARG", "SGEMM_ERR_SCRATCH", "PATH_AUTO", "PATH_FFMA",
-    "PATH_3XTF32", "PATH_TF32", "SgemmError", "library_path", "load",
+    "PATH_3XTF32", "PATH_TF32", "PATH_GEMV", "SgemmError", "library_path", "load",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
     "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
@@ -34,6 +34,7 @@ PATH_AUTO = 0
 PATH_FFMA = 1
 PATH_3XTF32 = 2
 PATH_TF32 = 3
+PATH_GEMV = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libsgemm_gb300.so"

@@ -1,0 +1,418 @@
+// Thin GEMMs: min(M, N) <= 16 (SGEMM_PATH_GEMV).
+//
+// "Matmul II: register blocking, warp tiling, tensor cores", section 8
+// ("What cuBLAS does that we do not"): when M is 1 (decode) to a few dozen,
+// none of the tile kernels' compute tricks apply; the GEMM is a memory-bound
+// GEMV and the only thing that counts is streaming the large operand once.
+// So this path has no tiles and no shared-memory staging of the large
+// operand.  With S = min(M, N) (the small dimension) and P the other one:
+//
+//   out(s, p) = sum_k Small(s, k) * Big(p, k)
+//
+// M small: s = row of C, p = column; Small = op(A), Big(p, k) = op(B)(k, p).
+// N small: s = column of C, p = row;  Small(s, k) = op(B)(k, s), Big = op(A).
+// Then C(s, p) = alpha * out + beta * C (C not read when beta == 0), with
+// the same epilogue roundings as the other paths.
+//
+// Two kernels, by how Big lies in memory:
+//   * dot form (Big's rows run along K): a warp owns PB rows of Big and
+//     streams them with 16-byte loads along K, each lane summing 4 of every
+//     128 consecutive k; Small (S x K, a few KB per row) is read through L1.
+//     A warp butterfly adds the 32 lane sums of each output.
+//   * axpy form (Big's rows run along P): a lane owns 4 consecutive p and
+//     reads Big(p .. p+3, k) with one 16-byte load per k; Small(s, k) is the
+//     same for the whole warp (a broadcast load).  The 8 warps of a CTA take
+//     interleaved k of the CTA's K range and are added through shared
+//     memory in warp order; when K is also split across CTAs (to fill the
+//     GPU), the CTAs' partial sums are added in K order by a second kernel.
+// Every sum is a fixed order of fp32 FMAs and adds: deterministic, and, as
+// any summation order, inside the 4 K 2^-24 bound.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/sgemm_gb300.h"
+#include "gemv.h"
+#include "plan.h"
+#include "tc_gemm.h"
+
+namespace sgemm_gb300 {
+namespace gemv {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+constexpr int AX_P = 128;              // axpy form: p per CTA (32 lanes x 4)
+
+struct Params {
+    const float *big;
+    int64_t big_ld;
+    const float *small;
+    int64_t small_ss, small_sk;        // Small(s, k) = small[s * ss + k * sk]
+    float *C;
+    int64_t c_s, c_p;                  // C(s, p) = C[s * c_s + p * c_p]
+    int S, P, K;
+    float alpha, beta;
+    float *partial;                    // axpy form, K split: [ksplit][S][P]
+    int ksplit, kchunk;                // K range of CTA y: [y * kchunk, min(K, +kchunk))
+};
+
+__device__ __forceinline__ void store_out(const Params &p, int s, int q, float v) {
+    float *dst = p.C + (int64_t)s * p.c_s + (int64_t)q * p.c_p;
+    *dst = p.beta == 0.0f ? __fmul_rn(p.alpha, v)
+                          : __fmaf_rn(p.alpha, v, __fmul_rn(p.beta, *dst));
+}
+
+// ------------------------------------------------------------ dot form
+// SM: compile-time bound on S; PB: rows of Big per warp; VEC: Big rows and
+// Small rows start 16-byte aligned with K-contiguous Small (16-byte loads).
+template <int SM, int PB, bool VEC>
+__global__ void __launch_bounds__(THREADS) gemv_dot_kernel(const Params p) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int p0 = (blockIdx.x * WARPS + warp) * PB;
+    if (p0 >= p.P) return;
+    // acc[s][b]: two partial sums of output (s, p0 + b), k = 4i + {0, 1} and
+    // 4i + {2, 3}, advanced together by packed fma.rn.f32x2
+    float2 acc[SM][PB];
+#pragma unroll
+    for (int s = 0; s < SM; ++s)
+#pragma unroll
+        for (int b = 0; b < PB; ++b) acc[s][b] = make_float2(0.0f, 0.0f);
+    const float *rows[PB];
+#pragma unroll
+    for (int b = 0; b < PB; ++b)
+        rows[b] = p.big + (int64_t)min(p0 + b, p.P - 1) * p.big_ld;   // clamped: a row past P is read, never stored
+    int k = lane * 4;
+    if (VEC) {
+#pragma unroll 2
+        for (; k + 3 < p.K; k += 128) {
+            float4 bv[PB];
+#pragma unroll
+            for (int b = 0; b < PB; ++b) bv[b] = __ldg(reinterpret_cast<const float4 *>(rows[b] + k));
+#pragma unroll
+            for (int s = 0; s < SM; ++s) {
+                if (s < p.S) {
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(p.small + s * p.small_ss + k));
+#pragma unroll
+                    for (int b = 0; b < PB; ++b) {
+                        acc[s][b] = __ffma2_rn(make_float2(a.x, a.y), make_float2(bv[b].x, bv[b].y), acc[s][b]);
+                        acc[s][b] = __ffma2_rn(make_float2(a.z, a.w), make_float2(bv[b].z, bv[b].w), acc[s][b]);
+                    }
+                }
+            }
+        }
+    }
+    // the rest (all of K without 16-byte loads): 4 consecutive k per lane
+    for (; k < p.K; k += 128) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (k + j < p.K) {
+                float bv[PB];
+#pragma unroll
+                for (int b = 0; b < PB; ++b) bv[b] = __ldg(rows[b] + k + j);
+#pragma unroll
+                for (int s = 0; s < SM; ++s) {
+                    if (s < p.S) {
+                        const float a = __ldg(p.small + s * p.small_ss + (int64_t)(k + j) * p.small_sk);
+#pragma unroll
+                        for (int b = 0; b < PB; ++b) acc[s][b].x = __fmaf_rn(a, bv[b], acc[s][b].x);
+                    }
+                }
+            }
+        }
+    }
+    // butterfly over the warp, then output (s, b) is stored by lane (s * PB + b) % 32
+#pragma unroll
+    for (int s = 0; s < SM; ++s) {
+#pragma unroll
+        for (int b = 0; b < PB; ++b) {
+            float v = __fadd_rn(acc[s][b].x, acc[s][b].y);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (s < p.S && p0 + b < p.P && lane == (s * PB + b) % 32) store_out(p, s, p0 + b, v);
+        }
+    }
+}
+
+// ------------------------------------------------------------ axpy form
+constexpr int AX_KC = 256;             // k per shared-memory chunk of Small
+constexpr int AX_U = 8;                // consecutive k per warp step (row loads in flight)
+
+template <int SM>
+constexpr int ax_smem_floats() { return WARPS * SM * AX_P + AX_KC * SM; }
+
+template <int SM, bool VEC>
+__global__ void __launch_bounds__(THREADS, 2) gemv_axpy_kernel(const Params p) {
+    extern __shared__ __align__(16) float smem_f[];
+    float *red = smem_f;                               // [WARPS][SM][AX_P]
+    float *smt = smem_f + WARPS * SM * AX_P;           // Small chunk, [AX_KC][SM]
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int pc = blockIdx.x * AX_P + lane * 4;       // this lane's first p
+    const int k0 = blockIdx.y * p.kchunk;
+    const int k1 = min(p.K, k0 + p.kchunk);
+    // acc[s][h] = outputs (s, pc + 2h), (s, pc + 2h + 1): packed fma.rn.f32x2,
+    // two independent round-to-nearest FMAs, half the issue slots
+    float2 acc[SM][2];
+#pragma unroll
+    for (int s = 0; s < SM; ++s) acc[s][0] = acc[s][1] = make_float2(0.0f, 0.0f);
+    const bool whole = VEC && pc + 3 < p.P;
+    const bool s_fast = p.small_ss == 1;               // Small's stored rows run along s
+    constexpr int U = AX_U;
+    for (int kc = k0; kc < k1; kc += AX_KC) {
+        const int kn = min(AX_KC, k1 - kc);
+        __syncthreads();                               // the previous chunk is consumed
+        // Small(s, kc .. kc+kn) -> smt[k][s], reading along its contiguous dimension
+        for (int i = threadIdx.x; i < kn * SM; i += THREADS) {
+            const int s = s_fast ? i % SM : i / kn;
+            const int kk = s_fast ? i / SM : i % kn;
+            smt[kk * SM + s] = s < p.S ? __ldg(p.small + (int64_t)s * p.small_ss +
+                                               (int64_t)(kc + kk) * p.small_sk)
+                                       : 0.0f;
+        }
+        __syncthreads();
+        // warp w takes U consecutive k at a time (k = kc + (w + 8 i) U ..):
+        // all U row loads are issued before the first FMA
+        for (int kb = kc + warp * U; kb < kc + kn; kb += WARPS * U) {
+            float bv[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = kb + u;
+                const float *row = p.big + (int64_t)k * p.big_ld;
+                if (k >= kc + kn) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) bv[u][j] = 0.0f;
+                } else if (whole) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(row + pc));
+                    bv[u][0] = v.x; bv[u][1] = v.y; bv[u][2] = v.z; bv[u][3] = v.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) bv[u][j] = pc + j < p.P ? __ldg(row + pc + j) : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = kb + u;
+                if (k >= kc + kn) break;                // this chunk's Small ends here
+                const float *a = smt + (k - kc) * SM;  // the same address in every lane
+                float av[SM];
+                if constexpr (SM % 4 == 0) {
+#pragma unroll
+                    for (int s = 0; s < SM; s += 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(a + s);
+                        av[s] = v.x; av[s + 1] = v.y; av[s + 2] = v.z; av[s + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int s = 0; s < SM; ++s) av[s] = a[s];
+                }
+                const float2 b01 = make_float2(bv[u][0], bv[u][1]);
+                const float2 b23 = make_float2(bv[u][2], bv[u][3]);
+#pragma unroll
+                for (int s = 0; s < SM; ++s) {
+                    const float2 a2 = make_float2(av[s], av[s]);
+                    acc[s][0] = __ffma2_rn(a2, b01, acc[s][0]);
+                    acc[s][1] = __ffma2_rn(a2, b23, acc[s][1]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < SM; ++s)
+        *reinterpret_cast<float4 *>(red + (warp * SM + s) * AX_P + lane * 4) =
+            make_float4(acc[s][0].x, acc[s][0].y, acc[s][1].x, acc[s][1].y);
+    __syncthreads();
+    // thread t: outputs (s, q) with s * AX_P + q = t, t + 256, ...; warps added in order
+    for (int o = threadIdx.x; o < SM * AX_P; o += THREADS) {
+        const int s = o / AX_P, q = o % AX_P;
+        const int pp = blockIdx.x * AX_P + q;
+        if (s >= p.S || pp >= p.P) continue;
+        float v = red[s * AX_P + q];
+        for (int w = 1; w < WARPS; ++w) v = __fadd_rn(v, red[(w * SM + s) * AX_P + q]);
+        if (p.ksplit == 1) store_out(p, s, pp, v);
+        else p.partial[((int64_t)blockIdx.y * p.S + s) * p.P + pp] = v;
+    }
+}
+
+// The K-split CTAs' partial sums, added in K order, then the epilogue.
+__global__ void __launch_bounds__(THREADS) gemv_ksum_kernel(const Params p) {
+    const int64_t n = (int64_t)p.S * p.P;
+    for (int64_t o = blockIdx.x * (int64_t)THREADS + threadIdx.x; o < n;
+         o += (int64_t)gridDim.x * THREADS) {
+        float v = p.partial[o];
+        for (int y = 1; y < p.ksplit; ++y) v = __fadd_rn(v, p.partial[(int64_t)y * n + o]);
+        store_out(p, (int)(o / p.P), (int)(o % p.P), v);
+    }
+}
+
+}  // namespace gemv
+
+namespace {
+
+template <int SM, int PB, bool VEC>
+void launch_dot(const gemv::Params &p, cudaStream_t s) {
+    const int rows_per_cta = gemv::WARPS * PB;
+    gemv::gemv_dot_kernel<SM, PB, VEC><<<(p.P + rows_per_cta - 1) / rows_per_cta, gemv::THREADS, 0, s>>>(p);
+}
+
+template <int SM, bool VEC>
+void launch_dot_pb(const gemv::Params &p, int pb, cudaStream_t s) {
+    if (pb == 4) launch_dot<SM, 4, VEC>(p, s);
+    else if (pb == 2) launch_dot<SM, 2, VEC>(p, s);
+    else launch_dot<SM, 1, VEC>(p, s);
+}
+
+template <bool VEC>
+void launch_dot_s(const gemv::Params &p, int pb, cudaStream_t s) {
+    if (p.S <= 1) launch_dot_pb<1, VEC>(p, pb, s);
+    else if (p.S <= 2) launch_dot_pb<2, VEC>(p, pb, s);
+    else if (p.S <= 4) launch_dot_pb<4, VEC>(p, pb, s);
+    else if (p.S <= 8) launch_dot_pb<8, VEC>(p, pb, s);
+    else launch_dot_pb<16, VEC>(p, pb, s);
+}
+
+template <int SM, bool VEC>
+int launch_axpy(const gemv::Params &p, cudaStream_t s) {
+    auto kern = gemv::gemv_axpy_kernel<SM, VEC>;
+    const int smem = gemv::ax_smem_floats<SM>() * (int)sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    dim3 grid((p.P + gemv::AX_P - 1) / gemv::AX_P, p.ksplit);
+    kern<<<grid, gemv::THREADS, smem, s>>>(p);
+    return SGEMM_OK;
+}
+
+template <bool VEC>
+int launch_axpy_s(const gemv::Params &p, cudaStream_t s) {
+    if (p.S <= 1) return launch_axpy<1, VEC>(p, s);
+    if (p.S <= 2) return launch_axpy<2, VEC>(p, s);
+    if (p.S <= 4) return launch_axpy<4, VEC>(p, s);
+    if (p.S <= 8) return launch_axpy<8, VEC>(p, s);
+    return launch_axpy<16, VEC>(p, s);
+}
+
+bool al16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+
+int last_cuda_status() {
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace {
+
+// Launch geometry shared by run_gemv and gemv_ctas.
+struct Geometry {
+    bool dot;            // the large operand's rows run along K
+    int S, P;
+    int pb;              // dot form: rows of the large operand per warp
+    int kchunk, ksplit;  // axpy form: K range per CTA, CTAs along K
+    int ctas;
+};
+
+Geometry geometry(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
+    Geometry g{};
+    const bool rows_thin = M <= N;
+    g.S = (int)(rows_thin ? M : N);
+    g.P = (int)(rows_thin ? N : M);
+    g.dot = rows_thin ? !is_notrans(tb) : is_notrans(ta);
+    if (g.dot) {
+        // rows per warp: 4, 2 or 1, the largest that still gives 2 CTAs per SM
+        g.pb = 1;
+        for (int c : {4, 2}) {
+            if ((g.P + gemv::WARPS * c - 1) / (gemv::WARPS * c) >= 2 * sms) { g.pb = c; break; }
+        }
+        g.ctas = (g.P + gemv::WARPS * g.pb - 1) / (gemv::WARPS * g.pb);
+        g.ksplit = 1;
+        return g;
+    }
+    // axpy form: split K over CTAs until the grid covers 2 CTAs per SM,
+    // each CTA keeping at least 256 k (32 per warp)
+    const int pblocks = (g.P + gemv::AX_P - 1) / gemv::AX_P;
+    int64_t ks = std::max(1, (2 * sms + pblocks - 1) / pblocks);
+    ks = std::min<int64_t>(ks, std::max<int64_t>(1, K / 256));
+    g.kchunk = (int)((K + ks - 1) / ks);
+    g.ksplit = (int)((K + g.kchunk - 1) / g.kchunk);
+    g.ctas = pblocks * g.ksplit;
+    return g;
+}
+
+}  // namespace
+
+int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
+    return geometry(ta, tb, M, N, std::max<int64_t>(K, 1), sms).ctas;
+}
+
+int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+             int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+             cudaStream_t s, int sms) {
+    if (std::min(M, N) > kGemvMaxSmall) return SGEMM_ERR_UNSUPPORTED;
+    const bool a_n = is_notrans(ta), b_n = is_notrans(tb);
+    gemv::Params p{};
+    p.K = (int)K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    bool big_kcontig;
+    if (M <= N) {
+        // s = row i of C, p = column j: Small = op(A) (M x K), Big(j, k) = op(B)(k, j)
+        p.S = (int)M;
+        p.P = (int)N;
+        p.small = A;
+        p.small_ss = a_n ? lda : 1;
+        p.small_sk = a_n ? 1 : lda;
+        p.big = B;
+        p.big_ld = ldb;
+        big_kcontig = !b_n;                 // B 'T' is stored N x K
+        p.c_s = ldc;
+        p.c_p = 1;
+    } else {
+        // s = column j of C, p = row i: Small(j, k) = op(B)(k, j), Big = op(A)
+        p.S = (int)N;
+        p.P = (int)M;
+        p.small = B;
+        p.small_ss = b_n ? 1 : ldb;
+        p.small_sk = b_n ? ldb : 1;
+        p.big = A;
+        p.big_ld = lda;
+        big_kcontig = a_n;                  // A 'N' is stored M x K
+        p.c_s = 1;
+        p.c_p = ldc;
+    }
+    const Geometry g = geometry(ta, tb, M, N, K, sms);
+    if (g.dot != big_kcontig) return SGEMM_ERR_UNSUPPORTED;   // the two views agree by construction
+    if (big_kcontig) {
+        const bool vec = al16(p.big) && p.big_ld % 4 == 0 && p.small_sk == 1 && al16(p.small) &&
+                         p.small_ss % 4 == 0;
+        timing_mark(s, true);
+        if (vec) launch_dot_s<true>(p, g.pb, s);
+        else launch_dot_s<false>(p, g.pb, s);
+        timing_mark(s, false);
+        return last_cuda_status();
+    }
+    p.kchunk = g.kchunk;
+    p.ksplit = g.ksplit;
+    if (p.ksplit > 1) {
+        void *ws = nullptr;
+        int st = workspace(s, (size_t)p.ksplit * p.S * p.P * sizeof(float), &ws, 2);
+        if (st != SGEMM_OK) return st;
+        p.partial = static_cast<float *>(ws);
+    }
+    const bool vec = al16(p.big) && p.big_ld % 4 == 0;
+    timing_mark(s, true);
+    int st = vec ? launch_axpy_s<true>(p, s) : launch_axpy_s<false>(p, s);
+    timing_mark(s, false);
+    if (st != SGEMM_OK) return st;
+    if (p.ksplit > 1) {
+        const int64_t n = (int64_t)p.S * p.P;
+        const int blocks = (int)std::min<int64_t>((n + gemv::THREADS - 1) / gemv::THREADS, 4 * sms);
+        gemv::gemv_ksum_kernel<<<blocks, gemv::THREADS, 0, s>>>(p);
+    }
+    return last_cuda_status();
+}
+
+}  // namespace sgemm_gb300

@@ -1,0 +1,20 @@
+// Thin GEMMs (min(M, N) <= kGemvMaxSmall) on the CUDA cores: the large
+// operand is streamed once.  Defined in gemv.cu.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace sgemm_gb300 {
+
+constexpr int64_t kGemvMaxSmall = 16;
+
+// CTAs of the main GEMV launch for this problem (what run_gemv launches).
+int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms);
+
+// Arguments already validated (check_args), M, N, K > 0, alpha != 0.
+int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+             int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+             cudaStream_t s, int sms);
+
+}  // namespace sgemm_gb300

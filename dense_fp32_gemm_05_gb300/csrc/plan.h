@@ -60,6 +60,19 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
                      int64_t ldb, int64_t ldc, bool a_al, bool b_al, bool c_al, int path,
                      int split, int sms, Plan *out) {
     Plan pl;
+    // Thin problems (min(M, N) <= 16, "Matmul II", section 8: decode's
+    // M = 1 to a few dozen) stream their large operand once on the CUDA
+    // cores; the tile paths would compute mostly padding.
+    if (path == SGEMM_PATH_GEMV || (path == SGEMM_PATH_AUTO && std::min(M, N) <= 16)) {
+        if (std::min(M, N) > 16) return SGEMM_ERR_UNSUPPORTED;
+        pl.path = SGEMM_PATH_GEMV;
+        pl.tile_m = (int)std::min(M, N);
+        pl.tile_n = 0;
+        pl.split = 1;
+        pl.vector = (a_al && b_al && lda % 4 == 0 && ldb % 4 == 0) ? 1 : 0;
+        *out = pl;
+        return 0;
+    }
     if (path == SGEMM_PATH_AUTO) {
         // 3xTF32 runs the tensor cores at 3 MMAs per product and beats the
         // CUDA-core path by 1.5x (1024^3) to 5x (8192^3) on GB300, but it

@@ -14,6 +14,7 @@
 #include "../../include/sgemm_gb300.h"
 #include "ffma_kernel.cuh"
 #include "plan.h"
+#include "gemv.h"
 #include "tc_gemm.h"
 
 namespace sgemm_gb300 {
@@ -201,7 +202,7 @@ int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
                      float *C, int64_t ldc, cudaStream_t s, int path, int split) {
     int st = check_args(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
     if (st != SGEMM_OK) return st;
-    if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_TF32) return SGEMM_ERR_ARG;
+    if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_GEMV) return SGEMM_ERR_ARG;
     if (split < 0) return SGEMM_ERR_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;
 
@@ -219,6 +220,8 @@ int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
     st = make_plan(ta, tb, M, N, K, lda, ldb, ldc, aligned16(A), aligned16(B), aligned16(C),
                    path, split, d->sms, &pl);
     if (st != SGEMM_OK) return st;
+    if (pl.path == SGEMM_PATH_GEMV)
+        return run_gemv(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms);
     if (pl.path == SGEMM_PATH_FFMA)
         return run_ffma(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s);
     return run_tc(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms);
@@ -250,7 +253,7 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
     int st = check_args(transA, transB, M, N, K, 1.0f, nullptr, lda, nullptr, ldb, 0.0f,
                         nullptr, ldc, /*pointers_checked=*/false);
     if (st != SGEMM_OK) return st;
-    if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_TF32 || split < 0 || num_sms <= 0)
+    if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_GEMV || split < 0 || num_sms <= 0)
         return SGEMM_ERR_ARG;
     Plan pl;
     st = make_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned != 0, b_aligned != 0,
@@ -264,6 +267,8 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
     if (out_ctas) {
         if (pl.path == SGEMM_PATH_FFMA) {
             *out_ctas = pl.dp_tiles + pl.ctas;
+        } else if (pl.path == SGEMM_PATH_GEMV) {
+            *out_ctas = gemv_ctas(transA, transB, M, N, K, num_sms);
         } else {
             // units of work; one CTA each (two for SM pairs), or one CTA (pair)
             // per SM (pair) walking them when no operand is split in the kernel

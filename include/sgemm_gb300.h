@@ -83,9 +83,15 @@ typedef enum {
                               operand split x = hi + lo into two TF32 parts
                               and the three products lo*hi + hi*lo + hi*hi
                               accumulated in fp32: fp32-level accuracy.      */
-    SGEMM_PATH_TF32 = 3    /* the same tensor-core kernel with only hi*hi:
+    SGEMM_PATH_TF32 = 3,   /* the same tensor-core kernel with only hi*hi:
                               single-pass TF32, LOWER accuracy than fp32
                               ("Optimising fp32 GEMM on A100", "Kernel 1").  */
+    SGEMM_PATH_GEMV = 4    /* thin problems, min(M, N) <= 16: CUDA-core fp32
+                              FMAs streaming the large operand once, no tiles
+                              ("Matmul II", section 8: dedicated GEMV kernels
+                              for decode's M = 1 to a few dozen).  AUTO takes
+                              it whenever min(M, N) <= 16; forced on a larger
+                              problem it returns SGEMM_ERR_UNSUPPORTED.       */
 } sgemm_path;
 
 /*

@@ -172,6 +172,22 @@ def test_plan_split_k_for_small_grids(lib):
     assert p["split"] == 3
 
 
+def test_plan_thin_problems_take_the_gemv_path(lib):
+    # min(M, N) <= 16 ("Matmul II", section 8: decode's M = 1 to a few dozen)
+    for (M, N, K) in [(1, 16384, 8192), (16, 4096, 4096), (16384, 8, 8192), (5, 5, 5)]:
+        st, p = sg.sgemm_plan("N", "T", M, N, K, K, K, N)
+        assert st == 0 and p["path"] == sg.PATH_GEMV, (M, N, K)
+        assert p["tile_m"] == min(M, N)
+    # 17 and up: the tile paths
+    st, p = sg.sgemm_plan("N", "N", 17, 4096, 4096, 4096, 4096, 4096)
+    assert st == 0 and p["path"] != sg.PATH_GEMV
+    # forced on a wide problem: refused
+    st, _ = sg.sgemm_plan("N", "N", 64, 64, 64, 64, 64, 64, path=sg.PATH_GEMV)
+    assert st == sg.SGEMM_ERR_UNSUPPORTED
+    st, _ = sg.sgemm_plan("N", "N", 64, 64, 64, 64, 64, 64, path=5)
+    assert st == sg.SGEMM_ERR_ARG
+
+
 def test_plan_forced_tensor_core_path(lib):
     st, p = sg.sgemm_plan("N", "N", 1024, 1024, 1024, 1024, 1024, 1024, path=sg.PATH_3XTF32)
     assert st == 0 and p["path"] == sg.PATH_3XTF32

@@ -1,0 +1,125 @@
+"""Parity of the thin-problem path (SGEMM_PATH_GEMV, min(M, N) <= 16) with the
+oracle: exact on small integers, within the fp32 bound on random inputs over
+both forms of the kernel (the large operand contiguous along K, or along
+the long dimension), both thin sides (few rows of C, few columns), ragged K
+and ragged long dimensions, padded leading dimensions and misaligned base
+pointers, and the K split across CTAs with its ordered reduction."""
+import itertools
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_05_gb300 as sg
+import gemm_inputs as gi
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")]
+
+
+def stored(op_mat, trans):
+    return np.ascontiguousarray(op_mat if trans == "N" else op_mat.T)
+
+
+def embed_ld(arr, pad):
+    out = np.full((arr.shape[0], arr.shape[1] + pad), np.nan, np.float32)
+    out[:, : arr.shape[1]] = arr
+    return out
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("thin", ["rows", "cols"])
+@pytest.mark.parametrize("S", [1, 3, 16])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_gemv_small_integers_exact(ta, tb, thin, S, misalign):
+    # |partial sums| < 2^24: every summation order gives the exact integer
+    P, K = 517, 1031
+    M, N = (S, P) if thin == "rows" else (P, S)
+    opA = gi.small_ints(11, (M, K))
+    opB = gi.small_ints(12, (K, N))
+    C = gi.small_ints(13, (M, N))
+    want = 2.0 * (opA.astype(np.int64) @ opB.astype(np.int64)) - 1.0 * C.astype(np.int64)
+    A, B = stored(opA, ta), stored(opB, tb)
+    off = (1, 3, 1) if misalign else (0, 0, 0)
+    st, out = gh.run(ta, tb, M, N, K, 2.0, A, A.shape[1], B, B.shape[1], -1.0, C, N,
+                     path=sg.PATH_GEMV, offsets=off)
+    assert st == 0
+    assert np.array_equal(out.astype(np.float64), want.astype(np.float64))
+
+
+def _cases():
+    rng = np.random.default_rng(23)
+    S_vals = [1, 2, 5, 8, 9, 15, 16]
+    P_vals = [1, 7, 129, 1000, 4097]
+    K_vals = [1, 3, 64, 300, 2049, 20000]
+    combos = list(itertools.product(S_vals, P_vals, K_vals))
+    picks = rng.choice(len(combos), size=36, replace=False)
+    out = []
+    for t, i in enumerate(picks):
+        S, P, K = combos[i]
+        ta, tb = LAYOUTS[t % 4]
+        thin = "rows" if (t // 4) % 2 == 0 else "cols"
+        out.append((t, S, P, K, ta, tb, thin))
+    # the K split across CTAs (long K, few blocks of the long dimension)
+    out.append((99, 4, 300, 40000, "N", "N", "rows"))
+    out.append((98, 2, 200, 30000, "T", "N", "cols"))
+    return out
+
+
+@pytest.mark.parametrize("t,S,P,K,ta,tb,thin", _cases())
+def test_gemv_random_within_bound(oracle_mod, t, S, P, K, ta, tb, thin):
+    M, N = (S, P) if thin == "rows" else (P, S)
+    opA = gi.random_matrix(600 + t, M, K)
+    opB = gi.random_matrix(700 + t, K, N)
+    C = gi.random_matrix(800 + t, M, N)
+    alpha, beta = [(1.0, 0.0), (-1.5, 0.5), (0.75, 1.0), (2.0, -1.0)][t % 4]
+    A, B = stored(opA, ta), stored(opB, tb)
+    pad = (t % 3, (t + 1) % 3)
+    A, B = embed_ld(A, pad[0]), embed_ld(B, pad[1])
+    ldc = N + t % 2
+    Cpad = embed_ld(C, ldc - N)
+    st, out = gh.run(ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta,
+                     C if beta else None, ldc, path=sg.PATH_GEMV,
+                     offsets=(t % 2, (t // 2) % 2, 0))
+    assert st == 0, (M, N, K)
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1],
+                                     beta, Cpad if beta else None, ldc)
+    rep = oracle_mod.compare(out, ref, bound, K, alpha)
+    assert rep["pass"], rep
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_gemv_is_the_selectors_choice(ta, tb):
+    # min(M, N) <= 16: sgemm() (AUTO) runs this path, bit for bit
+    M, N, K = 8, 3000, 777
+    A = stored(gi.random_matrix(31, M, K), ta)
+    B = stored(gi.random_matrix(32, K, N), tb)
+    st1, out1 = gh.run(ta, tb, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, None, N,
+                       path=sg.PATH_GEMV)
+    st2, out2 = gh.run(ta, tb, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, None, N,
+                       path=sg.PATH_AUTO)
+    assert st1 == 0 and st2 == 0
+    assert np.array_equal(out1.view(np.uint32), out2.view(np.uint32))
+
+
+def test_gemv_special_cases(oracle_mod):
+    # beta = 0 never reads C (NaN stays out); K = 0 and alpha = 0 scale C
+    M, N, K = 1, 900, 500
+    A = gi.random_matrix(41, M, K)
+    B = gi.random_matrix(42, K, N)
+    st, out = gh.run("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, path=sg.PATH_GEMV)
+    assert st == 0 and np.all(np.isfinite(out))
+    C = gi.random_matrix(43, M, N)
+    st, out = gh.run("N", "N", M, N, 0, 1.0, None, 1, None, N, 0.5, C, N, path=sg.PATH_GEMV)
+    assert st == 0 and np.array_equal(out, (np.float32(0.5) * C).astype(np.float32))
+    st, out = gh.run("N", "N", M, N, K, 0.0, A, K, B, N, -2.0, C, N, path=sg.PATH_GEMV)
+    assert st == 0 and np.array_equal(out, (np.float32(-2.0) * C).astype(np.float32))
+
+
+def test_gemv_forced_on_a_wide_problem_is_refused():
+    import torch
+    x = torch.zeros(64 * 64, device="cuda")
+    st = sg.sgemm_ex("N", "N", 64, 64, 64, 1.0, x.data_ptr(), 64, x.data_ptr(), 64, 0.0,
+                     x.data_ptr(), 64, torch.cuda.current_stream(), sg.PATH_GEMV, 0)
+    assert st == sg.SGEMM_ERR_UNSUPPORTED
