@@ -239,6 +239,66 @@ def reference_arm(args):
     return 0
 
 
+def workload_table(dev, stream, flush, ffma_peak, tf32_peak, hbm_gbs, reps=5):
+    """Every workload through sgemm() (the selector's path), device-timed with
+    L2 flushed between calls, against the roofline of the path that ran:
+    attainable = min(the path's compute peak, arithmetic intensity x HBM).
+    Inputs are drawn on the device (seeded, the workload's distribution):
+    this table times; the parity tests check."""
+    import torch
+    import dense_fp32_gemm_05_gb300 as sg
+
+    names = {sg.PATH_FFMA: "ffma", sg.PATH_3XTF32: "3xtf32", sg.PATH_TF32: "tf32",
+             sg.PATH_GEMV: "gemv"}
+    table = {}
+    for name, w in gi.WORKLOADS.items():
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        sa, sb, sc = w.stored_shapes()
+
+        def draw(shape):
+            if w.dist == "uniform":
+                return torch.rand(shape, generator=g, device=dev) * 2.0 - 1.0
+            return torch.randn(shape, generator=g, device=dev) * w.std
+        dA, dB = draw(sa), draw(sb)
+        dC = draw(sc) if w.beta != 0 else torch.zeros(sc, device=dev)
+        st, plan = sg.sgemm_plan(w.transA, w.transB, w.M, w.N, w.K, sa[1], sb[1], w.N)
+        path = names.get(plan["path"], str(plan["path"])) if st == 0 else "?"
+
+        def call():
+            st = sg.sgemm(w.transA, w.transB, w.M, w.N, w.K, w.alpha, dA.data_ptr(), sa[1],
+                          dB.data_ptr(), sb[1], w.beta, dC.data_ptr(), w.N, stream)
+            if st != 0:
+                raise sg.SgemmError(st)
+        call()
+        torch.cuda.synchronize(dev)
+        ev = []
+        for _ in range(reps):
+            flush.fill_(0.25)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        tfl = w.flops / (ms / 1e3) / 1e12
+        gbs = w.compulsory_bytes() / (ms / 1e3) / 1e9
+        compute = {"ffma": ffma_peak, "gemv": ffma_peak, "3xtf32": tf32_peak / 3.0,
+                   "tf32": tf32_peak}.get(path, ffma_peak)
+        hbm_roof = w.flops / w.compulsory_bytes() * hbm_gbs / 1e3
+        attain = min(compute, hbm_roof)
+        table[name] = {"path": path, "ms": round(ms, 4), "tflops": round(tfl, 3),
+                       "gbs": round(gbs, 1),
+                       "bound": "hbm" if hbm_roof < compute else
+                                ("tensor" if path in ("3xtf32", "tf32") else "alu"),
+                       "attainable_tflops": round(attain, 3), "frac": round(tfl / attain, 4)}
+        del dA, dB, dC
+    torch.cuda.empty_cache()
+    return table
+
+
 def workload_config(w, flushed=True):
     cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
            "layout": w.transA + w.transB, "alpha": w.alpha, "beta": w.beta,
@@ -383,8 +443,14 @@ def gpu_arm(args):
                         "max_rel": rep["max_rel"]})
         paths[name] = ent
 
+    # ---- every workload through the selector, against its path's roofline
+    workloads = None
+    if rank == 0 and not args.no_workloads:
+        workloads = workload_table(dev, stream, flush, ffma_peak, tf32_peak, peaks["hbm_gbs"])
+
     # ---- dominant kernel of the timed call: its launches measured alone
-    main_name = {sg.PATH_FFMA: "ffma", sg.PATH_3XTF32: "3xtf32", sg.PATH_TF32: "tf32"}[plan["path"]]
+    main_name = {sg.PATH_FFMA: "ffma", sg.PATH_3XTF32: "3xtf32", sg.PATH_TF32: "tf32",
+                 sg.PATH_GEMV: "gemv"}[plan["path"]]
     # the dominant kernel's own launches inside the timed region (library
     # timing hook: events around the main kernel only)
     k_ms = statistics.mean(kernel_ms) if kernel_ms else ms_per_step
@@ -457,7 +523,7 @@ def gpu_arm(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"], "samples": clocks["samples"]},
-            "plan": plan, "paths": paths, "ffma_peak_tflops": ffma_peak,
+            "plan": plan, "paths": paths, "workloads": workloads, "ffma_peak_tflops": ffma_peak,
             "wall_s_timed": t_wall, "peaks_source": peak_src,
         }
         print(json.dumps(line), flush=True)
@@ -515,6 +581,8 @@ def main():
                     help="profiling mode: run only W + K calls of this path on the "
                          "workload (no baseline, e2e or oracle) and print their timing")
     ap.add_argument("--no-check", action="store_true", help="skip the oracle sample check")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload table (every workload through sgemm)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
