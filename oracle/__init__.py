@@ -60,6 +60,9 @@ def _load():
             lib.oracle_gemm_f64.restype = ctypes.c_int
             lib.oracle_gemm_f32_seq.argtypes = common + [vp]
             lib.oracle_gemm_f32_seq.restype = ctypes.c_int
+            lib.oracle_gemm_epilogue_f64.argtypes = (
+                common[:13] + [vp, vp, ctypes.c_int] + common[13:] + [vp, vp])
+            lib.oracle_gemm_epilogue_f64.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -136,6 +139,51 @@ def gemm_f32_seq(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
         raise OracleArgError(f"oracle rejected argument {-st}")
     out = out[:n_out]
     return out.reshape(M, N) if points is None else out
+
+
+def gemm_epilogue_f64(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                      row_scale=None, bias=None, act=0, points=None):
+    """Reference and bound of the fused-epilogue GEMM
+    D = act(alpha * diag(row_scale) * op(A) op(B) + beta * C + bias[None, :])
+    (oracle.c, oracle_gemm_epilogue_f64).  row_scale: M fp32 values or None
+    (all ones); bias: N fp32 values or None (zero); act: 0 identity, 1 ReLU.
+    Returns (ref, bound) like gemm_f64."""
+    A, B, C = _prep(A, B, C)
+    rs = None if row_scale is None else np.ascontiguousarray(row_scale, dtype=np.float32)
+    bs = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    rows, cols, npts = _points(points)
+    n_out = npts if points is not None else M * N
+    ref = np.empty(max(n_out, 1), dtype=np.float64)
+    bound = np.empty(max(n_out, 1), dtype=np.float64)
+    st = _load().oracle_gemm_epilogue_f64(
+        transA.encode(), transB.encode(), M, N, K, float(alpha), _ptr(A), lda,
+        _ptr(B), ldb, float(beta), _ptr(C), ldc, _ptr(rs), _ptr(bs), int(act),
+        _ptr(rows), _ptr(cols), npts, ref.ctypes.data, bound.ctypes.data)
+    if st != 0:
+        raise OracleArgError(f"oracle rejected argument {-st}")
+    ref, bound = ref[:n_out], bound[:n_out]
+    if points is None:
+        ref, bound = ref.reshape(M, N), bound.reshape(M, N)
+    return ref, bound
+
+
+def compare_bound(candidate, ref, bound):
+    """Elementwise |cand - ref| <= bound everywhere (no exact special case:
+    the fused-epilogue bound already carries the epilogue's own roundings).
+    Same report fields as compare()."""
+    cand = np.asarray(candidate, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = np.asarray(bound, dtype=np.float64)
+    err = np.abs(cand - ref)
+    ok = bool(np.all(np.isfinite(cand))) and bool(np.all(err <= bound))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(bound > 0, err / np.where(bound > 0, bound, 1.0),
+                     np.where(err > 0, np.inf, 0.0))
+    worst = float(q.max()) if q.size else 0.0
+    nz = np.abs(ref) > 2.0 ** -60
+    max_rel = float((err[nz] / np.abs(ref[nz])).max()) if nz.any() else 0.0
+    return {"pass": ok, "max_err_over_bound": worst, "max_rel": max_rel,
+            "n_bad": int(np.count_nonzero(~(err <= bound))), "n": int(cand.size)}
 
 
 def compare(candidate, ref, bound, K, alpha):

@@ -189,3 +189,73 @@ int oracle_gemm_f32_seq(char ta, char tb, int64_t M, int64_t N, int64_t K,
     }
     return ORACLE_OK;
 }
+
+/*
+ * GEMM with a fused epilogue (the pages' "prologue and epilogue" fusion,
+ * "Optimising fp32 GEMM on A100", section "Performance comparison"; the
+ * axpby epilogue of "CuTe-ly writing an SM86 SGEMM", section "epilogue",
+ * extended by per-row scaling, "Matmul II", section 6, and a bias and an
+ * activation applied to each element):
+ *
+ *   D(i,j) = act( alpha * s_i * sum_k op(A)(i,k) op(B)(k,j)
+ *                 + beta * C(i,j) + bias_j )
+ *
+ * s = row_scale (M entries; NULL means every s_i = 1), bias (N entries;
+ * NULL means 0), act 0 = identity, 1 = ReLU (max(x, 0)).  Evaluated in
+ * fp64 exactly as the plain reference (alpha == 0: no product term, A and
+ * B not read; beta == 0: C not read), ReLU applied to the fp64 value.
+ * The bound adds the epilogue's own fp32 roundings (alpha*s_i, the fused
+ * multiply-add with beta*c, the bias add: at most three, each within 2^-24
+ * of the magnitudes involved) to the summation bound:
+ *   bound = (4*K + 3) * 2^-24 * (|alpha*s_i| * sum_k |a||b|
+ *                                + |beta|*|c| + |bias_j|);
+ * ReLU is 1-Lipschitz and leaves it valid.
+ */
+int oracle_gemm_epilogue_f64(char ta, char tb, int64_t M, int64_t N, int64_t K,
+                             float alpha, const float *A, int64_t lda,
+                             const float *B, int64_t ldb,
+                             float beta, const float *C, int64_t ldc,
+                             const float *row_scale, const float *bias, int act,
+                             const int64_t *rows, const int64_t *cols, int64_t npts,
+                             double *ref, double *bound)
+{
+    int st = check_args(ta, tb, M, N, K, lda, ldb, ldc);
+    if (st != ORACLE_OK) return st;
+    if (act != 0 && act != 1) return -16;
+    const int ta_n = is_n(ta), tb_n = is_n(tb);
+    const int64_t total = rows ? npts : M * N;
+    const double unit = ldexp(1.0, -24);
+
+    int64_t p;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
+    for (p = 0; p < total; ++p) {
+        const int64_t i = rows ? rows[p] : p / N;
+        const int64_t j = rows ? cols[p] : p % N;
+        const double scale = (double)alpha * (row_scale ? (double)row_scale[i] : 1.0);
+        double sum = 0.0, mag = 0.0;
+        const int64_t kend = (alpha == 0.0f) ? 0 : K;
+        for (int64_t k = 0; k < kend; ++k) {
+            const double a = (double)op_a(A, lda, ta_n, i, k);
+            const double b = (double)op_b(B, ldb, tb_n, k, j);
+            sum += a * b;
+            mag += fabs(a) * fabs(b);
+        }
+        double r = (alpha == 0.0f) ? 0.0 : scale * sum;
+        double m = fabs(scale) * mag;
+        if (beta != 0.0f) {
+            const double c = (double)C[i * ldc + j];
+            r += (double)beta * c;
+            m += fabs((double)beta) * fabs(c);
+        }
+        if (bias) {
+            r += (double)bias[j];
+            m += fabs((double)bias[j]);
+        }
+        if (act == 1 && r < 0.0) r = 0.0;
+        ref[p] = r;
+        bound[p] = (4.0 * (double)K + 3.0) * unit * m;
+    }
+    return ORACLE_OK;
+}

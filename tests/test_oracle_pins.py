@@ -327,3 +327,96 @@ def test_compare_detects_errors(oracle_mod):
     bad = good.copy()
     bad[0, 0] = np.nan
     assert not oracle_mod.compare(bad, ref, bound, K, 1.0)["pass"]
+
+
+# ------------------------------------------------------------ fused epilogue
+# D = act(alpha * s_i * (op(A) op(B))_ij + beta * C_ij + bias_j): each term
+# pinned against something other than the epilogue oracle itself.
+
+def _epi_inputs(seed, M, N, K):
+    rng = np.random.default_rng(seed)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    C = rng.uniform(-1, 1, (M, N)).astype(np.float32)
+    return A, B, C
+
+
+def test_epilogue_reduces_to_the_plain_definition(oracle_mod):
+    M, N, K = 7, 9, 13
+    A, B, C = _epi_inputs(1, M, N, K)
+    for beta, Cin in ((0.0, None), (0.5, C)):
+        r0, _ = oracle_mod.gemm_f64("N", "N", M, N, K, 1.5, A, K, B, N, beta, Cin, N)
+        r1, _ = oracle_mod.gemm_epilogue_f64("N", "N", M, N, K, 1.5, A, K, B, N, beta, Cin, N)
+        assert np.array_equal(r0, r1)
+
+
+def test_epilogue_row_scale_scales_rows(oracle_mod):
+    # powers of two: exact in fp64, so row i is exactly s_i times the plain row
+    M, N, K = 6, 5, 11
+    A, B, _ = _epi_inputs(2, M, N, K)
+    s = np.array([2.0 ** (i % 5 - 2) * (-1) ** i for i in range(M)], np.float32)
+    r0, _ = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    r1, _ = oracle_mod.gemm_epilogue_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N,
+                                         row_scale=s)
+    assert np.array_equal(r1, s.astype(np.float64)[:, None] * r0)
+
+
+def test_epilogue_bias_is_per_column(oracle_mod):
+    # alpha = beta = 0: only the bias is left, the same in every row; A, B, C unread
+    M, N = 4, 6
+    bias = np.arange(N, dtype=np.float32) - 2.5
+    r, b = oracle_mod.gemm_epilogue_f64("N", "N", M, N, 3, 0.0, None, 3, None, N, 0.0, None, N,
+                                        bias=bias)
+    assert np.array_equal(r, np.tile(bias.astype(np.float64), (M, 1)))
+    assert np.array_equal(b, (4 * 3 + 3) * 2.0 ** -24 * np.abs(np.tile(bias, (M, 1))).astype(np.float64))
+
+
+def test_epilogue_relu_clamps_the_identity_result(oracle_mod):
+    M, N, K = 8, 8, 17
+    A, B, C = _epi_inputs(3, M, N, K)
+    bias = np.linspace(-1, 1, N).astype(np.float32)
+    r_id, b_id = oracle_mod.gemm_epilogue_f64("T", "N", M, N, K, 1.0, np.ascontiguousarray(A.T), M,
+                                              B, N, 0.5, C, N, bias=bias, act=0)
+    r_re, b_re = oracle_mod.gemm_epilogue_f64("T", "N", M, N, K, 1.0, np.ascontiguousarray(A.T), M,
+                                              B, N, 0.5, C, N, bias=bias, act=1)
+    assert np.array_equal(r_re, np.maximum(r_id, 0.0))
+    assert np.array_equal(b_re, b_id)
+    assert (r_id < 0).any() and (r_id > 0).any()
+
+
+def test_epilogue_small_integers_exact(oracle_mod):
+    # every term an integer: the int64 computation is the exact answer
+    rng = np.random.default_rng(4)
+    M, N, K = 9, 7, 23
+    A = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    B = rng.integers(-8, 9, (N, K)).astype(np.float32)          # stored N x K ('T')
+    C = rng.integers(-8, 9, (M, N)).astype(np.float32)
+    s = rng.integers(-3, 4, M).astype(np.float32)
+    bias = rng.integers(-50, 51, N).astype(np.float32)
+    want = (2 * s.astype(np.int64)[:, None] * (A.astype(np.int64) @ B.astype(np.int64).T)
+            - 1 * C.astype(np.int64) + bias.astype(np.int64)[None, :])
+    for act in (0, 1):
+        r, _ = oracle_mod.gemm_epilogue_f64("N", "T", M, N, K, 2.0, A, K, B, K, -1.0, C, N,
+                                            row_scale=s, bias=bias, act=act)
+        w = want if act == 0 else np.maximum(want, 0)
+        assert np.array_equal(r, w.astype(np.float64))
+
+
+def test_epilogue_bound_closed_form(oracle_mod):
+    # all ones, alpha = 2, s_i = 3, beta = -1 (c = 1), bias = 5:
+    # bound = (4K + 3) 2^-24 (6 K + 1 + 5)
+    M, N, K = 3, 4, 10
+    A = np.ones((M, K), np.float32)
+    B = np.ones((K, N), np.float32)
+    C = np.ones((M, N), np.float32)
+    r, b = oracle_mod.gemm_epilogue_f64("N", "N", M, N, K, 2.0, A, K, B, N, -1.0, C, N,
+                                        row_scale=np.full(M, 3.0, np.float32),
+                                        bias=np.full(N, 5.0, np.float32))
+    assert np.all(r == 6.0 * K - 1.0 + 5.0)
+    assert np.allclose(b, (4 * K + 3) * 2.0 ** -24 * (6.0 * K + 1.0 + 5.0), rtol=0, atol=0)
+
+
+def test_epilogue_rejects_unknown_activation(oracle_mod):
+    with pytest.raises(oracle_mod.OracleArgError):
+        oracle_mod.gemm_epilogue_f64("N", "N", 2, 2, 2, 1.0, np.ones((2, 2), np.float32), 2,
+                                     np.ones((2, 2), np.float32), 2, 0.0, None, 2, act=7)
