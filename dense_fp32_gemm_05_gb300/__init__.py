@@ -15,7 +15,7 @@ import threading
 __all__ = [
     "SGEMM_OK", "SGEMM_ERR_CUDA", "SGEMM_ERR_TIMEOUT", "SGEMM_ERR_NOMEM",
     "SGEMM_ERR_UNSUPPORTED", "SGEMM_ERR_ARG", "SGEMM_ERR_SCRATCH", "PATH_AUTO", "PATH_FFMA",
-    "PATH_3XTF32", "PATH_TF32", "PATH_GEMV", "SgemmError", "library_path", "load",
+    "PATH_3XTF32", "PATH_TF32", "PATH_GEMV", "ACT_NONE", "ACT_RELU", "sgemm_epilogue", "SgemmError", "library_path", "load",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
     "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
@@ -35,6 +35,8 @@ PATH_FFMA = 1
 PATH_3XTF32 = 2
 PATH_TF32 = 3
 PATH_GEMV = 4
+ACT_NONE = 0
+ACT_RELU = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libsgemm_gb300.so"
@@ -61,6 +63,8 @@ def _declare(lib):
     lib.sgemm.restype = i32
     lib.sgemm_ex.argtypes = gemm_args + [i32, i32]
     lib.sgemm_ex.restype = i32
+    lib.sgemm_epilogue.argtypes = gemm_args[:13] + [vp, vp, i32, vp, i32, i32]
+    lib.sgemm_epilogue.restype = i32
     lib.sgemm_host.argtypes = gemm_args
     lib.sgemm_host.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
@@ -103,7 +107,7 @@ def load():
 
 def exported_symbols(lib=None):
     """Names of the entry points this binding declares, for export checks."""
-    return ["sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
+    return ["sgemm", "sgemm_ex", "sgemm_epilogue", "sgemm_host", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
             "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
             "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read"]
 
@@ -131,6 +135,15 @@ def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, strea
     """sgemm with the path and the FFMA split-K factor forced."""
     return load().sgemm_ex(_b(transA), _b(transB), M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                            _stream(stream), path, split)
+
+
+def sgemm_epilogue(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, row_scale=0,
+                   bias=0, activation=ACT_NONE, stream=None, path=PATH_AUTO, split=0) -> int:
+    """GEMM with the fused epilogue C = act(alpha * s_i * AB + beta * C + bias_j);
+    row_scale / bias are device addresses (0 = none)."""
+    return load().sgemm_epilogue(_b(transA), _b(transB), M, N, K, alpha, A, lda, B, ldb, beta,
+                                 C, ldc, row_scale or None, bias or None, activation,
+                                 _stream(stream), path, split)
 
 
 def sgemm_host(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

@@ -55,6 +55,7 @@
 #include <type_traits>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
 #include "ptx_util.cuh"
 
 namespace sgemm_gb300 {
@@ -81,6 +82,9 @@ struct Params {
     int sk_ctas;           // CTAs sharing the remaining tiles' iterations
     int64_t sk_iters;      // (tiles - dp_tiles) * kt, counted from tile dp_tiles
     int c_vec;             // C base 16-byte aligned and ldc % 4 == 0
+    const float *row_scale;   // fused epilogue: M row scales or null
+    const float *bias;        // N column biases or null
+    int act;                  // SGEMM_ACT_*
 };
 
 // First remaining-tile iteration of share c.
@@ -206,7 +210,9 @@ __device__ __forceinline__ float axpby(float alpha, float acc, float beta, float
 __device__ __forceinline__ void store_quad(const Params &p, int row, int col, float4 v) {
     if (row >= p.M || col >= p.N) return;
     float *dst = p.C + (int64_t)row * p.ldc + col;
-    const float alpha = p.alpha, beta = p.beta;
+    // alpha * s_row with a row scale (fused epilogue), else alpha
+    const float alpha = epi_alpha(p.alpha, p.row_scale, row), beta = p.beta;
+    const bool tail = p.bias || p.act != SGEMM_ACT_NONE;
     if (p.c_vec && col + 3 < p.N) {
         float4 o;
         if (beta == 0.0f) {
@@ -217,14 +223,22 @@ __device__ __forceinline__ void store_quad(const Params &p, int row, int col, fl
             o = make_float4(axpby(alpha, v.x, beta, c.x), axpby(alpha, v.y, beta, c.y),
                             axpby(alpha, v.z, beta, c.z), axpby(alpha, v.w, beta, c.w));
         }
+        if (tail) {
+            o.x = epi_tail(o.x, p.bias, col, p.act);
+            o.y = epi_tail(o.y, p.bias, col + 1, p.act);
+            o.z = epi_tail(o.z, p.bias, col + 2, p.act);
+            o.w = epi_tail(o.w, p.bias, col + 3, p.act);
+        }
         *reinterpret_cast<float4 *>(dst) = o;
     } else {
         const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (col + j < p.N) {
-                dst[j] = (beta == 0.0f) ? __fmul_rn(alpha, vv[j])
-                                        : axpby(alpha, vv[j], beta, dst[j]);
+                float t = (beta == 0.0f) ? __fmul_rn(alpha, vv[j])
+                                         : axpby(alpha, vv[j], beta, dst[j]);
+                if (tail) t = epi_tail(t, p.bias, col + j, p.act);
+                dst[j] = t;
             }
         }
     }
@@ -452,14 +466,17 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
 }
 
 // C = beta * C (C = 0 when beta == 0, without reading C): the K == 0 and
-// alpha == 0 quick return.
-__global__ void scale_c_kernel(int M, int N, float beta, float *__restrict__ C, int64_t ldc) {
+// alpha == 0 quick return; with a fused epilogue's bias and activation
+// applied after it (the product term is zero, so a row scale has no effect).
+__global__ void scale_c_kernel(int M, int N, float beta, float *__restrict__ C, int64_t ldc,
+                               const float *bias, int act) {
     const int64_t total = (int64_t)M * N;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = idx / N, col = idx - row * N;
         float *dst = C + row * ldc + col;
-        *dst = (beta == 0.0f) ? 0.0f : __fmul_rn(beta, *dst);
+        const float t = (beta == 0.0f) ? 0.0f : __fmul_rn(beta, *dst);
+        *dst = epi_tail(t, bias, (int)col, act);
     }
 }
 

@@ -55,12 +55,18 @@ struct Params {
     float alpha, beta;
     float *partial;                    // axpy form, K split: [ksplit][S][P]
     int ksplit, kchunk;                // K range of CTA y: [y * kchunk, min(K, +kchunk))
+    int rows_thin;                     // s is the row of C (M small), else its column
+    const float *row_scale;            // fused epilogue: M row scales or null
+    const float *bias;                 // N column biases or null
+    int act;                           // SGEMM_ACT_*
 };
 
 __device__ __forceinline__ void store_out(const Params &p, int s, int q, float v) {
     float *dst = p.C + (int64_t)s * p.c_s + (int64_t)q * p.c_p;
-    *dst = p.beta == 0.0f ? __fmul_rn(p.alpha, v)
-                          : __fmaf_rn(p.alpha, v, __fmul_rn(p.beta, *dst));
+    const int row = p.rows_thin ? s : q, col = p.rows_thin ? q : s;
+    const float a = epi_alpha(p.alpha, p.row_scale, row);
+    const float t = p.beta == 0.0f ? __fmul_rn(a, v) : __fmaf_rn(a, v, __fmul_rn(p.beta, *dst));
+    *dst = epi_tail(t, p.bias, col, p.act);
 }
 
 // ------------------------------------------------------------ dot form
@@ -349,7 +355,7 @@ int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
 
 int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
              int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
-             cudaStream_t s, int sms) {
+             cudaStream_t s, int sms, const Epilogue &epi) {
     if (std::min(M, N) > kGemvMaxSmall) return SGEMM_ERR_UNSUPPORTED;
     const bool a_n = is_notrans(ta), b_n = is_notrans(tb);
     gemv::Params p{};
@@ -357,6 +363,10 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
     p.alpha = alpha;
     p.beta = beta;
     p.C = C;
+    p.rows_thin = M <= N;
+    p.row_scale = epi.row_scale;
+    p.bias = epi.bias;
+    p.act = epi.act;
     bool big_kcontig;
     if (M <= N) {
         // s = row i of C, p = column j: Small = op(A) (M x K), Big(j, k) = op(B)(k, j)

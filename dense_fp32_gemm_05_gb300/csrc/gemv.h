@@ -5,6 +5,8 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
+
 namespace sgemm_gb300 {
 
 constexpr int64_t kGemvMaxSmall = 16;
@@ -15,6 +17,6 @@ int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms);
 // Arguments already validated (check_args), M, N, K > 0, alpha != 0.
 int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
              int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
-             cudaStream_t s, int sms);
+             cudaStream_t s, int sms, const Epilogue &epi = Epilogue{});
 
 }  // namespace sgemm_gb300

@@ -131,7 +131,8 @@ static void launch_ffma_t(const ffma::Params &p, int grid, cudaStream_t s) {
 // static-scratch entry point).
 static ffma::Params ffma_params(const Plan &pl, int64_t M, int64_t N, int64_t K, float alpha,
                                 const float *A, int64_t lda, const float *B, int64_t ldb,
-                                float beta, float *C, int64_t ldc) {
+                                float beta, float *C, int64_t ldc,
+                                const Epilogue &epi = Epilogue{}) {
     ffma::Params p{};
     p.A = A; p.B = B; p.C = C; p.partial = nullptr;
     p.lda = lda; p.ldb = ldb; p.ldc = ldc;
@@ -146,6 +147,9 @@ static ffma::Params ffma_params(const Plan &pl, int64_t M, int64_t N, int64_t K,
     p.sk_iters = (tiles - p.dp_tiles) * p.kt;
     p.sk_ctas = p.sk_iters == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(pl.ctas, p.sk_iters));
     p.c_vec = pl.c_vector;
+    p.row_scale = epi.row_scale;
+    p.bias = epi.bias;
+    p.act = epi.act;
     return p;
 }
 
@@ -176,8 +180,8 @@ static int launch_ffma(const ffma::Params &p, char ta, char tb, bool vec, cudaSt
 
 static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K,
                     float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
-                    float beta, float *C, int64_t ldc, cudaStream_t s) {
-    ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+                    float beta, float *C, int64_t ldc, cudaStream_t s, const Epilogue &epi) {
+    ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi);
     const bool partials = ffma_has_partials(p);
     if (partials) {
         void *ws = nullptr;
@@ -199,7 +203,8 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
 
 int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
                      const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
-                     float *C, int64_t ldc, cudaStream_t s, int path, int split) {
+                     float *C, int64_t ldc, cudaStream_t s, int path, int split,
+                     const Epilogue &epi) {
     int st = check_args(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
     if (st != SGEMM_OK) return st;
     if (path < SGEMM_PATH_AUTO || path > SGEMM_PATH_GEMV) return SGEMM_ERR_ARG;
@@ -212,8 +217,9 @@ int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
     if (!(d->cc_major == 10 && d->cc_minor == 3)) return SGEMM_ERR_UNSUPPORTED;
 
     if (K == 0 || alpha == 0.0f) {
-        if (beta == 1.0f) return SGEMM_OK;
-        ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc);
+        if (beta == 1.0f && !epi.bias && epi.act == SGEMM_ACT_NONE) return SGEMM_OK;
+        ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc,
+                                                                     epi.bias, epi.act);
         return launch_status();
     }
     Plan pl;
@@ -221,10 +227,10 @@ int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
                    path, split, d->sms, &pl);
     if (st != SGEMM_OK) return st;
     if (pl.path == SGEMM_PATH_GEMV)
-        return run_gemv(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms);
+        return run_gemv(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms, epi);
     if (pl.path == SGEMM_PATH_FFMA)
-        return run_ffma(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s);
-    return run_tc(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms);
+        return run_ffma(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, epi);
+    return run_tc(pl, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, d->sms, epi);
 }
 
 }  // namespace sgemm_gb300
@@ -243,6 +249,20 @@ extern "C" int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t 
                         float *C, int64_t ldc, sgemm_stream_t stream, int path, int split) {
     return gemm_impl(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                      reinterpret_cast<cudaStream_t>(stream), path, split);
+}
+
+extern "C" int sgemm_epilogue(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                              float alpha, const float *A, int64_t lda, const float *B,
+                              int64_t ldb, float beta, float *C, int64_t ldc,
+                              const float *row_scale, const float *bias, int activation,
+                              sgemm_stream_t stream, int path, int split) {
+    if (activation != SGEMM_ACT_NONE && activation != SGEMM_ACT_RELU) return -16;
+    Epilogue epi;
+    epi.row_scale = row_scale;
+    epi.bias = bias;
+    epi.act = activation;
+    return gemm_impl(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     reinterpret_cast<cudaStream_t>(stream), path, split, epi);
 }
 
 extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
@@ -421,7 +441,8 @@ extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, in
     if (!(d->cc_major == 10 && d->cc_minor == 3)) return SGEMM_ERR_UNSUPPORTED;
     if (K == 0 || alpha == 0.0f) {
         if (beta == 1.0f) return SGEMM_OK;
-        ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc);
+        ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc,
+                                                                     nullptr, SGEMM_ACT_NONE);
         return launch_status();
     }
     Plan pl;

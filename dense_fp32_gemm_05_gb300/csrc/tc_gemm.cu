@@ -115,6 +115,9 @@ struct Params {
     int fuse_a, fuse_b;         // operand loaded raw (fp32) and split in shared memory
     int units;                  // dp_tiles + (tiles - dp_tiles) * tail_nsplit
     unsigned long long wait_ns; // bounded-wait limit
+    const float *row_scale;     // fused epilogue: M row scales or null
+    const float *bias;          // N column biases or null
+    int act;                    // SGEMM_ACT_*
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -762,7 +765,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();
                 const int col = n0 + c * 32 + lane;
-                if (col < p.N) {
+                if (col < p.N && (p.row_scale || p.bias || p.act != SGEMM_ACT_NONE)) {
+                    // fused epilogue: alpha * s_row, + bias_col, activation
+                    float *__restrict__ dst = p.C + (int64_t)row0 * p.ldc + col;
+#pragma unroll 4
+                    for (int rr = 0; rr < rows_here; ++rr) {
+                        const float a_r = epi_alpha(alpha, p.row_scale, row0 + rr);
+                        const float v = stg[rr * EPI_LD + lane];
+                        float t = beta == 0.0f
+                                      ? __fmul_rn(a_r, v)
+                                      : __fmaf_rn(a_r, v, __fmul_rn(beta, dst[(int64_t)rr * p.ldc]));
+                        dst[(int64_t)rr * p.ldc] = epi_tail(t, p.bias, col, p.act);
+                    }
+                } else if (col < p.N) {
                     float *__restrict__ dst = p.C + (int64_t)row0 * p.ldc + col;
                     if (beta == 0.0f) {
 #pragma unroll 8
@@ -1042,7 +1057,7 @@ static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int
 
 int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
            const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-           int64_t ldc, cudaStream_t s, int sms) {
+           int64_t ldc, cudaStream_t s, int sms, const Epilogue &epi) {
     const bool three = pl.path == SGEMM_PATH_3XTF32;
     const int BN = pl.tile_n;
     const int Kp = (int)((K + tc::KPAD - 1) / tc::KPAD) * tc::KPAD;
@@ -1116,6 +1131,9 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.num_kb = Kp / bk;
     p.fuse_a = fuse_a;
     p.fuse_b = fuse_b;
+    p.row_scale = epi.row_scale;
+    p.bias = epi.bias;
+    p.act = epi.act;
     p.units = p.dp_tiles + (p.tiles_m * p.tiles_n - p.dp_tiles) * nsplit;
     {
         std::lock_guard<std::mutex> lk(g_tc_mu);

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "plan.h"
 
 namespace sgemm_gb300 {
@@ -12,7 +13,7 @@ namespace sgemm_gb300 {
 // Runs the tensor-core path chosen in `pl` (SGEMM_PATH_3XTF32 or _TF32).
 int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
            const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-           int64_t ldc, cudaStream_t s, int sms);
+           int64_t ldc, cudaStream_t s, int sms, const Epilogue &epi = Epilogue{});
 
 // Reads and clears the current device's sticky device error word.
 int tc_take_device_error();
@@ -30,6 +31,6 @@ int workspace(cudaStream_t stream, size_t bytes, void **out, int which = 0);
 // The whole device-pointer GEMM call (checks, quick returns, selector, launch).
 int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
               int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
-              cudaStream_t s, int path, int split);
+              cudaStream_t s, int path, int split, const Epilogue &epi = Epilogue{});
 
 }  // namespace sgemm_gb300

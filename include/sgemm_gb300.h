@@ -66,6 +66,12 @@ typedef enum {
                                   sgemm_ffma_static_scratch holds            */
 } sgemm_status;
 
+/* Activation of the fused epilogue (sgemm_epilogue). */
+typedef enum {
+    SGEMM_ACT_NONE = 0,
+    SGEMM_ACT_RELU = 1     /* max(x, 0); NaN passes through */
+} sgemm_activation;
+
 /* Arithmetic path.  AUTO lets the per-shape selector choose among the
    fp32-accurate paths (FFMA and 3xTF32); TF32 is never chosen by AUTO. */
 typedef enum {
@@ -119,6 +125,38 @@ int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
              const float *B, int64_t ldb,
              float beta, float *C, int64_t ldc, sgemm_stream_t stream,
              int path, int split);
+
+/*
+ * sgemm_epilogue - the GEMM with a fused epilogue, on every path:
+ *
+ *   C(i,j) = act( alpha * s_i * (op(A) op(B))(i,j) + beta * C(i,j) + bias_j )
+ *
+ * "Optimising fp32 GEMM on A100", section "Performance comparison": GEMM
+ * kernels are fused with the work before and after them as prologue and
+ * epilogue; "CuTe-ly writing an SM86 SGEMM", section "epilogue": other
+ * epilogues swap in for alpha/beta; "Matmul II", section 6: per-row scaling
+ * as position-dependent work on the accumulator.
+ *
+ *   row_scale   device pointer to M fp32 values s_i, or NULL (all ones)
+ *   bias        device pointer to N fp32 values bias_j, or NULL (zero)
+ *   activation  sgemm_activation: SGEMM_ACT_NONE or SGEMM_ACT_RELU
+ *   path, split as in sgemm_ex (0, 0: the selector)
+ *
+ * Evaluated once per output in fp32 in this order: a_i = alpha * s_i,
+ * t = a_i * acc (beta == 0: C not read) or fma(a_i, acc, beta * C(i,j)),
+ * t = t + bias_j, then the activation.  With row_scale = bias = NULL and
+ * SGEMM_ACT_NONE it is sgemm_ex, bit for bit.  When K == 0 or alpha == 0
+ * the product term is absent: C = act(beta * C + bias).  The vectors are
+ * caller-owned device memory, read only, and must hold M and N values;
+ * their sizes cannot be checked.  Other arguments and errors as sgemm_ex;
+ * an unknown activation returns -16.
+ */
+int sgemm_epilogue(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                   float alpha, const float *A, int64_t lda,
+                   const float *B, int64_t ldb,
+                   float beta, float *C, int64_t ldc,
+                   const float *row_scale, const float *bias, int activation,
+                   sgemm_stream_t stream, int path, int split);
 
 /*
  * sgemm_host - the same operation on HOST buffers (same arguments and

@@ -78,6 +78,18 @@ def test_argument_validation_without_gpu(lib, args, want):
     assert sg.sgemm_ex(*args, path=sg.PATH_FFMA, split=1) == want
 
 
+def test_epilogue_argument_validation_without_gpu(lib):
+    # checked before any CUDA call: unknown activation, then the GEMM arguments
+    assert sg.sgemm_epilogue("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4,
+                             activation=3) == -16
+    assert sg.sgemm_epilogue("Q", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4,
+                             bias=FAKE, activation=sg.ACT_RELU) == -1
+    assert sg.sgemm_epilogue("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 3,
+                             row_scale=FAKE) == -13
+    assert sg.sgemm_epilogue("N", "N", 0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4,
+                             bias=FAKE, activation=sg.ACT_RELU) == sg.SGEMM_OK
+
+
 def test_quick_return_touches_nothing(lib):
     # M == 0 / N == 0: nothing to do, valid with null pointers, no CUDA call
     assert sg.sgemm("N", "N", 0, 5, 7, 1.0, 0, 7, 0, 5, 0.0, 0, 5) == sg.SGEMM_OK
