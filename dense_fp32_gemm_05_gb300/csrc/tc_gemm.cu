@@ -66,9 +66,11 @@ __device__ unsigned int g_error;        // sticky device error word (per device)
 // PAIR: a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2 (M = 256): each CTA holds its 128 rows of A and
 // half (BN / 2 columns) of B, and its 128 rows of the accumulator.
-template <int BN, bool THREE, bool PAIR = false>
+// WIDE: 3xTF32 with 32-wide k-blocks (128-byte rows): the skinny tiles whose
+// raw A streams from HBM, where 64-byte row pieces halve DRAM efficiency.
+template <int BN, bool THREE, bool PAIR = false, bool WIDE = false>
 struct Cfg {
-    static constexpr int BK = KBlock<THREE>::BK;
+    static constexpr int BK = WIDE ? 32 : KBlock<THREE>::BK;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 4;
     static constexpr int PARTS = THREE ? 2 : 1;
@@ -365,16 +367,15 @@ __device__ __forceinline__ void split_tile(uint32_t hi, uint32_t lo, int n16, in
 // Split of this thread's row of a raw A tile (TMA-swizzled, rows of BK
 // floats) into tensor memory: row r = 32 q + lane, k = half * BK/2 .. +BK/2;
 // hi = round(x) to columns tslot + k, lo = round(x - hi) to tslot + BK + k
-// (THREE only).  TMA's 64-byte swizzle (BK = 16) flips the 16-byte chunk
-// index by bits 1-2 of the row, its 128-byte swizzle (BK = 32) by bits 0-2.
+// (THREE only).  TMA's 64-byte swizzle (BK_ = 16) flips the 16-byte chunk
+// index by bits 1-2 of the row, its 128-byte swizzle (BK_ = 32) by bits 0-2.
 // `taddr` is the warp's lane quarter and column tslot of tensor memory.
-template <bool THREE>
+template <bool THREE, int BK_>
 __device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, int q, int half,
                                                 int lane) {
-    constexpr int BK_ = KBlock<THREE>::BK;
     constexpr int KH = BK_ / 2;                       // k values per thread: 8 or 16
     const int r = q * 32 + lane;
-    const uint32_t sw = THREE ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
+    const uint32_t sw = BK_ == 16 ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
     const uint32_t row = raw + (uint32_t)(r * BK_ * 4);
 #pragma unroll
     for (int g = 0; g < KH / 8; ++g) {                // 8 k values per TMEM store
@@ -448,7 +449,7 @@ __device__ __forceinline__ void unit_of(const Params &p, int TM, int BN_, int u,
 // both CTAs (multicast); every epilogue warp of both CTAs hands the
 // accumulator back on the leader's acce barrier.  Halving B per SM cuts the
 // shared-memory traffic per flop by a third.
-template <int BN, bool THREE, bool PAIR>
+template <int BN, bool THREE, bool PAIR, bool WIDE>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi,
                    const __grid_constant__ CUtensorMap tm_alo,
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_blo,
                    const __grid_constant__ CUtensorMap tm_bhi_tail,
                    const __grid_constant__ CUtensorMap tm_blo_tail, const Params p) {
-    using K_ = Cfg<BN, THREE, PAIR>;
+    using K_ = Cfg<BN, THREE, PAIR, WIDE>;
     constexpr int BK = K_::BK;
     constexpr int NW = WORKERS / 32;                   // split / epilogue warps
     constexpr int TM = PAIR ? 2 * BM : BM;             // tile rows
@@ -716,7 +717,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // them: no shared-memory traffic for A in the MMAs
                         const uint32_t slot = tmem + ((uint32_t)(q * 32) << 16) +
                                               (uint32_t)(K_::A_TMEM_COL + s * K_::A_SLOT_COLS);
-                        split_a_to_tmem<THREE>(a_hi(s), slot, q, half, lane);
+                        split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
                         tmem_st_wait();
                         tc_fence_before();
                     }
@@ -991,10 +992,10 @@ static void launch_split_pair(bool three, const tc::SplitJob &a, const tc::Split
     else tc::split_pair_kernel<false><<<blocks, 256, 0, s>>>(a, b);
 }
 
-template <int BN, bool THREE, bool PAIR>
+template <int BN, bool THREE, bool PAIR, bool WIDE = false>
 static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, cudaStream_t s) {
-    using K_ = tc::Cfg<BN, THREE, PAIR>;
-    auto kern = tc::tc_gemm_kernel<BN, THREE, PAIR>;
+    using K_ = tc::Cfg<BN, THREE, PAIR, WIDE>;
+    auto kern = tc::tc_gemm_kernel<BN, THREE, PAIR, WIDE>;
     // the shared-memory opt-in is a per-device function attribute
     static uint64_t attr_done = 0;   // bit d: set on device d
     int dev = 0;
@@ -1097,7 +1098,11 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     if (st != SGEMM_OK) return st;
 
     const int nsplit = std::max(1, pl.tail_nsplit);
-    const int bk = three ? tc::KBlock<true>::BK : tc::KBlock<false>::BK;
+    // 64-wide 3xTF32 tiles that split A into TMEM stream raw A from HBM: 32-wide
+    // k-blocks (128-byte rows) there (skinny 16384 x 64 x 8192: 2.3 -> 4.5 TB/s
+    // of A in the TF32 mode, which always has them)
+    const bool wide = three && BN == 64 && fuse_a && !pair;
+    const int bk = (wide || !three) ? 32 : tc::KBlock<true>::BK;
     CUtensorMap maps[6];
     bool ok;
     if (fuse_a) {
@@ -1152,6 +1157,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     if (BN == 128)
         return three ? launch_main_any<128, true>(pair, maps, p, grid, s)
                      : launch_main_any<128, false>(pair, maps, p, grid, s);
+    if (wide) return launch_main<64, true, false, true>(maps, p, grid, s);
     return three ? launch_main_any<64, true>(pair, maps, p, grid, s)
                  : launch_main_any<64, false>(pair, maps, p, grid, s);
 }
