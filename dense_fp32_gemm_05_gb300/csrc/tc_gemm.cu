@@ -1,33 +1,39 @@
 // Tensor-core path for sm_103a: tcgen05 kind::tf32 MMAs into TMEM, operands
 // brought into shared memory by TMA, fp32 accuracy by a 3xTF32 split.
 //
-// Each fp32 operand x is split once, in a pre-pass, into two TF32 numbers:
-// hi = rna_tf32(x), lo = rna_tf32(x - hi) (x - hi is exact in fp32).  Then
+// Each fp32 operand x is split into two TF32 numbers: hi = rna_tf32(x),
+// lo = rna_tf32(x - hi) (x - hi is exact in fp32).  Then
 //   a*b = a_hi*b_hi + a_hi*b_lo + a_lo*b_hi + a_lo*b_lo
 // and the last term (~2^-22 |ab|) is dropped: the three TF32 products are
 // accumulated in fp32 in TMEM.  Single-pass TF32 keeps only a_hi*b_hi (the
 // tensor-core mode of "Optimising fp32 GEMM on A100", kernels 1-7, which
-// trade accuracy for speed).
+// trade accuracy for speed).  An operand is split either by a pre-pass into
+// a K-contiguous workspace, or, when its rows already run along K, inside
+// the kernel: A into tensor memory, B in shared memory.
 //
-// Kernel layout (one CTA per 128 x BN tile of C, 320 threads):
-//   warp 0, one lane : TMA producer - per k-block of 32 (128 bytes, the
-//                      128-byte swizzle span) loads A_hi/A_lo (128 x 32) and
-//                      B_hi/B_lo (BN x 32) into a ring of shared stages,
-//                      completing on the stage's "full" mbarrier;
-//   warp 1           : allocates BN TMEM columns; one lane issues the MMAs
-//                      (M = 128, N = BN, K = 8) for each k-block and commits
-//                      them to the stage's "empty" mbarrier, then to the
-//                      "accumulator ready" mbarrier after the last block;
-//   warps 2..9       : while the main loop runs, split the operands that
-//                      were loaded raw (hi over the raw tile, lo beside it);
-//                      then the epilogue - tcgen05.ld of the 128 x BN
-//                      accumulator (warp w reads TMEM lanes 32*(w%4)..+31 =
-//                      its rows), C = alpha*acc + beta*C, stores.
+// Kernel (320 threads; tiles of 128 x BN, or 256 x BN on a pair of SMs):
+//   warp 0, one lane : TMA producer - per k-block (16 wide for 3xTF32, 32 for
+//                      TF32 and for narrow tiles with A split in TMEM) loads
+//                      the hi/lo (or raw) A and B tiles into a ring of
+//                      shared stages, completing on the stage's "full"
+//                      mbarrier (for a pair: the leader's, counting both);
+//   warp 1           : allocates TMEM; one lane of the leader issues the MMAs
+//                      (K = 8 per instruction) and commits them to the
+//                      stage's "empty" mbarrier, and after a tile's last
+//                      k-block to the "accumulator full" one;
+//   warps 2..9       : split raw tiles while the main loop runs, then the
+//                      epilogue - tcgen05.ld of the accumulator (warp w reads
+//                      TMEM lanes 32*(w%4)..+31 = its rows), the fused
+//                      alpha/beta (+ row scale, bias, activation) epilogue,
+//                      row-contiguous stores.
+// CTAs are persistent (one per SM, or per SM pair) when no operand is split
+// in the kernel: the stage ring runs on across tiles and two TMEM
+// accumulators alternate, so a tile's epilogue overlaps the next main loop.
 // The multi-stage ring is the asynchronous copy pipeline of "CuTe-ly
 // writing an SM86 SGEMM" (section "mainloop") and "Matmul II" (section 7)
 // rebuilt on TMA + mbarriers; the operand and accumulator placement is
-// Blackwell's (shared-memory descriptors, TMEM) and has no counterpart on
-// the pages.
+// Blackwell's (shared-memory descriptors, TMEM, CTA pairs) and has no
+// counterpart on the pages.
 // Every mbarrier wait is bounded (%globaltimer): on expiry the thread sets
 // the library's device error word, stops its role, drains what it issued
 // (also bounded) and the CTA frees its TMEM and exits.
@@ -48,7 +54,8 @@ constexpr int BM = 128;
 // k-block width in fp32: 3xTF32 uses 16 (64-byte rows, 64-byte swizzle: six
 // MMAs per block and twice the stages); single-pass TF32 uses 32 (128-byte
 // rows and swizzle: four MMAs per block, so the per-block barrier round trip
-// of the MMA thread stays small against the tensor work).
+// of the MMA thread stays small against the tensor work).  Cfg's WIDE
+// variant gives 3xTF32 32-wide blocks too.
 template <bool THREE> struct KBlock { static constexpr int BK = THREE ? 16 : 32; };
 constexpr int KPAD = 32;               // K padding of the split operands
 constexpr int THREADS = 320;               // 10 warps: TMA, MMA, 8 split/epilogue
