@@ -53,6 +53,7 @@ struct Plan {
     int fuse_a = 1;       // tensor cores: split A in shared memory when its layout allows
     int fuse_b = 1;       // tensor cores: same for B
     int pair = 0;         // tensor cores: 256-row tiles on a pair of SMs (cta_group::2)
+    int tc_sk = 0;        // tensor cores: stream-K CTAs sharing all k-block iterations (0: off)
 };
 
 // Chooses path, tile, split and vectorisation.  `path`/`split` 0 = auto.
@@ -164,6 +165,43 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
                 pl.dp_tiles = (int)full;
                 pl.tail_nsplit = ns;
             }
+        }
+        // Stream-K on single SMs: with fewer 128-row tiles than SMs, the
+        // tiles x k-blocks iterations are shared in equal contiguous ranges
+        // by up to one CTA per SM (at least 8 k-blocks each), so all CTAs
+        // end together; tiles that several CTAs share leave partial sums for
+        // a fixup pass.  Modelled in microseconds: a tile's main loop at the
+        // measured MMA rate (2047 MAC per clock per SM at ~1.9 GHz; 0.75 of
+        // it reached on 128- and 256-wide tiles, 0.45 on 64-wide ones), the
+        // fixup as 4 us plus its partial-tile traffic at 6 TB/s; taken when
+        // 3 % faster than the choice above.  A forced split s > 1 runs
+        // stream-K with min(s x tiles, 8 x SMs, iterations) CTAs; split = 1
+        // never does.
+        const bool three = pl.path == SGEMM_PATH_3XTF32;
+        const int64_t kp = (K + 31) / 32 * 32;
+        const int64_t nkb = kp / ((three && !(pl.tile_n == 64 && pl.fuse_a)) ? 16 : 32);
+        const int64_t tiles1 = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
+        const int64_t iters = tiles1 * nkb;
+        int64_t g_sk = 0;
+        if (split > 1) {
+            g_sk = std::min<int64_t>(std::min<int64_t>(tiles1 * split, 8LL * sms), iters);
+        } else if (split == 0 && tiles1 < sms) {
+            const int64_t g = std::min<int64_t>(sms, iters / 8);
+            if (g > tiles1) {
+                const double rate = 2047.0 * 1900.0 * (pl.tile_n >= 128 ? 0.75 : 0.45);
+                const double tile_us = 128.0 * pl.tile_n * (double)kp * (three ? 3 : 1) / rate;
+                const double fix = 4.0 + (double)(g + tiles1) * 128.0 * pl.tile_n * 8.0 / 6.0e6;
+                const double t_sk = (double)iters / (double)g / (double)nkb * tile_us + fix;
+                if (t_sk < 0.97 * best * tile_us) g_sk = g;
+            }
+        }
+        if (g_sk > 0) {
+            pl.pair = 0;
+            pl.tile_m = 128;
+            pl.dp_tiles = (int)tiles1;
+            pl.tail_nsplit = 1;
+            pl.tc_sk = (int)g_sk;
+            pl.split = (int)((g_sk + tiles1 - 1) / tiles1);
         }
     }
     *out = pl;

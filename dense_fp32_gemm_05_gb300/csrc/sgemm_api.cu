@@ -289,6 +289,8 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
             *out_ctas = pl.dp_tiles + pl.ctas;
         } else if (pl.path == SGEMM_PATH_GEMV) {
             *out_ctas = gemv_ctas(transA, transB, M, N, K, num_sms);
+        } else if (pl.tc_sk > 0) {
+            *out_ctas = pl.tc_sk;   // stream-K: one CTA per share of the iterations
         } else {
             // units of work; one CTA each (two for SM pairs), or one CTA (pair)
             // per SM (pair) walking them when no operand is split in the kernel

@@ -112,6 +112,13 @@ struct Cfg {
 // dp_tiles run as whole tiles; each later tile (the last, partly filled
 // wave) runs as tail_nsplit CTAs of BN / tail_nsplit columns each, so the
 // last wave finishes in a fraction of a tile's time.
+// Stream-K (sk_ctas > 0, single-SM tiles only): the tiles x num_kb k-block
+// iterations, tile after tile, are cut into sk_ctas contiguous ranges of
+// equal length, one per CTA.  A CTA's range covers the end of one tile, any
+// number of whole tiles and the start of another; a tile it covers only in
+// part leaves its fp32 partial sum in `partial` (slot 2c for the range's
+// first tile, 2c + 1 for its last), and sk_fixup_kernel adds a tile's
+// partials in ascending k order and applies the epilogue.
 struct Params {
     float *C;
     int64_t ldc;
@@ -127,6 +134,9 @@ struct Params {
     const float *row_scale;     // fused epilogue: M row scales or null
     const float *bias;          // N column biases or null
     int act;                    // SGEMM_ACT_*
+    int sk_ctas;                // stream-K: CTAs sharing the iterations (0: off)
+    long long sk_iters;         // stream-K: tiles * num_kb
+    float *partial;             // stream-K: 2 * sk_ctas tiles of BM x BN floats
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -440,6 +450,55 @@ __device__ __forceinline__ void unit_of(const Params &p, int TM, int BN_, int u,
     n0 = tn * BN_ + sub * bn;
 }
 
+// One piece of a CTA's work: the k-blocks [kb0, kb1) of a tile (or of a
+// column slice of one).  slot < 0: the piece is the whole tile and its
+// epilogue writes C; else its partial sum goes to partial slot `slot`.
+struct Piece {
+    int m0, n0, bn, nsub, kb0, kb1, slot;
+};
+
+// Walks a CTA's pieces in order; every role of the CTA walks the same list.
+struct Walk {
+    long long i, i1;            // stream-K: iterations left
+    int u;                      // otherwise: next unit
+    int c;                      // the CTA (pair) index
+    bool first;
+};
+
+__device__ __forceinline__ void walk_begin(const Params &p, int group, Walk &w) {
+    w.u = group;
+    w.c = group;
+    w.first = true;
+    w.i = w.i1 = 0;
+    if (p.sk_ctas) {
+        w.i = (long long)group * p.sk_iters / p.sk_ctas;
+        w.i1 = (long long)(group + 1) * p.sk_iters / p.sk_ctas;
+    }
+}
+
+__device__ __forceinline__ bool walk_next(const Params &p, int TM, int BN_, int groups, Walk &w,
+                                          Piece &pc) {
+    if (p.sk_ctas) {
+        if (w.i >= w.i1) return false;
+        const int tile = (int)(w.i / p.num_kb);
+        pc.kb0 = (int)(w.i - (long long)tile * p.num_kb);
+        const long long left = w.i1 - w.i;
+        pc.kb1 = left < (long long)(p.num_kb - pc.kb0) ? pc.kb0 + (int)left : p.num_kb;
+        unit_of(p, TM, BN_, tile, pc.m0, pc.n0, pc.bn, pc.nsub);   // every tile whole
+        pc.slot = (pc.kb0 == 0 && pc.kb1 == p.num_kb) ? -1 : 2 * w.c + (w.first ? 0 : 1);
+        w.i += pc.kb1 - pc.kb0;
+    } else {
+        if (w.u >= p.units) return false;
+        unit_of(p, TM, BN_, w.u, pc.m0, pc.n0, pc.bn, pc.nsub);
+        pc.kb0 = 0;
+        pc.kb1 = p.num_kb;
+        pc.slot = -1;
+        w.u += groups;
+    }
+    w.first = false;
+    return true;
+}
+
 // Persistent over units: CTA (or CTA pair) c handles units c, c + count, ...
 // The k-block stream of the TMA producer and of the MMA issuer runs on across
 // units (stage and phase from a per-CTA k-block counter), and the two TMEM
@@ -537,8 +596,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int nkb = p.num_kb;
     const uint64_t lim = p.wait_ns;
+    // A CTA that splits A into TMEM has one accumulator (the A slots take
+    // the columns of the second), so its pieces take turns on it.
+    const int nbuf = p.fuse_a ? 1 : 2;
 
     // Roles are dispatched per WARP: the epilogue's tcgen05.ld is warp-collective,
     // so no lane of the producer or MMA warp may fall into it.
@@ -549,9 +610,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             // a pair: the leader's full barrier counts both CTAs' bytes
             const uint32_t lead_full0 = PAIR ? leader_addr(full_bar(0)) : 0u;
-            for (int u = group; u < p.units && ok; u += groups) {
-                int m0, n0, bn, nsub;
-                unit_of(p, TM, BN, u, m0, n0, bn, nsub);
+            Walk w;
+            walk_begin(p, group, w);
+            Piece pc;
+            while (ok && walk_next(p, TM, BN, groups, w, pc)) {
+                const int m0 = pc.m0, n0 = pc.n0, bn = pc.bn, nsub = pc.nsub;
                 const CUtensorMap *mb_hi = nsub == 1 ? &tm_bhi : &tm_bhi_tail;
                 const CUtensorMap *mb_lo = nsub == 1 ? &tm_blo : &tm_blo_tail;
                 const int b_rows = PAIR ? bn / 2 : bn;            // this CTA's B rows
@@ -559,7 +622,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t a_bytes = (uint32_t)K_::A_BYTES, b_bytes = (uint32_t)(b_rows * BK * 4);
                 const uint32_t tx = (p.fuse_a ? a_bytes : K_::PARTS * a_bytes) +
                                     (p.fuse_b ? b_bytes : K_::PARTS * b_bytes);
-                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                for (int kb = pc.kb0; kb < pc.kb1; ++kb, ++g) {
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, lim)) { ok = false; break; }
@@ -598,14 +661,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0 && leader) {
             // ------------------------------------------ MMA issuer
             int64_t g = 0;
-            int j = 0;                                 // units done by this CTA
+            int j = 0;                                 // pieces done by this CTA
             bool ok = true;
-            for (int u = group; u < p.units && ok; u += groups, ++j) {
-                int m0, n0, bn, nsub;
-                unit_of(p, TM, BN, u, m0, n0, bn, nsub);
-                const int b = j & 1;
-                // the epilogue must have emptied this accumulator (unit j - 2)
-                const uint32_t eph = ((uint32_t)(j >> 1) & 1u) ^ 1u;
+            Walk w;
+            walk_begin(p, group, w);
+            Piece pc;
+            for (; ok && walk_next(p, TM, BN, groups, w, pc); ++j) {
+                const int bn = pc.bn, kb0 = pc.kb0;
+                const int b = j % nbuf;
+                // the epilogue must have emptied this accumulator (piece j - nbuf)
+                const uint32_t eph = ((uint32_t)(j / nbuf) & 1u) ^ 1u;
                 if (!(PAIR ? mbar_wait_cluster(acce_bar(b), eph, lim) : mbar_wait(acce_bar(b), eph, lim)))
                     break;
                 tc_fence_after();
@@ -613,7 +678,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 constexpr int NA = K_::NACC;
                 const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
                                        ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
-                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                for (int kb = kb0; kb < pc.kb1; ++kb, ++g) {
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     const uint32_t ready = fused ? conv_bar(s) : full_bar(s);
@@ -629,7 +694,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int kk = 0; kk < BK / 8; ++kk) {
                             const uint32_t off = kk * 32;
                             const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
-                            const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                            const uint32_t first = (kb == kb0 && kk == 0) ? 0u : 1u;
                             const uint32_t ah = at + (uint32_t)(kk * 8);
                             if (BCAT && !p.fuse_b) {
                                 // [B_hi | B_lo] starts at b_hi(s): hi*hi to BN.., hi*lo to 2 BN..
@@ -644,7 +709,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 umma_tf32_ta(d + (NA == 3 ? BN : 0), ah, bh, idesc, f2);
                             } else {
                                 const int ka = NA == 2 ? (kk & 1) : 0;
-                                const uint32_t fa = (kb == 0 && kk < NA) ? 0u : 1u;
+                                const uint32_t fa = (kb == kb0 && kk < NA) ? 0u : 1u;
                                 umma_tf32_ta(d + (uint32_t)(ka * BN), ah, bh, idesc, fa);
                             }
                         }
@@ -656,7 +721,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint32_t off = kk * 32;            // 8 tf32 = 32 bytes
                         const uint64_t ah = smem_desc<BK * 4>(a_hi(s) + off);
                         const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
-                        const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                        const uint32_t first = (kb == kb0 && kk == 0) ? 0u : 1u;
                         if (THREE) {
                             const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
                             const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
@@ -675,7 +740,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 umma_tf32_pair(d, ah, bh, idesc, first);
                             } else {
                                 const int ka = NA == 2 ? (kk & 1) : 0;
-                                const uint32_t fa = (kb == 0 && kk < NA) ? 0u : 1u;
+                                const uint32_t fa = (kb == kb0 && kk < NA) ? 0u : 1u;
                                 umma_tf32(d + (uint32_t)(ka * BN), ah, bh, idesc, fa);
                             }
                         }
@@ -689,8 +754,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // all MMAs of this CTA retired before TMEM can be freed
             if (j > 0) {
-                const int b = (j - 1) & 1;
-                mbar_wait(accf_bar(b), (uint32_t)((j - 1) >> 1) & 1u, kDrainNs);
+                const int b = (j - 1) % nbuf;
+                mbar_wait(accf_bar(b), (uint32_t)((j - 1) / nbuf) & 1u, kDrainNs);
             }
         }
         __syncwarp();
@@ -708,14 +773,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int ct = threadIdx.x - 64;
         int64_t g = 0;
         int j = 0;
-        for (int u = group; u < p.units; u += groups, ++j) {
-            int m0, n0, bn, nsub;
-            unit_of(p, TM, BN, u, m0, n0, bn, nsub);
+        Walk w;
+        walk_begin(p, group, w);
+        Piece pc;
+        for (; walk_next(p, TM, BN, groups, w, pc); ++j) {
+            const int m0 = pc.m0, n0 = pc.n0, bn = pc.bn;
             const int b_rows = PAIR ? bn / 2 : bn;
             if (fused) {
                 // during the main loop these warps split the raw operand tiles
                 bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                for (int kb = pc.kb0; kb < pc.kb1; ++kb, ++g) {
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(full_bar(s), ph, lim)) { ok = false; break; }
@@ -738,8 +805,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (!ok) break;
             }
-            const int b = j & 1;
-            const bool ready = mbar_wait(accf_bar(b), (uint32_t)(j >> 1) & 1u, lim);
+            const int b = j % nbuf;
+            const bool ready = mbar_wait(accf_bar(b), (uint32_t)(j / nbuf) & 1u, lim);
             tc_fence_after();
             if (!ready) break;
             const float alpha = p.alpha, beta = p.beta;
@@ -773,7 +840,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();
                 const int col = n0 + c * 32 + lane;
-                if (col < p.N && (p.row_scale || p.bias || p.act != SGEMM_ACT_NONE)) {
+                if (pc.slot >= 0) {
+                    // a share of a tile's k range: the raw sum, tile-local
+                    float *__restrict__ dst = p.partial + (int64_t)pc.slot * (BM * BN) +
+                                              (q * 32) * BN + c * 32 + lane;
+#pragma unroll 8
+                    for (int rr = 0; rr < 32; ++rr) dst[rr * BN] = stg[rr * EPI_LD + lane];
+                } else if (col < p.N && (p.row_scale || p.bias || p.act != SGEMM_ACT_NONE)) {
                     // fused epilogue: alpha * s_row, + bias_col, activation
                     float *__restrict__ dst = p.C + (int64_t)row0 * p.ldc + col;
 #pragma unroll 4
@@ -827,6 +900,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         else
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                          :: "r"(tmem), "r"(K_::TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- stream-K fixup
+// CTA (t, y) finishes tile t: when the tile's k-blocks were shared by
+// several CTAs, it adds their partial sums in ascending k order (the CTAs'
+// order) and applies the epilogue exactly as the main kernel does; a tile
+// computed whole by one CTA was written by that CTA and is skipped.
+// Iteration x belongs to CTA ((x + 1) * G - 1) / T, the last c with
+// floor(c * T / G) <= x.
+template <int BN>
+__global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
+    const long long T = p.sk_iters, G = p.sk_ctas;
+    const int t = (int)blockIdx.x;
+    const long long first = (long long)t * p.num_kb, last = first + p.num_kb - 1;
+    const int c_lo = (int)(((first + 1) * G - 1) / T);
+    const int c_hi = (int)(((last + 1) * G - 1) / T);
+    if (c_lo == c_hi) return;
+    int m0, n0, bn, nsub;
+    unit_of(p, BM, BN, t, m0, n0, bn, nsub);
+    constexpr int ELEMS = BM * BN;
+    for (int e = (int)(blockIdx.y * blockDim.x + threadIdx.x); e < ELEMS;
+         e += (int)(gridDim.y * blockDim.x)) {
+        const int r = e / BN, cc = e - r * BN;
+        const int row = m0 + r, col = n0 + cc;
+        if (row >= p.M || col >= p.N) continue;
+        float v = 0.0f;
+        for (int c = c_lo; c <= c_hi; ++c) {
+            // the tile is CTA c's first piece when c's range starts inside it
+            const long long i0 = (long long)c * T / G;
+            const int slot = 2 * c + (i0 >= first ? 0 : 1);
+            const float x = p.partial[(int64_t)slot * ELEMS + e];
+            v = c == c_lo ? x : __fadd_rn(v, x);
+        }
+        float *dst = p.C + (int64_t)row * p.ldc + col;
+        const float a_r = epi_alpha(p.alpha, p.row_scale, row);
+        const float tt = p.beta == 0.0f ? __fmul_rn(a_r, v)
+                                        : __fmaf_rn(a_r, v, __fmul_rn(p.beta, *dst));
+        *dst = epi_tail(tt, p.bias, col, p.act);
     }
 }
 
@@ -1075,23 +1187,31 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // the canonical K-contiguous workspace layout.
     const bool fuse_a = pl.fuse_a && is_notrans(ta) && aligned16(A) && lda % 4 == 0;
     const bool fuse_b = pl.fuse_b && !is_notrans(tb) && aligned16(B) && ldb % 4 == 0;
-    // the pair kernel takes pre-split operands only
-    const bool pair = pl.pair != 0 && !fuse_a && !fuse_b;
+    // the pair kernel takes pre-split operands only, and no stream-K
+    const bool sk = pl.tc_sk > 0;
+    const bool pair = pl.pair != 0 && !fuse_a && !fuse_b && !sk;
     const int TM = pair ? 2 * tc::BM : tc::BM;          // tile rows
     const int bdiv = pair ? 2 : 1;                      // B rows per CTA = tile columns / bdiv
     auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
     const size_t a_elems = fuse_a ? 0 : up((size_t)M * Kp * 4) / 4;
     const size_t b_elems = fuse_b ? 0 : up((size_t)N * Kp * 4) / 4;
     const int parts = three ? 2 : 1;
-    float *a_hi = nullptr, *b_hi = nullptr, *a_lo = nullptr, *b_lo = nullptr;
-    if (a_elems + b_elems > 0) {
+    // stream-K: the iterations of all tiles (at full width) and their sharing
+    const int64_t tiles_all = ((M + TM - 1) / TM) * ((N + BN - 1) / BN);
+    const int nkb_all = Kp / ((three && !(BN == 64 && fuse_a)) ? tc::KBlock<true>::BK : 32);
+    const int64_t sk_iters = sk ? tiles_all * nkb_all : 0;
+    const int sk_ctas = sk ? (int)std::min<int64_t>(pl.tc_sk, sk_iters) : 0;
+    const size_t part_elems = sk ? (size_t)2 * sk_ctas * tc::BM * BN : 0;
+    float *a_hi = nullptr, *b_hi = nullptr, *a_lo = nullptr, *b_lo = nullptr, *partial = nullptr;
+    if (a_elems + b_elems + part_elems > 0) {
         void *ws = nullptr;
-        int st = workspace(s, (size_t)parts * (a_elems + b_elems) * 4, &ws);
+        int st = workspace(s, ((size_t)parts * (a_elems + b_elems) + part_elems) * 4, &ws);
         if (st != SGEMM_OK) return st;
         a_hi = static_cast<float *>(ws);
         b_hi = a_hi + a_elems;
         a_lo = three ? b_hi + b_elems : a_hi;
         b_lo = three ? a_lo + a_elems : b_hi;
+        partial = a_hi + (size_t)parts * (a_elems + b_elems);
     }
 
     // canonical K-major operands: A as [M][Kp], B as [N][Kp]
@@ -1147,6 +1267,15 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.bias = epi.bias;
     p.act = epi.act;
     p.units = p.dp_tiles + (p.tiles_m * p.tiles_n - p.dp_tiles) * nsplit;
+    if (sk) {
+        if (p.num_kb != nkb_all) return SGEMM_ERR_UNSUPPORTED;   // one k-block width
+        p.dp_tiles = p.tiles_m * p.tiles_n;
+        p.tail_nsplit = 1;
+        p.units = p.dp_tiles;
+        p.sk_ctas = sk_ctas;
+        p.sk_iters = sk_iters;
+        p.partial = partial;
+    }
     {
         std::lock_guard<std::mutex> lk(g_tc_mu);
         p.wait_ns = g_wait_ns;
@@ -1155,18 +1284,29 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // under the main loop of the next) unless an operand is split in the
     // kernel: the split warps are also the epilogue warps, so those CTAs take
     // one unit each.
+    // Stream-K: one CTA per share of the iterations.
     const int slots = pair ? std::max(sms / 2, 1) : std::max(sms, 1);
-    const int groups = (fuse_a || fuse_b) ? p.units : std::min(p.units, slots);
+    const int groups = sk ? sk_ctas : (fuse_a || fuse_b) ? p.units : std::min(p.units, slots);
     const int grid = groups * (pair ? 2 : 1);
+    int st2;
     if (BN == 256)
-        return three ? launch_main_any<256, true>(pair, maps, p, grid, s)
-                     : launch_main_any<256, false>(pair, maps, p, grid, s);
-    if (BN == 128)
-        return three ? launch_main_any<128, true>(pair, maps, p, grid, s)
-                     : launch_main_any<128, false>(pair, maps, p, grid, s);
-    if (wide) return launch_main<64, true, false, true>(maps, p, grid, s);
-    return three ? launch_main_any<64, true>(pair, maps, p, grid, s)
-                 : launch_main_any<64, false>(pair, maps, p, grid, s);
+        st2 = three ? launch_main_any<256, true>(pair, maps, p, grid, s)
+                    : launch_main_any<256, false>(pair, maps, p, grid, s);
+    else if (BN == 128)
+        st2 = three ? launch_main_any<128, true>(pair, maps, p, grid, s)
+                    : launch_main_any<128, false>(pair, maps, p, grid, s);
+    else if (wide)
+        st2 = launch_main<64, true, false, true>(maps, p, grid, s);
+    else
+        st2 = three ? launch_main_any<64, true>(pair, maps, p, grid, s)
+                    : launch_main_any<64, false>(pair, maps, p, grid, s);
+    if (st2 != SGEMM_OK || !sk) return st2;
+    // the shared tiles' partial sums, added in k order, then the epilogue
+    const dim3 fgrid((unsigned)p.units, (unsigned)(tc::BM * BN / 1024));
+    if (BN == 256) tc::sk_fixup_kernel<256><<<fgrid, 256, 0, s>>>(p);
+    else if (BN == 128) tc::sk_fixup_kernel<128><<<fgrid, 256, 0, s>>>(p);
+    else tc::sk_fixup_kernel<64><<<fgrid, 256, 0, s>>>(p);
+    return last_status();
 }
 
 }  // namespace sgemm_gb300

@@ -111,13 +111,19 @@ int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
 
 /*
  * sgemm_ex - as sgemm, with the path forced (sgemm_path) and the split-K
- * factor forced (split >= 1, or 0 to let the selector decide).  The split
- * applies to the FFMA path: split = 1 computes every output tile whole
- * (bit-identical to the naive ascending-k FMA loop); split > 1 sums K in
- * `split` contiguous slices per tile whose partial results are added in a
- * fixed order; 0 lets the selector share all tiles x k-tiles iterations
- * equally among two CTAs per SM ("stream-K": deterministic, not
- * bit-identical to the naive loop where a tile is shared).
+ * factor forced (split >= 1, or 0 to let the selector decide).
+ * FFMA path: split = 1 computes every output tile whole (bit-identical to
+ * the naive ascending-k FMA loop); split > 1 sums K in `split` contiguous
+ * slices per tile whose partial results are added in a fixed order; 0 lets
+ * the selector share all tiles x k-tiles iterations equally among two CTAs
+ * per SM ("stream-K": deterministic, not bit-identical to the naive loop
+ * where a tile is shared).
+ * Tensor-core paths: split = 1 computes every 128- or 256-row tile whole;
+ * split > 1 shares all tiles x k-blocks iterations in equal contiguous
+ * ranges among min(split x tiles, 8 x SMs, iterations) CTAs, one SM each
+ * (stream-K; shared tiles' partial sums are added in k order by a second
+ * kernel); 0 lets the selector choose stream-K when fewer 128-row tiles
+ * than SMs would leave SMs idle.
  * Returns SGEMM_ERR_UNSUPPORTED when the forced path cannot run the problem.
  */
 int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
@@ -183,8 +189,9 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * anything and without touching the GPU.  `path` and `split` as in
  * sgemm_ex (0 = let the selector decide); num_sms is the GPU's SM count.
  * a_aligned/b_aligned/c_aligned say whether the base pointer is 16-byte
- * aligned.  On success writes the chosen path (sgemm_path), the FFMA CTAs
- * per output tile rounded up (1 = every tile whole), the tile rows and
+ * aligned.  On success writes the chosen path (sgemm_path), the CTAs per
+ * output tile rounded up (FFMA or tensor-core stream-K; 1 = every tile
+ * whole), the tile rows and
  * columns, whether the FFMA path uses 16-byte loads (1) or the 4-byte edge
  * path (0), and the number of CTAs of the main kernel.  Any output pointer
  * may be NULL.  Returns SGEMM_OK or a negative argument index as sgemm.

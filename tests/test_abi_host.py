@@ -154,6 +154,36 @@ def test_plan_sm_pair_tiles(lib):
     assert st == 0 and p["tile_m"] == 128
 
 
+def test_plan_tensor_core_stream_k(lib):
+    # 16384 x 64 x 8192 skinny: 128 tiles for 152 SMs, 256 k-blocks each ->
+    # the iterations are shared by one CTA per SM
+    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152)
+    assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["ctas"] == 152 and p["split"] == 2
+    st, p = sg.sgemm_plan("N", "T", 2048, 64, 8192, 8192, 8192, 64, num_sms=152)
+    assert st == 0 and p["ctas"] == 152 and p["split"] == 10
+    # deep K on a few tiles
+    st, p = sg.sgemm_plan("N", "N", 512, 512, 16384, 16384, 512, 512, num_sms=152)
+    assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["ctas"] == 152
+    # 2048^3: the partial tiles' traffic outweighs the 128/152 fill
+    st, p = sg.sgemm_plan("N", "N", 2048, 2048, 2048, 2048, 2048, 2048, num_sms=152)
+    assert st == 0 and p["ctas"] == 128 and p["split"] == 1
+    # a full wave or more: never (4096^3 stays on SM pairs)
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152)
+    assert st == 0 and p["tile_m"] == 256 and p["split"] == 1
+    # forced: split = 1 keeps tiles whole; split = s shares among s x tiles CTAs
+    st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152, split=1)
+    assert st == 0 and p["ctas"] == 128 and p["split"] == 1
+    st, p = sg.sgemm_plan("T", "N", 300, 260, 1000, 300, 260, 260, num_sms=152,
+                          path=sg.PATH_3XTF32, split=3)
+    assert st == 0 and p["tile_m"] == 128 and p["ctas"] == 18 and p["split"] == 3
+    # capped at 8 CTAs per SM and at one k-block per CTA
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152,
+                          path=sg.PATH_3XTF32, split=64)
+    assert st == 0 and p["ctas"] == 8 * 152
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 96, 96, 256, 256, path=sg.PATH_3XTF32, split=8)
+    assert st == 0 and p["ctas"] == 12
+
+
 def test_plan_ffma_stream_k_tail(lib):
     # 4096^3: 1024 tiles = 3 full waves of 304 + 112; the 112 are shared by 304 CTAs
     st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152,
