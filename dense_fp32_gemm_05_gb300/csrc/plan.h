@@ -179,7 +179,7 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // never does.
         const bool three = pl.path == SGEMM_PATH_3XTF32;
         const int64_t kp = (K + 31) / 32 * 32;
-        const int64_t nkb = kp / ((three && !(pl.tile_n == 64 && pl.fuse_a)) ? 16 : 32);
+        const int64_t nkb = kp / ((three && !(pl.tile_n <= 128 && pl.fuse_a)) ? 16 : 32);
         const int64_t tiles1 = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
         const int64_t iters = tiles1 * nkb;
         int64_t g_sk = 0;

@@ -73,8 +73,9 @@ __device__ unsigned int g_error;        // sticky device error word (per device)
 // PAIR: a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2 (M = 256): each CTA holds its 128 rows of A and
 // half (BN / 2 columns) of B, and its 128 rows of the accumulator.
-// WIDE: 3xTF32 with 32-wide k-blocks (128-byte rows): the skinny tiles whose
-// raw A streams from HBM, where 64-byte row pieces halve DRAM efficiency.
+// WIDE: 3xTF32 with 32-wide k-blocks (128-byte rows): the 64- and 128-wide
+// tiles whose raw A streams from HBM (one or two tile columns read each row
+// of A), where 64-byte row pieces halve DRAM efficiency.
 template <int BN, bool THREE, bool PAIR = false, bool WIDE = false>
 struct Cfg {
     static constexpr int BK = WIDE ? 32 : KBlock<THREE>::BK;
@@ -1198,7 +1199,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     const int parts = three ? 2 : 1;
     // stream-K: the iterations of all tiles (at full width) and their sharing
     const int64_t tiles_all = ((M + TM - 1) / TM) * ((N + BN - 1) / BN);
-    const int nkb_all = Kp / ((three && !(BN == 64 && fuse_a)) ? tc::KBlock<true>::BK : 32);
+    const int nkb_all = Kp / ((three && !(BN <= 128 && fuse_a)) ? tc::KBlock<true>::BK : 32);
     const int64_t sk_iters = sk ? tiles_all * nkb_all : 0;
     const int sk_ctas = sk ? (int)std::min<int64_t>(pl.tc_sk, sk_iters) : 0;
     const size_t part_elems = sk ? (size_t)2 * sk_ctas * tc::BM * BN : 0;
@@ -1225,10 +1226,11 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     if (st != SGEMM_OK) return st;
 
     const int nsplit = std::max(1, pl.tail_nsplit);
-    // 64-wide 3xTF32 tiles that split A into TMEM stream raw A from HBM: 32-wide
-    // k-blocks (128-byte rows) there (skinny 16384 x 64 x 8192: 2.3 -> 4.5 TB/s
-    // of A in the TF32 mode, which always has them)
-    const bool wide = three && BN == 64 && fuse_a && !pair;
+    // 64- and 128-wide 3xTF32 tiles that split A into TMEM stream raw A from
+    // HBM: 32-wide k-blocks (128-byte rows) there (16384 x 64 x 8192: 2.3 ->
+    // 4.5 TB/s of A in the TF32 mode, which always has them; 16384 x 128 x
+    // 8192 3xTF32: 142 -> 170 TFLOP/s)
+    const bool wide = three && BN <= 128 && fuse_a && !pair;
     const int bk = (wide || !three) ? 32 : tc::KBlock<true>::BK;
     CUtensorMap maps[6];
     bool ok;
@@ -1292,6 +1294,8 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     if (BN == 256)
         st2 = three ? launch_main_any<256, true>(pair, maps, p, grid, s)
                     : launch_main_any<256, false>(pair, maps, p, grid, s);
+    else if (BN == 128 && wide)
+        st2 = launch_main<128, true, false, true>(maps, p, grid, s);
     else if (BN == 128)
         st2 = three ? launch_main_any<128, true>(pair, maps, p, grid, s)
                     : launch_main_any<128, false>(pair, maps, p, grid, s);
