@@ -58,7 +58,9 @@ def dist_env():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 25 ms) of SM clock and throttle reasons; each
+    sample carries its host arrival time so that only those taken inside the
+    timed region count."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -73,7 +75,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -83,7 +85,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -96,10 +98,14 @@ class ClockSampler:
         if self._t:
             self._t.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in samples that
+        arrived within [t0, t1] (host perf_counter; all samples if None)."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -361,20 +367,25 @@ def gpu_arm(args):
     sg.sgemm_timing_enable(args.steps)
     barrier()
     t_wall = time.perf_counter()
+    t_begin = t_wall
     for i in range(args.steps):
         flush.fill_(float(i))
         starts[i].record(stream)
         call()
         ends[i].record(stream)
     barrier()
-    t_wall = time.perf_counter() - t_wall
+    t_end = time.perf_counter()
+    t_wall = t_end - t_wall
+    time.sleep(0.05)                # the last in-region sample reaches the reader
     sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sg.sgemm_timing_read(args.steps)
     sg.sgemm_timing_enable(0)
     total_ms, value = job_throughput(sum(step_ms), args.steps, w.flops, device=dev)
     ms_per_step = total_ms / args.steps
-    clocks = sampler.summary()
+    # samples that arrived while the timed steps ran (nvidia-smi prints each
+    # shortly after taking it: a 25 ms allowance at the end)
+    clocks = sampler.summary(t_begin, t_end + 0.025)
 
     # ---- plan of the timed call: which kernels ran
     st, plan = sg.sgemm_plan(w.transA, w.transB, w.M, w.N, w.K, lda, ldb, ldc, True, True, True,
@@ -569,7 +580,7 @@ def only_path(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--path-reps", type=int, default=10)
