@@ -127,11 +127,11 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         const int64_t rem = tiles - dp;
         pl.split = (sk == 0 || rem == 0) ? 1 : (int)((sk + rem - 1) / rem);
     } else {
-        // tensor-core path: 128-row tiles, N of the MMA from the problem's N,
-        // one CTA per SM.  Tiles after the last full wave may run as 2 or 4
-        // narrower CTAs (MMA N = tile_n / slices, at least 64) so the last
-        // wave is short; a narrower tile is charged ~5 % per halving for its
-        // higher shared-memory traffic per flop.
+        // tensor-core path: 128-row tiles (256 on SM pairs), N of the MMA from
+        // the problem's N, one CTA (pair) per SM.  Tiles after the last full
+        // wave may run as 2 or 4 narrower units, or all tiles x k-blocks
+        // iterations may be shared by the CTAs (stream-K), when a model of
+        // their cost says so (below).
         pl.tile_m = 128;
         pl.tile_n = N > 128 ? 256 : (N > 64 ? 128 : 64);
         pl.split = 1;
@@ -156,11 +156,24 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         double best = (double)((tiles + slots - 1) / slots);
         pl.dp_tiles = (int)tiles;
         pl.tail_nsplit = 1;
+        const bool three = pl.path == SGEMM_PATH_3XTF32;
+        // Time of a unit 1/ns as wide as a tile, in tile-times, measured on
+        // GB300: narrow units are bound by the stage ring's round trip and the
+        // per-stage TMA issue (SM pairs, shared-memory operands), or by MMAs
+        // reading A from TMEM at a cost nearly independent of N (A split in
+        // the kernel), not by their share of the flops.  (4095 x 3073 x 1537
+        // ran 1.43x faster with whole tiles than with quarter units.)
+        const bool tmem_a = !pl.pair && pl.fuse_a;
+        auto unit_cost = [&](int ns) {
+            if (!tmem_a) return ns == 2 ? 0.90 : 0.76;
+            if (three) return ns == 2 ? 0.97 : 0.96;
+            return ns == 2 ? 0.90 : 0.87;
+        };
         for (int ns = 2; ns <= 4 && pl.tile_n / ns >= 64; ns *= 2) {
             if (tail == 0) break;
             const double waves = (double)((tail * ns + slots - 1) / slots);
-            const double c = (double)(full / slots) + waves / ns * (ns == 2 ? 1.05 : 1.10);
-            if (c < best * 0.97) {
+            const double c = (double)(full / slots) + waves * unit_cost(ns);
+            if (c < best * 0.995) {
                 best = c;
                 pl.dp_tiles = (int)full;
                 pl.tail_nsplit = ns;
@@ -172,12 +185,12 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // end together; tiles that several CTAs share leave partial sums for
         // a fixup pass.  Modelled in microseconds: a tile's main loop at the
         // measured MMA rate (2047 MAC per clock per SM at ~1.9 GHz; 0.75 of
-        // it reached on 128- and 256-wide tiles, 0.45 on 64-wide ones), the
-        // fixup as 4 us plus its partial-tile traffic at 6 TB/s; taken when
-        // 3 % faster than the choice above.  A forced split s > 1 runs
+        // it reached on 128- and 256-wide tiles, 0.45 on 64-wide ones), two
+        // partial-tile epilogues per CTA (4.5 us for 128 x 256), and the
+        // fixup as 3 us plus its partial-tile traffic at 6 TB/s; taken when
+        // 5 % faster than the choice above.  A forced split s > 1 runs
         // stream-K with min(s x tiles, 8 x SMs, iterations) CTAs; split = 1
         // never does.
-        const bool three = pl.path == SGEMM_PATH_3XTF32;
         const int64_t kp = (K + 31) / 32 * 32;
         const int64_t nkb = kp / ((three && !(pl.tile_n <= 128 && pl.fuse_a)) ? 16 : 32);
         const int64_t tiles1 = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
@@ -190,9 +203,10 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
             if (g > tiles1) {
                 const double rate = 2047.0 * 1900.0 * (pl.tile_n >= 128 ? 0.75 : 0.45);
                 const double tile_us = 128.0 * pl.tile_n * (double)kp * (three ? 3 : 1) / rate;
-                const double fix = 4.0 + (double)(g + tiles1) * 128.0 * pl.tile_n * 8.0 / 6.0e6;
-                const double t_sk = (double)iters / (double)g / (double)nkb * tile_us + fix;
-                if (t_sk < 0.97 * best * tile_us) g_sk = g;
+                const double epi = 2.0 * 4.5 * pl.tile_n / 256.0;
+                const double fix = 3.0 + (double)(g + tiles1) * 128.0 * pl.tile_n * 8.0 / 6.0e6;
+                const double t_sk = (double)iters / (double)g / (double)nkb * tile_us + epi + fix;
+                if (t_sk < 0.95 * best * tile_us) g_sk = g;
             }
         }
         if (g_sk > 0) {

@@ -280,7 +280,10 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
                    c_aligned != 0, path, split, num_sms, &pl);
     if (st != SGEMM_OK) return st;
     if (out_path) *out_path = pl.path;
-    if (out_split) *out_split = pl.split;
+    // tensor cores: the CTAs (pairs) sharing one tile -- stream-K's split, or
+    // the column slices of the last-wave tiles
+    if (out_split) *out_split = (pl.path == SGEMM_PATH_3XTF32 || pl.path == SGEMM_PATH_TF32) && pl.tc_sk == 0
+                                    ? pl.tail_nsplit : pl.split;
     if (out_tile_m) *out_tile_m = pl.tile_m;
     if (out_tile_n) *out_tile_n = pl.tile_n;
     if (out_vector) *out_vector = pl.vector;

@@ -922,24 +922,35 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
     int m0, n0, bn, nsub;
     unit_of(p, BM, BN, t, m0, n0, bn, nsub);
     constexpr int ELEMS = BM * BN;
-    for (int e = (int)(blockIdx.y * blockDim.x + threadIdx.x); e < ELEMS;
-         e += (int)(gridDim.y * blockDim.x)) {
+    // Only the first CTA can start before the tile (its piece is its range's
+    // last, slot 2c + 1, unless its range starts exactly at the tile); every
+    // later CTA's range starts inside the tile: slot 2c.
+    const int lo_slot = 2 * c_lo + ((long long)c_lo * T / G >= first ? 0 : 1);
+    const float4 *part = reinterpret_cast<const float4 *>(p.partial);
+    for (int e4 = (int)(blockIdx.y * blockDim.x + threadIdx.x); e4 < ELEMS / 4;
+         e4 += (int)(gridDim.y * blockDim.x)) {
+        const int e = 4 * e4;
         const int r = e / BN, cc = e - r * BN;
         const int row = m0 + r, col = n0 + cc;
         if (row >= p.M || col >= p.N) continue;
-        float v = 0.0f;
-        for (int c = c_lo; c <= c_hi; ++c) {
-            // the tile is CTA c's first piece when c's range starts inside it
-            const long long i0 = (long long)c * T / G;
-            const int slot = 2 * c + (i0 >= first ? 0 : 1);
-            const float x = p.partial[(int64_t)slot * ELEMS + e];
-            v = c == c_lo ? x : __fadd_rn(v, x);
+        float4 v = part[(int64_t)lo_slot * (ELEMS / 4) + e4];
+        for (int c = c_lo + 1; c <= c_hi; ++c) {
+            const float4 x = part[(int64_t)(2 * c) * (ELEMS / 4) + e4];
+            v.x = __fadd_rn(v.x, x.x);
+            v.y = __fadd_rn(v.y, x.y);
+            v.z = __fadd_rn(v.z, x.z);
+            v.w = __fadd_rn(v.w, x.w);
         }
+        const float vs[4] = {v.x, v.y, v.z, v.w};
         float *dst = p.C + (int64_t)row * p.ldc + col;
         const float a_r = epi_alpha(p.alpha, p.row_scale, row);
-        const float tt = p.beta == 0.0f ? __fmul_rn(a_r, v)
-                                        : __fmaf_rn(a_r, v, __fmul_rn(p.beta, *dst));
-        *dst = epi_tail(tt, p.bias, col, p.act);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (col + q >= p.N) break;
+            const float tt = p.beta == 0.0f ? __fmul_rn(a_r, vs[q])
+                                            : __fmaf_rn(a_r, vs[q], __fmul_rn(p.beta, dst[q]));
+            dst[q] = epi_tail(tt, p.bias, col + q, p.act);
+        }
     }
 }
 
@@ -1306,7 +1317,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
                     : launch_main_any<64, false>(pair, maps, p, grid, s);
     if (st2 != SGEMM_OK || !sk) return st2;
     // the shared tiles' partial sums, added in k order, then the epilogue
-    const dim3 fgrid((unsigned)p.units, (unsigned)(tc::BM * BN / 1024));
+    const dim3 fgrid((unsigned)p.units, (unsigned)(tc::BM * BN / 4096));
     if (BN == 256) tc::sk_fixup_kernel<256><<<fgrid, 256, 0, s>>>(p);
     else if (BN == 128) tc::sk_fixup_kernel<128><<<fgrid, 256, 0, s>>>(p);
     else tc::sk_fixup_kernel<64><<<fgrid, 256, 0, s>>>(p);

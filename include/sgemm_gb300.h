@@ -190,8 +190,9 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * sgemm_ex (0 = let the selector decide); num_sms is the GPU's SM count.
  * a_aligned/b_aligned/c_aligned say whether the base pointer is 16-byte
  * aligned.  On success writes the chosen path (sgemm_path), the CTAs per
- * output tile rounded up (FFMA or tensor-core stream-K; 1 = every tile
- * whole), the tile rows and
+ * output tile rounded up (FFMA or tensor-core stream-K, or the column slices
+ * of the tensor cores' last-wave tiles; 1 = every tile whole), the tile rows
+ * and
  * columns, whether the FFMA path uses 16-byte loads (1) or the 4-byte edge
  * path (0), and the number of CTAs of the main kernel.  Any output pointer
  * may be NULL.  Returns SGEMM_OK or a negative argument index as sgemm.

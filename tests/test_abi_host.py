@@ -142,7 +142,7 @@ def test_plan_sm_pair_tiles(lib):
     # both operands through the split pre-pass and M > 128: 256-row tiles on SM pairs
     st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096)
     assert st == 0 and p["tile_m"] == 256 and p["ctas"] % 2 == 0
-    st, p = sg.sgemm_plan("T", "N", 300, 260, 1000, 300, 260, 260, path=sg.PATH_3XTF32)
+    st, p = sg.sgemm_plan("T", "N", 4096, 3000, 1000, 4096, 3000, 3000, path=sg.PATH_3XTF32)
     assert st == 0 and p["tile_m"] == 256
     # an operand split in shared memory (K-contiguous, small other side): single SMs
     st, p = sg.sgemm_plan("N", "N", 2048, 2048, 2048, 2048, 2048, 2048)
@@ -167,9 +167,10 @@ def test_plan_tensor_core_stream_k(lib):
     # 2048^3: the partial tiles' traffic outweighs the 128/152 fill
     st, p = sg.sgemm_plan("N", "N", 2048, 2048, 2048, 2048, 2048, 2048, num_sms=152)
     assert st == 0 and p["ctas"] == 128 and p["split"] == 1
-    # a full wave or more: never (4096^3 stays on SM pairs)
+    # a full wave or more: never (4096^3 stays on SM pairs, its last wave in
+    # half-width slices)
     st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152)
-    assert st == 0 and p["tile_m"] == 256 and p["split"] == 1
+    assert st == 0 and p["tile_m"] == 256 and p["split"] == 2 and p["ctas"] == 152
     # forced: split = 1 keeps tiles whole; split = s shares among s x tiles CTAs
     st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152, split=1)
     assert st == 0 and p["ctas"] == 128 and p["split"] == 1
@@ -182,6 +183,20 @@ def test_plan_tensor_core_stream_k(lib):
     assert st == 0 and p["ctas"] == 8 * 152
     st, p = sg.sgemm_plan("N", "N", 256, 256, 96, 96, 256, 256, path=sg.PATH_3XTF32, split=8)
     assert st == 0 and p["ctas"] == 12
+
+
+def test_plan_tensor_core_last_wave_slices(lib):
+    # 4096^3 on SM pairs: 256 tiles = 3 waves of 76 + 28; the 28 run as 56
+    # half-width units (a half unit measured ~0.9 of a tile, so it pays here)
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152)
+    assert st == 0 and p["tile_m"] == 256 and p["split"] == 2
+    # 4095 x 3073 x 1537: 208 tiles = 2 waves + 56; narrow units would cost
+    # more rounds than one more wave of whole tiles (1.43x measured)
+    st, p = sg.sgemm_plan("N", "N", 4095, 3073, 1537, 1537, 3073, 3073, num_sms=152)
+    assert st == 0 and p["tile_m"] == 256 and p["split"] == 1
+    # single SMs with A split into TMEM: 160 tiles = 152 + 8 -> the 8 as narrower units
+    st, p = sg.sgemm_plan("N", "N", 2560, 2048, 256, 256, 2048, 2048, num_sms=152)
+    assert st == 0 and p["tile_m"] == 128 and p["split"] in (2, 4)
 
 
 def test_plan_ffma_stream_k_tail(lib):

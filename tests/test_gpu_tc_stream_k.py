@@ -133,3 +133,31 @@ def test_stream_k_one_k_block_per_cta(oracle_mod):
     assert st == 0
     ref, bound = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
     assert oracle_mod.compare(out, ref, bound, K, 1.0)["pass"]
+
+
+@pytest.mark.parametrize("shape,pair", [((4096, 4096, 256), True), ((2560, 2048, 256), False)],
+                         ids=["pair_half_units", "single_sm_tmem_a_units"])
+def test_last_wave_slices_sampled(oracle_mod, shape, pair):
+    """The tiles after the last full wave run as narrower column slices
+    (checked through the plan), every other tile whole; seeded samples over
+    the whole result, the last rows and columns included, against the oracle."""
+    import torch
+    M, N, K = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = sg.sgemm_plan("N", "N", M, N, K, K, N, N, num_sms=sms)
+    assert st == 0 and p["split"] > 1 and (p["tile_m"] == 256) == pair
+    A = gi.random_matrix(101, M, K)
+    B = gi.random_matrix(102, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.full((M, N), float("nan"), device="cuda")
+    st = sg.sgemm("N", "N", M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0, dC.data_ptr(), N,
+                  torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert st == 0
+    out = dC.cpu().numpy()
+    assert np.all(np.isfinite(out))
+    rows, cols = gi.sample_points(M, N, 12000, seed=103)
+    ref, bound = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N,
+                                     points=(rows, cols))
+    rep = oracle_mod.compare(out[rows, cols], ref, bound, K, 1.0)
+    assert rep["pass"], rep
