@@ -54,6 +54,7 @@ struct Plan {
     int fuse_b = 1;       // tensor cores: same for B
     int pair = 0;         // tensor cores: 256-row tiles on a pair of SMs (cta_group::2)
     int tc_sk = 0;        // tensor cores: stream-K CTAs sharing all k-block iterations (0: off)
+    int tc_sk_tail = 0;   // tensor cores: the tiles after the last full wave shared by all CTAs
 };
 
 // Chooses path, tile, split and vectorisation.  `path`/`split` 0 = auto.
@@ -179,6 +180,28 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
                 pl.tail_nsplit = ns;
             }
         }
+        const int64_t kp = (K + 31) / 32 * 32;
+        const double tile_us = 128.0 * pl.tile_n * (double)kp * (three ? 3 : 1) /
+                               (2047.0 * 1900.0 * (pl.tile_n >= 128 ? 0.75 : 0.45));
+        double cur_us = best * tile_us;
+        // Stream-K over the last wave (persistent CTAs: both operands come
+        // pre-split): the whole waves first, then the k-blocks of the
+        // remaining tiles shared equally by all CTAs (pairs), instead of
+        // narrower units.  Charged one partial epilogue per CTA (4.5 us for
+        // 128 x 256 rows per SM) and the fixup (3 us plus the partial tiles'
+        // traffic at 6 TB/s); taken when 2 % faster.
+        if (split == 0 && tail > 0 && !pl.fuse_a && !pl.fuse_b) {
+            const double t_sk = (double)(full / slots) * tile_us + (double)tail / slots * tile_us +
+                                4.5 * (pl.tile_m / 128) * pl.tile_n / 256.0 + 3.0 +
+                                (double)(slots + tail) * pl.tile_m * pl.tile_n * 8.0 / 6.0e6;
+            if (t_sk < 0.98 * cur_us) {
+                cur_us = t_sk;
+                pl.dp_tiles = (int)full;
+                pl.tail_nsplit = 1;
+                pl.tc_sk_tail = 1;
+                pl.split = (int)((slots + tail - 1) / tail);
+            }
+        }
         // Stream-K on single SMs: with fewer 128-row tiles than SMs, the
         // tiles x k-blocks iterations are shared in equal contiguous ranges
         // by up to one CTA per SM (at least 8 k-blocks each), so all CTAs
@@ -191,7 +214,6 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // 5 % faster than the choice above.  A forced split s > 1 runs
         // stream-K with min(s x tiles, 8 x SMs, iterations) CTAs; split = 1
         // never does.
-        const int64_t kp = (K + 31) / 32 * 32;
         const int64_t nkb = kp / ((three && !(pl.tile_n <= 128 && pl.fuse_a)) ? 16 : 32);
         const int64_t tiles1 = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
         const int64_t iters = tiles1 * nkb;
@@ -201,12 +223,10 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         } else if (split == 0 && tiles1 < sms) {
             const int64_t g = std::min<int64_t>(sms, iters / 8);
             if (g > tiles1) {
-                const double rate = 2047.0 * 1900.0 * (pl.tile_n >= 128 ? 0.75 : 0.45);
-                const double tile_us = 128.0 * pl.tile_n * (double)kp * (three ? 3 : 1) / rate;
                 const double epi = 2.0 * 4.5 * pl.tile_n / 256.0;
                 const double fix = 3.0 + (double)(g + tiles1) * 128.0 * pl.tile_n * 8.0 / 6.0e6;
                 const double t_sk = (double)iters / (double)g / (double)nkb * tile_us + epi + fix;
-                if (t_sk < 0.95 * best * tile_us) g_sk = g;
+                if (t_sk < 0.95 * cur_us) g_sk = g;
             }
         }
         if (g_sk > 0) {
@@ -214,6 +234,7 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
             pl.tile_m = 128;
             pl.dp_tiles = (int)tiles1;
             pl.tail_nsplit = 1;
+            pl.tc_sk_tail = 0;
             pl.tc_sk = (int)g_sk;
             pl.split = (int)((g_sk + tiles1 - 1) / tiles1);
         }

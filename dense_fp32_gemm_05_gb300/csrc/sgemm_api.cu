@@ -282,7 +282,8 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
     if (out_path) *out_path = pl.path;
     // tensor cores: the CTAs (pairs) sharing one tile -- stream-K's split, or
     // the column slices of the last-wave tiles
-    if (out_split) *out_split = (pl.path == SGEMM_PATH_3XTF32 || pl.path == SGEMM_PATH_TF32) && pl.tc_sk == 0
+    if (out_split) *out_split = (pl.path == SGEMM_PATH_3XTF32 || pl.path == SGEMM_PATH_TF32) &&
+                                        pl.tc_sk == 0 && pl.tc_sk_tail == 0
                                     ? pl.tail_nsplit : pl.split;
     if (out_tile_m) *out_tile_m = pl.tile_m;
     if (out_tile_n) *out_tile_n = pl.tile_n;
@@ -302,7 +303,7 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
             const bool fa = pl.fuse_a && is_notrans(transA) && a_aligned && lda % 4 == 0;
             const bool fb = pl.fuse_b && !is_notrans(transB) && b_aligned && ldb % 4 == 0;
             const int64_t slots = pl.pair ? std::max(num_sms / 2, 1) : num_sms;
-            const int64_t groups = (fa || fb) ? units : std::min<int64_t>(units, slots);
+            const int64_t groups = pl.tc_sk_tail ? slots : (fa || fb) ? units : std::min<int64_t>(units, slots);
             *out_ctas = (int)(groups * (pl.pair ? 2 : 1));
         }
     }

@@ -113,13 +113,16 @@ struct Cfg {
 // dp_tiles run as whole tiles; each later tile (the last, partly filled
 // wave) runs as tail_nsplit CTAs of BN / tail_nsplit columns each, so the
 // last wave finishes in a fraction of a tile's time.
-// Stream-K (sk_ctas > 0, single-SM tiles only): the tiles x num_kb k-block
-// iterations, tile after tile, are cut into sk_ctas contiguous ranges of
-// equal length, one per CTA.  A CTA's range covers the end of one tile, any
-// number of whole tiles and the start of another; a tile it covers only in
-// part leaves its fp32 partial sum in `partial` (slot 2c for the range's
-// first tile, 2c + 1 for its last), and sk_fixup_kernel adds a tile's
-// partials in ascending k order and applies the epilogue.
+// Stream-K (sk_ctas > 0): the k-block iterations of tiles sk_tile0.. (tile
+// after tile, num_kb each) are cut into sk_ctas contiguous ranges of equal
+// length, one per CTA (pair).  A range covers the end of one tile, any number
+// of whole tiles and the start of another; a tile it covers only in part
+// leaves its fp32 partial sum in `partial` (slot 2c for the range's first
+// tile, 2c + 1 for its last), and sk_fixup_kernel adds a tile's partials in
+// ascending k order and applies the epilogue.  Either every tile is shared
+// this way (sk_tile0 = 0, single SMs), or the CTAs first compute the first
+// dp_units tiles whole, one wave after another, and share only the rest: the
+// last, partly filled wave.
 struct Params {
     float *C;
     int64_t ldc;
@@ -135,9 +138,11 @@ struct Params {
     const float *row_scale;     // fused epilogue: M row scales or null
     const float *bias;          // N column biases or null
     int act;                    // SGEMM_ACT_*
-    int sk_ctas;                // stream-K: CTAs sharing the iterations (0: off)
-    long long sk_iters;         // stream-K: tiles * num_kb
-    float *partial;             // stream-K: 2 * sk_ctas tiles of BM x BN floats
+    int dp_units;               // units computed whole before any stream-K range
+    int sk_ctas;                // stream-K: CTAs (pairs) sharing the iterations (0: off)
+    int sk_tile0;               // stream-K: first shared tile
+    long long sk_iters;         // stream-K: shared tiles * num_kb
+    float *partial;             // stream-K: 2 * sk_ctas tiles of TM x BN floats
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -479,23 +484,23 @@ __device__ __forceinline__ void walk_begin(const Params &p, int group, Walk &w) 
 
 __device__ __forceinline__ bool walk_next(const Params &p, int TM, int BN_, int groups, Walk &w,
                                           Piece &pc) {
-    if (p.sk_ctas) {
-        if (w.i >= w.i1) return false;
-        const int tile = (int)(w.i / p.num_kb);
-        pc.kb0 = (int)(w.i - (long long)tile * p.num_kb);
-        const long long left = w.i1 - w.i;
-        pc.kb1 = left < (long long)(p.num_kb - pc.kb0) ? pc.kb0 + (int)left : p.num_kb;
-        unit_of(p, TM, BN_, tile, pc.m0, pc.n0, pc.bn, pc.nsub);   // every tile whole
-        pc.slot = (pc.kb0 == 0 && pc.kb1 == p.num_kb) ? -1 : 2 * w.c + (w.first ? 0 : 1);
-        w.i += pc.kb1 - pc.kb0;
-    } else {
-        if (w.u >= p.units) return false;
+    if (w.u < p.dp_units) {
+        // whole units, one wave after another
         unit_of(p, TM, BN_, w.u, pc.m0, pc.n0, pc.bn, pc.nsub);
         pc.kb0 = 0;
         pc.kb1 = p.num_kb;
         pc.slot = -1;
         w.u += groups;
+        return true;
     }
+    if (!p.sk_ctas || w.i >= w.i1) return false;
+    const int t = (int)(w.i / p.num_kb);
+    pc.kb0 = (int)(w.i - (long long)t * p.num_kb);
+    const long long left = w.i1 - w.i;
+    pc.kb1 = left < (long long)(p.num_kb - pc.kb0) ? pc.kb0 + (int)left : p.num_kb;
+    unit_of(p, TM, BN_, p.sk_tile0 + t, pc.m0, pc.n0, pc.bn, pc.nsub);   // whole tiles
+    pc.slot = (pc.kb0 == 0 && pc.kb1 == p.num_kb) ? -1 : 2 * w.c + (w.first ? 0 : 1);
+    w.i += pc.kb1 - pc.kb0;
     w.first = false;
     return true;
 }
@@ -843,8 +848,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int col = n0 + c * 32 + lane;
                 if (pc.slot >= 0) {
                     // a share of a tile's k range: the raw sum, tile-local
-                    float *__restrict__ dst = p.partial + (int64_t)pc.slot * (BM * BN) +
-                                              (q * 32) * BN + c * 32 + lane;
+                    // (a pair's CTAs each write their 128 rows)
+                    float *__restrict__ dst = p.partial + (int64_t)pc.slot * (TM * BN) +
+                                              ((int)rank * BM + q * 32) * BN + c * 32 + lane;
 #pragma unroll 8
                     for (int rr = 0; rr < 32; ++rr) dst[rr * BN] = stg[rr * EPI_LD + lane];
                 } else if (col < p.N && (p.row_scale || p.bias || p.act != SGEMM_ACT_NONE)) {
@@ -911,17 +917,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 // computed whole by one CTA was written by that CTA and is skipped.
 // Iteration x belongs to CTA ((x + 1) * G - 1) / T, the last c with
 // floor(c * T / G) <= x.
-template <int BN>
+template <int BN, int TM>
 __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
     const long long T = p.sk_iters, G = p.sk_ctas;
-    const int t = (int)blockIdx.x;
-    const long long first = (long long)t * p.num_kb, last = first + p.num_kb - 1;
+    const int t = p.sk_tile0 + (int)blockIdx.x;
+    const long long first = (long long)blockIdx.x * p.num_kb, last = first + p.num_kb - 1;
     const int c_lo = (int)(((first + 1) * G - 1) / T);
     const int c_hi = (int)(((last + 1) * G - 1) / T);
     if (c_lo == c_hi) return;
     int m0, n0, bn, nsub;
-    unit_of(p, BM, BN, t, m0, n0, bn, nsub);
-    constexpr int ELEMS = BM * BN;
+    unit_of(p, TM, BN, t, m0, n0, bn, nsub);
+    constexpr int ELEMS = TM * BN;
     // Only the first CTA can start before the tile (its piece is its range's
     // last, slot 2c + 1, unless its range starts exactly at the tile); every
     // later CTA's range starts inside the tile: slot 2c.
@@ -1199,21 +1205,28 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // the canonical K-contiguous workspace layout.
     const bool fuse_a = pl.fuse_a && is_notrans(ta) && aligned16(A) && lda % 4 == 0;
     const bool fuse_b = pl.fuse_b && !is_notrans(tb) && aligned16(B) && ldb % 4 == 0;
-    // the pair kernel takes pre-split operands only, and no stream-K
+    // the pair kernel takes pre-split operands only; stream-K over every tile
+    // runs on single SMs, stream-K over the last wave on either
     const bool sk = pl.tc_sk > 0;
     const bool pair = pl.pair != 0 && !fuse_a && !fuse_b && !sk;
+    const bool sk_tail = !sk && pl.tc_sk_tail != 0 && !fuse_a && !fuse_b;
     const int TM = pair ? 2 * tc::BM : tc::BM;          // tile rows
     const int bdiv = pair ? 2 : 1;                      // B rows per CTA = tile columns / bdiv
     auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
     const size_t a_elems = fuse_a ? 0 : up((size_t)M * Kp * 4) / 4;
     const size_t b_elems = fuse_b ? 0 : up((size_t)N * Kp * 4) / 4;
     const int parts = three ? 2 : 1;
-    // stream-K: the iterations of all tiles (at full width) and their sharing
+    // stream-K: the iterations of the shared tiles (at full width) and their
+    // sharing -- every tile, or those after the last full wave
     const int64_t tiles_all = ((M + TM - 1) / TM) * ((N + BN - 1) / BN);
     const int nkb_all = Kp / ((three && !(BN <= 128 && fuse_a)) ? tc::KBlock<true>::BK : 32);
-    const int64_t sk_iters = sk ? tiles_all * nkb_all : 0;
-    const int sk_ctas = sk ? (int)std::min<int64_t>(pl.tc_sk, sk_iters) : 0;
-    const size_t part_elems = sk ? (size_t)2 * sk_ctas * tc::BM * BN : 0;
+    const int slots = pair ? std::max(sms / 2, 1) : std::max(sms, 1);
+    const int64_t sk_tile0 = sk_tail ? std::min<int64_t>(pl.dp_tiles, tiles_all) : 0;
+    const int64_t sk_tiles = (sk || sk_tail) ? tiles_all - sk_tile0 : 0;
+    const int64_t sk_iters = sk_tiles * nkb_all;
+    const int sk_ctas = sk ? (int)std::min<int64_t>(pl.tc_sk, sk_iters)
+                           : sk_tail ? (int)std::min<int64_t>(slots, sk_iters) : 0;
+    const size_t part_elems = sk_ctas > 0 ? (size_t)2 * sk_ctas * TM * BN : 0;
     float *a_hi = nullptr, *b_hi = nullptr, *a_lo = nullptr, *b_lo = nullptr, *partial = nullptr;
     if (a_elems + b_elems + part_elems > 0) {
         void *ws = nullptr;
@@ -1280,12 +1293,17 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.bias = epi.bias;
     p.act = epi.act;
     p.units = p.dp_tiles + (p.tiles_m * p.tiles_n - p.dp_tiles) * nsplit;
-    if (sk) {
+    p.dp_units = p.units;
+    if (sk_ctas > 0) {
         if (p.num_kb != nkb_all) return SGEMM_ERR_UNSUPPORTED;   // one k-block width
+        // whole tiles up to sk_tile0 (none for stream-K over every tile),
+        // then the shared ones; unit_of decodes every tile at full width
         p.dp_tiles = p.tiles_m * p.tiles_n;
         p.tail_nsplit = 1;
         p.units = p.dp_tiles;
+        p.dp_units = (int)sk_tile0;
         p.sk_ctas = sk_ctas;
+        p.sk_tile0 = (int)sk_tile0;
         p.sk_iters = sk_iters;
         p.partial = partial;
     }
@@ -1297,9 +1315,8 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // under the main loop of the next) unless an operand is split in the
     // kernel: the split warps are also the epilogue warps, so those CTAs take
     // one unit each.
-    // Stream-K: one CTA per share of the iterations.
-    const int slots = pair ? std::max(sms / 2, 1) : std::max(sms, 1);
-    const int groups = sk ? sk_ctas : (fuse_a || fuse_b) ? p.units : std::min(p.units, slots);
+    // Stream-K: one CTA (pair) per share of the iterations.
+    const int groups = sk_ctas > 0 ? sk_ctas : (fuse_a || fuse_b) ? p.units : std::min(p.units, slots);
     const int grid = groups * (pair ? 2 : 1);
     int st2;
     if (BN == 256)
@@ -1315,12 +1332,18 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     else
         st2 = three ? launch_main_any<64, true>(pair, maps, p, grid, s)
                     : launch_main_any<64, false>(pair, maps, p, grid, s);
-    if (st2 != SGEMM_OK || !sk) return st2;
+    if (st2 != SGEMM_OK || sk_ctas == 0) return st2;
     // the shared tiles' partial sums, added in k order, then the epilogue
-    const dim3 fgrid((unsigned)p.units, (unsigned)(tc::BM * BN / 4096));
-    if (BN == 256) tc::sk_fixup_kernel<256><<<fgrid, 256, 0, s>>>(p);
-    else if (BN == 128) tc::sk_fixup_kernel<128><<<fgrid, 256, 0, s>>>(p);
-    else tc::sk_fixup_kernel<64><<<fgrid, 256, 0, s>>>(p);
+    const dim3 fgrid((unsigned)sk_tiles, (unsigned)(TM * BN / 4096));
+    if (pair) {
+        if (BN == 256) tc::sk_fixup_kernel<256, 256><<<fgrid, 256, 0, s>>>(p);
+        else if (BN == 128) tc::sk_fixup_kernel<128, 256><<<fgrid, 256, 0, s>>>(p);
+        else tc::sk_fixup_kernel<64, 256><<<fgrid, 256, 0, s>>>(p);
+    } else {
+        if (BN == 256) tc::sk_fixup_kernel<256, 128><<<fgrid, 256, 0, s>>>(p);
+        else if (BN == 128) tc::sk_fixup_kernel<128, 128><<<fgrid, 256, 0, s>>>(p);
+        else tc::sk_fixup_kernel<64, 128><<<fgrid, 256, 0, s>>>(p);
+    }
     return last_status();
 }
 

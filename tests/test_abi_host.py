@@ -167,10 +167,10 @@ def test_plan_tensor_core_stream_k(lib):
     # 2048^3: the partial tiles' traffic outweighs the 128/152 fill
     st, p = sg.sgemm_plan("N", "N", 2048, 2048, 2048, 2048, 2048, 2048, num_sms=152)
     assert st == 0 and p["ctas"] == 128 and p["split"] == 1
-    # a full wave or more: never (4096^3 stays on SM pairs, its last wave in
-    # half-width slices)
+    # a full wave or more: never over every tile (4096^3 stays on SM pairs;
+    # its last wave of 28 tiles is shared by the 76 pairs: 3 per tile)
     st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152)
-    assert st == 0 and p["tile_m"] == 256 and p["split"] == 2 and p["ctas"] == 152
+    assert st == 0 and p["tile_m"] == 256 and p["split"] == 3 and p["ctas"] == 152
     # forced: split = 1 keeps tiles whole; split = s shares among s x tiles CTAs
     st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152, split=1)
     assert st == 0 and p["ctas"] == 128 and p["split"] == 1
@@ -186,10 +186,15 @@ def test_plan_tensor_core_stream_k(lib):
 
 
 def test_plan_tensor_core_last_wave_slices(lib):
-    # 4096^3 on SM pairs: 256 tiles = 3 waves of 76 + 28; the 28 run as 56
-    # half-width units (a half unit measured ~0.9 of a tile, so it pays here)
-    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 4096, 4096, 4096, num_sms=152)
+    # 4096 x 4096 x 256 on SM pairs: 256 tiles = 3 waves of 76 + 28; with K this
+    # short a shared last wave costs more in partial sums than it saves, and
+    # the 28 run as 56 half-width units (a half unit measured ~0.9 of a tile)
+    st, p = sg.sgemm_plan("N", "N", 4096, 4096, 256, 256, 4096, 4096, num_sms=152)
     assert st == 0 and p["tile_m"] == 256 and p["split"] == 2
+    # 4096^3 and 8192^3: the last wave shared by all pairs instead (stream-K)
+    for n in (4096, 8192):
+        st, p = sg.sgemm_plan("N", "N", n, n, n, n, n, n, num_sms=152)
+        assert st == 0 and p["tile_m"] == 256 and p["split"] > 1 and p["ctas"] == 152
     # 4095 x 3073 x 1537: 208 tiles = 2 waves + 56; narrow units would cost
     # more rounds than one more wave of whole tiles (1.43x measured)
     st, p = sg.sgemm_plan("N", "N", 4095, 3073, 1537, 1537, 3073, 3073, num_sms=152)

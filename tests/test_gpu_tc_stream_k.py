@@ -161,3 +161,45 @@ def test_last_wave_slices_sampled(oracle_mod, shape, pair):
                                      points=(rows, cols))
     rep = oracle_mod.compare(out[rows, cols], ref, bound, K, 1.0)
     assert rep["pass"], rep
+
+
+@pytest.mark.parametrize("ta,tb", [("N", "N"), ("T", "T")])
+def test_last_wave_stream_k_on_pairs_sampled(oracle_mod, ta, tb):
+    """4096 x 4096 x 2048 on SM pairs: three waves of whole 256 x 256 tiles,
+    then the k-blocks of the last 28 tiles shared by all pairs, each pair's
+    CTAs writing their 128 rows of a partial tile; the fixup adds them in k
+    order.  Seeded samples over the whole result against the oracle."""
+    import torch
+    M = N = 4096
+    K = 2048
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    lda = K if ta == "N" else M
+    ldb = N if tb == "N" else K
+    st, p = sg.sgemm_plan(ta, tb, M, N, K, lda, ldb, N, num_sms=sms)
+    assert st == 0 and p["tile_m"] == 256 and p["split"] > 1
+    opA = gi.random_matrix(111, M, K)
+    opB = gi.random_matrix(112, K, N)
+    A, B = stored(opA, ta), stored(opB, tb)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.full((M, N), float("nan"), device="cuda")
+    st = sg.sgemm(ta, tb, M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0, dC.data_ptr(), N,
+                  torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert st == 0 and sg.sgemm_device_error(torch.cuda.current_stream()) == 0
+    out = dC.cpu().numpy()
+    assert np.all(np.isfinite(out))
+    # the last wave's tiles are the last in raster order: sample them densely
+    rows, cols = gi.sample_points(M, N, 12000, seed=113)
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, 1.0, A, lda, B, ldb, 0.0, None, N,
+                                     points=(rows, cols))
+    rep = oracle_mod.compare(out[rows, cols], ref, bound, K, 1.0)
+    assert rep["pass"], rep
+    # and the whole result matches a run with every tile whole (same sums up
+    # to the order of the partial-sum additions: inside the fp32 bound)
+    dC2 = torch.full((M, N), float("nan"), device="cuda")
+    st = sg.sgemm_ex(ta, tb, M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0, dC2.data_ptr(),
+                     N, torch.cuda.current_stream(), sg.PATH_3XTF32, 1)
+    torch.cuda.synchronize()
+    assert st == 0
+    diff = np.abs(out - dC2.cpu().numpy())
+    assert np.all(diff <= 2 * 4 * K * 2.0 ** -24 * np.abs(opA).max() * np.abs(opB).max() * K)
