@@ -75,7 +75,10 @@ __device__ unsigned int g_error;        // sticky device error word (per device)
 // half (BN / 2 columns) of B, and its 128 rows of the accumulator.
 // WIDE: 3xTF32 with 32-wide k-blocks (128-byte rows): the 64- and 128-wide
 // tiles whose raw A streams from HBM (one or two tile columns read each row
-// of A), where 64-byte row pieces halve DRAM efficiency.
+// of A), where 64-byte row pieces halve DRAM efficiency.  Their split puts
+// A_hi in TMEM and A_lo in shared memory: an MMA reading A from TMEM costs
+// about the same at any N, so A_hi x [B_hi | B_lo] is one such MMA of twice
+// the width, and A_lo x B_hi a shared-memory MMA.
 template <int BN, bool THREE, bool PAIR = false, bool WIDE = false>
 struct Cfg {
     static constexpr int BK = WIDE ? 32 : KBlock<THREE>::BK;
@@ -89,20 +92,20 @@ struct Cfg {
     static constexpr int STAGES_RAW = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
-    // two accumulators (double-buffered TMEM) when they fit in the 512 columns
-    static constexpr int NBUF = 2;
-    // TMEM: the accumulators from column 0 (two of BN columns when the CTA
-    // walks several tiles); a CTA that splits A in the kernel takes one tile,
-    // so its single accumulator leaves columns 256.. for one slot of A per
-    // stage (hi, then lo: PARTS * BK columns).
+    // TMEM: the accumulators from column 0 (two of NACC * BN columns when the
+    // CTA walks several tiles); a CTA that splits A in the kernel keeps one
+    // accumulator, and the columns after it hold one slot of A per stage (hi,
+    // then lo: PARTS * BK columns; WIDE: hi only).
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int A_TMEM_COL = 256;
-    static constexpr int A_SLOT_COLS = PARTS * BK;
     // N = 64 MMAs are short enough that one dependent chain of them into a
     // single accumulator runs at about half the tensor rate: such tiles keep
     // independent accumulators (3xTF32: one per product; TF32: even and odd
-    // k-slices), summed by the epilogue.
-    static constexpr int NACC = (BN == 64 && !PAIR) ? (THREE ? 3 : 2) : 1;
+    // k-slices), summed by the epilogue.  WIDE tiles keep one per product too
+    // (lo*hi at 0, hi*hi at BN, hi*lo at BN + the unit's width).
+    static constexpr int NACC = (BN == 64 && !PAIR) ? (THREE ? 3 : 2) : (WIDE ? 3 : 1);
+    static constexpr int NBUF = WIDE ? 1 : 2;
+    static constexpr int A_TMEM_COL = WIDE ? NACC * BN : 256;
+    static constexpr int A_SLOT_COLS = WIDE ? BK : PARTS * BK;
     static_assert(NBUF * NACC * BN <= 512 && NACC * BN <= A_TMEM_COL, "accumulator columns");
     static_assert(A_TMEM_COL + STAGES * A_SLOT_COLS <= 512, "A slots in TMEM");
     static_assert(STAGES >= 2, "need at least two stages");
@@ -423,6 +426,41 @@ __device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, in
     }
 }
 
+// WIDE tiles: this thread's row of the raw A tile (128-byte swizzle), split
+// as split_a_to_tmem does, but only hi goes to tensor memory (columns tslot +
+// k); lo = round(x - hi) is stored in the A_lo tile at x's own swizzled
+// position, the layout the shared-memory MMA reads.
+template <int BK_>
+__device__ __forceinline__ void split_a_hi_lo(uint32_t raw, uint32_t lo_tile, uint32_t taddr, int q,
+                                              int half, int lane) {
+    constexpr int KH = BK_ / 2;                       // k values per thread
+    const int r = q * 32 + lane;
+    const uint32_t sw = BK_ == 16 ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
+    const uint32_t roff = (uint32_t)(r * BK_ * 4);
+#pragma unroll
+    for (int g = 0; g < KH / 8; ++g) {                // 8 k values per TMEM store
+        float hi[8];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const uint32_t chunk = (uint32_t)(half * (KH / 4) + g * 2 + c);
+            const uint32_t o = roff + ((chunk ^ sw) << 4);
+            float4 v;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(raw + o));
+            const float x[4] = {v.x, v.y, v.z, v.w};
+            float lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                hi[4 * c + e] = tf32_round(x[e]);
+                lo[e] = tf32_round(__fsub_rn(x[e], hi[4 * c + e]));
+            }
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(lo_tile + o), "f"(lo[0]), "f"(lo[1]), "f"(lo[2]), "f"(lo[3]) : "memory");
+        }
+        tmem_st8(taddr + (uint32_t)(half * KH + g * 8), hi);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group_m, int &tm,
                                        int &tn) {
@@ -549,14 +587,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto conv_bar = [&](int s) { return bar0 + 8u * (2 * K_::STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (3 * K_::STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (3 * K_::STAGES + 2 + b); };
+    // a stage: A_hi | A_lo | B_hi | B_lo, B_lo right after the unit's B_hi
+    // rows (so that [B_hi | B_lo] is one operand of twice the width)
     auto a_hi = [&](int s) { return smem0 + s * K_::STAGE_BYTES; };
-    auto b_hi = [&](int s) { return a_hi(s) + K_::A_BYTES; };
-    auto a_lo = [&](int s) { return b_hi(s) + K_::B_BYTES; };
-    auto b_lo = [&](int s) { return a_lo(s) + K_::A_BYTES; };
+    auto a_lo = [&](int s) { return a_hi(s) + K_::A_BYTES; };
+    auto b_hi = [&](int s) { return a_hi(s) + K_::PARTS * K_::A_BYTES; };
+    auto b_lo = [&](int s, int b_rows) { return b_hi(s) + (uint32_t)(b_rows * BK * 4); };
     const bool fused = p.fuse_a || p.fuse_b;
-    // 64-wide 3xTF32 tiles with A split into TMEM issue A_hi x [B_hi | B_lo]
-    // as one N = 128 MMA and A_lo x B_hi: 2 MMAs per k-slice instead of 3
-    constexpr bool BCAT = THREE && !PAIR && K_::NACC == 3;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -639,7 +676,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tma_load_2d_pair(a_hi(s), &tm_ahi, fb, kc, am);
                         tma_load_2d_pair(b_hi(s), mb_hi, fb, kc, bnn);
                         if (THREE) tma_load_2d_pair(a_lo(s), &tm_alo, fb, kc, am);
-                        if (THREE) tma_load_2d_pair(b_lo(s), mb_lo, fb, kc, bnn);
+                        if (THREE) tma_load_2d_pair(b_lo(s, b_rows), mb_lo, fb, kc, bnn);
                         continue;
                     }
                     mbar_expect_tx(full_bar(s), PAIR ? 2u * tx : tx);
@@ -647,10 +684,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d(a_hi(s), &tm_ahi, full_bar(s), kc, am);
                     tma_load_2d(b_hi(s), mb_hi, full_bar(s), kc, bnn);
                     if (THREE && !p.fuse_a) tma_load_2d(a_lo(s), &tm_alo, full_bar(s), kc, am);
-                    // with A in TMEM, A_lo's slot holds B_lo right after B_hi:
-                    // one N = 2 BN operand [B_hi | B_lo] (64-wide 3xTF32 tiles)
-                    if (THREE && !p.fuse_b)
-                        tma_load_2d(BCAT && p.fuse_a ? a_lo(s) : b_lo(s), mb_lo, full_bar(s), kc, bnn);
+                    if (THREE && !p.fuse_b) tma_load_2d(b_lo(s, b_rows), mb_lo, full_bar(s), kc, bnn);
                 }
             }
             // drain: the last arming of each stage must have landed before
@@ -702,16 +736,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint64_t bh = smem_desc<BK * 4>(b_hi(s) + off);
                             const uint32_t first = (kb == kb0 && kk == 0) ? 0u : 1u;
                             const uint32_t ah = at + (uint32_t)(kk * 8);
-                            if (BCAT && !p.fuse_b) {
-                                // [B_hi | B_lo] starts at b_hi(s): hi*hi to BN.., hi*lo to 2 BN..
+                            if (WIDE) {
+                                // A_hi (TMEM) x [B_hi | B_lo] (N = 2 bn): hi*hi to BN..,
+                                // hi*lo to BN + bn..; A_lo (shared memory) x B_hi: lo*hi to 0..
                                 const uint32_t idesc2 = idesc + ((uint32_t)(bn >> 3) << 17);
+                                const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
                                 umma_tf32_ta(d + (uint32_t)BN, ah, bh, idesc2, first);
-                                umma_tf32_ta(d, ah + (uint32_t)BK, bh, idesc, first);
+                                umma_tf32(d, al, bh, idesc, first);
                             } else if (THREE) {
-                                const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
+                                const uint64_t bl = smem_desc<BK * 4>(b_lo(s, bn) + off);
                                 const uint32_t f2 = NA == 3 ? first : 1u;
                                 umma_tf32_ta(d, ah + (uint32_t)BK, bh, idesc, first);
-                                umma_tf32_ta(d + (NA == 3 ? 2 * BN : 0), ah, bl, idesc, f2);
+                                umma_tf32_ta(d + (NA == 3 ? (uint32_t)(BN + bn) : 0u), ah, bl, idesc, f2);
                                 umma_tf32_ta(d + (NA == 3 ? BN : 0), ah, bh, idesc, f2);
                             } else {
                                 const int ka = NA == 2 ? (kk & 1) : 0;
@@ -730,7 +766,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint32_t first = (kb == kb0 && kk == 0) ? 0u : 1u;
                         if (THREE) {
                             const uint64_t al = smem_desc<BK * 4>(a_lo(s) + off);
-                            const uint64_t bl = smem_desc<BK * 4>(b_lo(s) + off);
+                            const uint64_t bl = smem_desc<BK * 4>(b_lo(s, PAIR ? bn / 2 : bn) + off);
                             if (PAIR) {
                                 umma_tf32_pair(d, al, bh, idesc, first);
                                 umma_tf32_pair(d, ah, bl, idesc, 1u);
@@ -738,7 +774,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             } else {
                                 const uint32_t f2 = NA == 3 ? first : 1u;
                                 umma_tf32(d, al, bh, idesc, first);
-                                umma_tf32(d + (NA == 3 ? 2 * BN : 0), ah, bl, idesc, f2);
+                                umma_tf32(d + (NA == 3 ? (uint32_t)(BN + bn) : 0u), ah, bl, idesc, f2);
                                 umma_tf32(d + (NA == 3 ? BN : 0), ah, bh, idesc, f2);
                             }
                         } else {
@@ -797,12 +833,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // them: no shared-memory traffic for A in the MMAs
                         const uint32_t slot = tmem + ((uint32_t)(q * 32) << 16) +
                                               (uint32_t)(K_::A_TMEM_COL + s * K_::A_SLOT_COLS);
-                        split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
+                        if (WIDE) split_a_hi_lo<BK>(a_hi(s), a_lo(s), slot, q, half, lane);
+                        else split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
                         tmem_st_wait();
                         tc_fence_before();
                     }
-                    if (p.fuse_b) {
-                        split_tile<THREE>(b_hi(s), b_lo(s), b_rows * BK * 4 / 16, ct);
+                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s, b_rows), b_rows * BK * 4 / 16, ct);
+                    if (p.fuse_b || (WIDE && p.fuse_a)) {
                         // generic-proxy stores must be visible to the tensor core's reads
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
@@ -832,7 +869,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // hi*hi + (lo*hi + hi*lo); TF32: even + odd k-slices
                     float f[32];
                     uint32_t r2[32];
-                    tmem_ld32(ta + (uint32_t)(K_::NACC == 3 ? 2 * BN : BN), r2);
+                    tmem_ld32(ta + (uint32_t)(K_::NACC == 3 ? BN + bn : BN), r2);
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj)
                         f[jj] = __fadd_rn(__uint_as_float(r[jj]), __uint_as_float(r2[jj]));
