@@ -9,7 +9,8 @@
 // tensor-core mode of "Optimising fp32 GEMM on A100", kernels 1-7, which
 // trade accuracy for speed).  An operand is split either by a pre-pass into
 // a K-contiguous workspace, or, when its rows already run along K, inside
-// the kernel: A into tensor memory, B in shared memory.
+// the kernel: A into tensor memory (on 64- and 128-wide tiles only A_hi, with
+// A_lo in shared memory), B in shared memory.
 //
 // Kernel (320 threads; tiles of 128 x BN, or 256 x BN on a pair of SMs):
 //   warp 0, one lane : TMA producer - per k-block (16 wide for 3xTF32, 32 for
@@ -29,6 +30,8 @@
 // CTAs are persistent (one per SM, or per SM pair) when no operand is split
 // in the kernel: the stage ring runs on across tiles and two TMEM
 // accumulators alternate, so a tile's epilogue overlaps the next main loop.
+// Tiles after the last full wave may be shared in k (stream-K, see Params),
+// as may every tile of a problem with fewer tiles than SMs.
 // The multi-stage ring is the asynchronous copy pipeline of "CuTe-ly
 // writing an SM86 SGEMM" (section "mainloop") and "Matmul II" (section 7)
 // rebuilt on TMA + mbarriers; the operand and accumulator placement is
