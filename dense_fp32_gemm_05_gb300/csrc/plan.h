@@ -208,8 +208,8 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // end together; tiles that several CTAs share leave partial sums for
         // a fixup pass.  Modelled in microseconds: a tile's main loop at the
         // measured MMA rate (2047 MAC per clock per SM at ~1.9 GHz; 0.75 of
-        // it reached on 128- and 256-wide tiles, 0.45 on 64-wide ones), two
-        // partial-tile epilogues per CTA (4.5 us for 128 x 256), and the
+        // it reached on 128- and 256-wide tiles, 0.45 on 64-wide ones), one
+        // or two partial-tile epilogues per CTA (4.5 us for 128 x 256), and the
         // fixup as 3 us plus its partial-tile traffic at 6 TB/s; taken when
         // 5 % faster than the choice above.  A forced split s > 1 runs
         // stream-K with min(s x tiles, 8 x SMs, iterations) CTAs; split = 1
@@ -221,12 +221,22 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         if (split > 1) {
             g_sk = std::min<int64_t>(std::min<int64_t>(tiles1 * split, 8LL * sms), iters);
         } else if (split == 0 && tiles1 < sms) {
-            const int64_t g = std::min<int64_t>(sms, iters / 8);
-            if (g > tiles1) {
-                const double epi = 2.0 * 4.5 * pl.tile_n / 256.0;
+            // g CTAs: most ranges straddle two tiles (two partial epilogues,
+            // back to back where A is split into TMEM); a multiple of the
+            // tile count keeps every range inside one tile (one epilogue)
+            const int64_t g1 = std::min<int64_t>(sms, iters / 8);
+            const int64_t g2 = tiles1 * (g1 / tiles1);
+            double t_best = 0.95 * cur_us;
+            for (int pass = 0; pass < 2; ++pass) {
+                const int64_t g = pass == 0 ? g1 : g2;
+                if (g <= tiles1 || (pass == 1 && g2 == g1)) continue;
+                const double epi = (pass == 0 && g1 % tiles1 != 0 ? 2.0 : 1.0) * 4.5 * pl.tile_n / 256.0;
                 const double fix = 3.0 + (double)(g + tiles1) * 128.0 * pl.tile_n * 8.0 / 6.0e6;
                 const double t_sk = (double)iters / (double)g / (double)nkb * tile_us + epi + fix;
-                if (t_sk < 0.95 * cur_us) g_sk = g;
+                if (t_sk < t_best) {
+                    t_best = t_sk;
+                    g_sk = g;
+                }
             }
         }
         if (g_sk > 0) {

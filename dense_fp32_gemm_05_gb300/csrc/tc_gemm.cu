@@ -980,12 +980,20 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
         const int row = m0 + r, col = n0 + cc;
         if (row >= p.M || col >= p.N) continue;
         float4 v = part[(int64_t)lo_slot * (ELEMS / 4) + e4];
-        for (int c = c_lo + 1; c <= c_hi; ++c) {
-            const float4 x = part[(int64_t)(2 * c) * (ELEMS / 4) + e4];
-            v.x = __fadd_rn(v.x, x.x);
-            v.y = __fadd_rn(v.y, x.y);
-            v.z = __fadd_rn(v.z, x.z);
-            v.w = __fadd_rn(v.w, x.w);
+        // the later partials four at a time: loads first, then the adds in order
+        for (int c = c_lo + 1; c <= c_hi; c += 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (c + u <= c_hi) x[u] = part[(int64_t)(2 * (c + u)) * (ELEMS / 4) + e4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (c + u > c_hi) break;
+                v.x = __fadd_rn(v.x, x[u].x);
+                v.y = __fadd_rn(v.y, x[u].y);
+                v.z = __fadd_rn(v.z, x[u].z);
+                v.w = __fadd_rn(v.w, x[u].w);
+            }
         }
         const float vs[4] = {v.x, v.y, v.z, v.w};
         float *dst = p.C + (int64_t)row * p.ldc + col;
@@ -1374,7 +1382,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
                     : launch_main_any<64, false>(pair, maps, p, grid, s);
     if (st2 != SGEMM_OK || sk_ctas == 0) return st2;
     // the shared tiles' partial sums, added in k order, then the epilogue
-    const dim3 fgrid((unsigned)sk_tiles, (unsigned)(TM * BN / 4096));
+    const dim3 fgrid((unsigned)sk_tiles, (unsigned)(TM * BN / 1024));   // one float4 per thread
     if (pair) {
         if (BN == 256) tc::sk_fixup_kernel<256, 256><<<fgrid, 256, 0, s>>>(p);
         else if (BN == 128) tc::sk_fixup_kernel<128, 256><<<fgrid, 256, 0, s>>>(p);

@@ -159,8 +159,12 @@ def test_plan_tensor_core_stream_k(lib):
     # the iterations are shared by one CTA per SM
     st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152)
     assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["ctas"] == 152 and p["split"] == 2
+    # 16 tiles: 9 CTAs per tile (144) keep every range inside one tile
     st, p = sg.sgemm_plan("N", "T", 2048, 64, 8192, 8192, 8192, 64, num_sms=152)
-    assert st == 0 and p["ctas"] == 152 and p["split"] == 10
+    assert st == 0 and p["ctas"] == 144 and p["split"] == 9
+    # 1024^3: 32 tiles of 128 x 256, 4 CTAs each
+    st, p = sg.sgemm_plan("N", "N", 1024, 1024, 1024, 1024, 1024, 1024, num_sms=152)
+    assert st == 0 and p["ctas"] == 128 and p["split"] == 4
     # deep K on a few tiles
     st, p = sg.sgemm_plan("N", "N", 512, 512, 16384, 16384, 512, 512, num_sms=152)
     assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["ctas"] == 152

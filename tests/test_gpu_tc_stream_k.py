@@ -102,11 +102,12 @@ def test_stream_k_fused_epilogue(oracle_mod, shape):
 
 def test_selector_takes_stream_k_for_few_tiles_and_long_k(oracle_mod):
     """2048 x 64 x 8192 NT: 16 tiles of 128 x 64 for 152 SMs.  The selector
-    shares the iterations among one CTA per SM; the whole result is checked."""
+    shares the iterations among 9 CTAs per tile (144, every range inside one
+    tile); the whole result is checked."""
     import torch
     M, N, K = 2048, 64, 8192
     st, p = sg.sgemm_plan("N", "T", M, N, K, K, K, N, num_sms=152)
-    assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["ctas"] == 152
+    assert st == 0 and p["path"] == sg.PATH_3XTF32 and p["ctas"] == 144 and p["split"] == 9
     A = gi.random_matrix(81, M, K)
     B = gi.random_matrix(82, N, K)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
