@@ -336,11 +336,24 @@ Geometry geometry(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
         g.ksplit = 1;
         return g;
     }
-    // axpy form: split K over CTAs until the grid covers 2 CTAs per SM,
-    // each CTA keeping at least 256 k (32 per warp)
+    // axpy form: split K over CTAs (each keeping at least 256 k, 32 per
+    // warp).  The time goes as the waves of 2 CTAs per SM times each CTA's
+    // k plus a fixed cost (staging Small, the reduction, the partial sums)
+    // of about 256 k, so take the split that minimises that (128 column
+    // blocks, K = 8192, 2 x 152 slots: 7 slices fill 2.95 waves, where the 3
+    // that first cover one wave leave 1.26).
     const int pblocks = (g.P + gemv::AX_P - 1) / gemv::AX_P;
-    int64_t ks = std::max(1, (2 * sms + pblocks - 1) / pblocks);
-    ks = std::min<int64_t>(ks, std::max<int64_t>(1, K / 256));
+    const int64_t slots = std::max(1, 2 * sms);
+    const int64_t ks_max = std::max<int64_t>(1, std::min<int64_t>(K / 256, 64));
+    int64_t ks = 1;
+    double best = 1e30;
+    for (int64_t c = 1; c <= ks_max; ++c) {
+        const double t = (double)((pblocks * c + slots - 1) / slots) * ((double)K / (double)c + 256.0);
+        if (t < best * 0.999) {
+            best = t;
+            ks = c;
+        }
+    }
     g.kchunk = (int)((K + ks - 1) / ks);
     g.ksplit = (int)((K + g.kchunk - 1) / g.kchunk);
     g.ctas = pblocks * g.ksplit;
