@@ -204,3 +204,37 @@ def test_last_wave_stream_k_on_pairs_sampled(oracle_mod, ta, tb):
     assert st == 0
     diff = np.abs(out - dC2.cpu().numpy())
     assert np.all(diff <= 2 * 4 * K * 2.0 ** -24 * np.abs(opA).max() * np.abs(opB).max() * K)
+
+
+@pytest.mark.parametrize("ta,tb,N", [("N", "N", 128), ("N", "T", 128), ("N", "T", 96)])
+def test_narrow_tile_last_wave_slices_sampled(oracle_mod, ta, tb, N):
+    """20480 x N x 256 with A split in the kernel: 160 tiles of 128 x 128 (A_hi in
+    TMEM, A_lo in shared memory, one N = 2 x width MMA over [B_hi | B_lo]); the
+    8 after the full wave run as 64-wide units, whose hi*lo products land at
+    column 128 + 64 of the accumulator.  N = 96 also cuts the last unit's
+    columns short.  Seeded samples, the last rows and columns included."""
+    import torch
+    M, K = 20480, 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ldb = N if tb == "N" else K
+    st, p = sg.sgemm_plan(ta, tb, M, N, K, K, ldb, N, num_sms=sms)
+    assert st == 0 and p["tile_n"] == 128 and (sms != 152 or p["split"] == 2)
+    opA = gi.random_matrix(121, M, K)
+    opB = gi.random_matrix(122, K, N)
+    A, B = stored(opA, ta), stored(opB, tb)
+    C = gi.random_matrix(123, M, N)
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
+    st = sg.sgemm(ta, tb, M, N, K, 1.5, dA.data_ptr(), K, dB.data_ptr(), ldb, -0.5, dC.data_ptr(), N,
+                  torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert st == 0 and sg.sgemm_device_error(torch.cuda.current_stream()) == 0
+    out = dC.cpu().numpy()
+    rows, cols = gi.sample_points(M, N, 16000, seed=124)
+    # and every column of the last 1024 rows (the last tiles in raster order)
+    tail_r = np.repeat(np.arange(M - 1024, M), N)
+    tail_c = np.tile(np.arange(N), 1024)
+    rows, cols = np.concatenate([rows, tail_r]), np.concatenate([cols, tail_c])
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, 1.5, A, K, B, ldb, -0.5, C, N,
+                                     points=(rows, cols))
+    rep = oracle_mod.compare(out[rows, cols], ref, bound, K, 1.5)
+    assert rep["pass"], rep
