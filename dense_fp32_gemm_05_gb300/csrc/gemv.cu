@@ -4,8 +4,8 @@
 // ("What cuBLAS does that we do not"): when M is 1 (decode) to a few dozen,
 // none of the tile kernels' compute tricks apply; the GEMM is a memory-bound
 // GEMV and the only thing that counts is streaming the large operand once.
-// So this path has no tiles and no shared-memory staging of the large
-// operand.  With S = min(M, N) (the small dimension) and P the other one:
+// So this path has no tiles.  With S = min(M, N) (the small dimension) and P
+// the other one:
 //
 //   out(s, p) = sum_k Small(s, k) * Big(p, k)
 //
@@ -25,16 +25,22 @@
 //     interleaved k of the CTA's K range and are added through shared
 //     memory in warp order; when K is also split across CTAs (to fill the
 //     GPU), the CTAs' partial sums are added in K order by a second kernel.
+//     For S = 8 and 16, where 16 or 64 accumulators per lane leave few
+//     registers for row loads, a variant streams Big through a shared-memory
+//     ring with TMA instead (gemv_axpy_tma_kernel).
 // Every sum is a fixed order of fp32 FMAs and adds: deterministic, and, as
 // any summation order, inside the 4 K 2^-24 bound.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/sgemm_gb300.h"
 #include "gemv.h"
 #include "plan.h"
+#include "ptx_util.cuh"
 #include "tc_gemm.h"
 
 namespace sgemm_gb300 {
@@ -59,7 +65,10 @@ struct Params {
     const float *row_scale;            // fused epilogue: M row scales or null
     const float *bias;                 // N column biases or null
     int act;                           // SGEMM_ACT_*
+    unsigned long long wait_ns;        // bounded-wait limit of the staged kernel
 };
+
+__device__ unsigned int g_error;       // sticky device error word of this path
 
 __device__ __forceinline__ void store_out(const Params &p, int s, int q, float v) {
     float *dst = p.C + (int64_t)s * p.c_s + (int64_t)q * p.c_p;
@@ -241,6 +250,183 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_axpy_kernel(const Params p) {
     }
 }
 
+// ------------------------------------------------------------ axpy form, staged
+// For S = 8 and 16 the axpy kernel above holds its row loads in registers
+// next to 64 accumulators, too few bytes in flight per SM to stream Big at
+// HBM speed.  This variant moves Big through shared memory instead: one
+// producer warp streams boxes of TX_KS rows x 128 columns of Big with TMA into
+// a ring of TX_ST stages (tensor map over Big: p innermost, row stride
+// big_ld), and TX_CW consumer warps read their rows from there.  Warp w takes
+// rows 4w .. 4w+3 of each stage; the sums per output stay in k order within
+// a warp and the warps are added in warp order, as in the kernel above.  Eight
+// warps per CTA (7 consumers + the producer) keep 2 CTAs per SM at 128
+// registers a thread; 9 would put 5 warps on some of the SM's 4 schedulers
+// and cap them at 96 (measured: spills on the 16-output kernel).
+constexpr int TX_CW = 7;               // consumer warps
+constexpr int TX_CT = TX_CW * 32;      // consumer threads
+constexpr int TX_KS = 4 * TX_CW;       // rows of Big per stage: 4 per consumer warp
+constexpr int TX_KC = 9 * TX_KS;       // rows per Small chunk (9 stages)
+constexpr int TX_ST = 6;               // stages in flight
+constexpr int TX_THREADS = TX_CT + 32;     // + the producer warp
+constexpr int TX_STAGE_FLOATS = TX_KS * AX_P;
+
+template <int SM>
+constexpr int tx_smem_bytes() {
+    // ring, Small chunk, barriers (the reduction reuses the ring), alignment
+    // slack: two CTAs per SM
+    return (TX_ST * TX_STAGE_FLOATS + TX_KC * SM) * 4 + 2 * TX_ST * 8 + 128;
+}
+
+__device__ __forceinline__ uint32_t tx_su32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ bool tx_try(uint32_t bar, uint32_t ph) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}" : "=r"(ok) : "r"(bar), "r"(ph) : "memory");
+    return ok != 0;
+}
+// Bounded wait; on expiry the device error word is raised and false returned.
+__device__ __forceinline__ bool tx_wait(uint32_t bar, uint32_t ph, uint64_t limit_ns) {
+    if (tx_try(bar, ph)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!tx_try(bar, ph)) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicExch(&g_error, (unsigned)SGEMM_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int SM>
+__global__ void __launch_bounds__(TX_THREADS, 2)
+    gemv_axpy_tma_kernel(const __grid_constant__ CUtensorMap big_map, const Params p) {
+    extern __shared__ __align__(16) float tx_smem[];
+    // the ring on a 128-byte boundary (TMA destination), as an element offset
+    // from the shared array so that every access stays a shared-memory one
+    float *ring = tx_smem + (((128u - (tx_su32(tx_smem) & 127u)) & 127u) >> 2);
+    float *smt = ring + TX_ST * TX_STAGE_FLOATS;        // Small chunk, [TX_KC][SM]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smt + TX_KC * SM);
+    const uint32_t bar0 = tx_su32(bars);
+    auto full = [&](int st) { return bar0 + 8u * st; };
+    auto empty = [&](int st) { return bar0 + 8u * (TX_ST + st); };
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int p0 = blockIdx.x * AX_P;
+    const int k0 = blockIdx.y * p.kchunk;
+    const int k1 = min(p.K, k0 + p.kchunk);
+    const int nst = (k1 - k0 + TX_KS - 1) / TX_KS;      // stages of this CTA
+    const uint64_t lim = p.wait_ns;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < TX_ST; ++st) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(full(st)) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(empty(st)), "r"(TX_CW) : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&big_map)) : "memory");
+    }
+    __syncthreads();
+
+    if (warp == TX_CW) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            int i = 0;
+            for (; i < nst; ++i) {
+                const int st = i % TX_ST;
+                const uint32_t ph = (uint32_t)(i / TX_ST) & 1u;
+                if (!tx_wait(empty(st), ph ^ 1u, lim)) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                             :: "r"(full(st)), "r"((uint32_t)(TX_STAGE_FLOATS * 4)) : "memory");
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%3, %4}], [%2];"
+                    :: "r"(tx_su32(ring + st * TX_STAGE_FLOATS)),
+                       "l"(reinterpret_cast<uint64_t>(&big_map)), "r"(full(st)), "r"(p0),
+                       "r"(k0 + i * TX_KS)
+                    : "memory");
+            }
+            // every issued copy has landed before the CTA can leave (a fixed
+            // 1 s bound, independent of the settable limit, so that a tiny
+            // limit never cuts the drain short)
+            for (int q = (i > TX_ST ? i - TX_ST : 0); q < i; ++q)
+                tx_wait(full(q % TX_ST), (uint32_t)(q / TX_ST) & 1u, 1000000000ull);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers (warps 0..TX_CW-1)
+    float2 acc[SM][2];
+#pragma unroll
+    for (int s = 0; s < SM; ++s) acc[s][0] = acc[s][1] = make_float2(0.0f, 0.0f);
+    const bool s_fast = p.small_ss == 1;
+    // A failed wait stops the compute and the empty-slot arrivals (the
+    // producer then times out too), but never a barrier: every consumer
+    // thread runs the same sequence of named-barrier syncs.
+    bool ok = true;
+    int i = 0;                                          // next stage
+    for (int kc = k0; kc < k1; kc += TX_KC) {
+        const int kn = min(TX_KC, k1 - kc);
+        asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");   // previous chunk consumed
+        for (int t = threadIdx.x; t < kn * SM; t += TX_CT) {
+            const int s = s_fast ? t % SM : t / kn;
+            const int kk = s_fast ? t / SM : t % kn;
+            smt[kk * SM + s] = s < p.S ? __ldg(p.small + (int64_t)s * p.small_ss +
+                                               (int64_t)(kc + kk) * p.small_sk)
+                                       : 0.0f;
+        }
+        asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
+        // the stages of this chunk (TX_KC is a multiple of TX_KS)
+        for (; i < nst && k0 + i * TX_KS < kc + kn; ++i) {
+            const int st = i % TX_ST;
+            if (ok && !tx_wait(full(st), (uint32_t)(i / TX_ST) & 1u, lim)) ok = false;
+            if (!ok) continue;
+            const float *rows = ring + st * TX_STAGE_FLOATS;
+#pragma unroll
+            for (int u = 0; u < TX_KS / TX_CW; ++u) {
+                const int r = warp * (TX_KS / TX_CW) + u;
+                const int k = k0 + i * TX_KS + r;
+                if (k >= k1) break;
+                const float4 b = *reinterpret_cast<const float4 *>(rows + r * AX_P + lane * 4);
+                const float *a = smt + (k - kc) * SM;  // the same address in every lane
+                const float2 b01 = make_float2(b.x, b.y);
+                const float2 b23 = make_float2(b.z, b.w);
+                // Small four values at a time: few registers beside the accumulators
+#pragma unroll
+                for (int s = 0; s < SM; s += 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(a + s);
+                    const float av[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a2 = make_float2(av[e], av[e]);
+                        acc[s + e][0] = __ffma2_rn(a2, b01, acc[s + e][0]);
+                        acc[s + e][1] = __ffma2_rn(a2, b23, acc[s + e][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(empty(st)) : "memory");
+        }
+    }
+    // all consumers are past the ring before it is reused for the reduction
+    asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
+    float *red = ring;                                  // [TX_CW][SM][AX_P]
+#pragma unroll
+    for (int s = 0; s < SM; ++s)
+        *reinterpret_cast<float4 *>(red + (warp * SM + s) * AX_P + lane * 4) =
+            make_float4(acc[s][0].x, acc[s][0].y, acc[s][1].x, acc[s][1].y);
+    asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
+    for (int o = threadIdx.x; o < SM * AX_P; o += TX_CT) {
+        const int s = o / AX_P, q = o % AX_P;
+        const int pp = p0 + q;
+        if (s >= p.S || pp >= p.P) continue;
+        float v = red[s * AX_P + q];
+        for (int w = 1; w < TX_CW; ++w) v = __fadd_rn(v, red[(w * SM + s) * AX_P + q]);
+        if (p.ksplit == 1) store_out(p, s, pp, v);
+        else p.partial[((int64_t)blockIdx.y * p.S + s) * p.P + pp] = v;
+    }
+}
+
 // The K-split CTAs' partial sums, added in K order, then the epilogue.
 __global__ void __launch_bounds__(THREADS) gemv_ksum_kernel(const Params p) {
     const int64_t n = (int64_t)p.S * p.P;
@@ -303,6 +489,63 @@ int launch_axpy_s(const gemv::Params &p, cudaStream_t s) {
 
 bool al16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
 
+std::mutex g_gemv_mu;
+uint64_t g_gemv_wait_ns = 2000000000ull;   // 2 s, as the tensor-core path
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn gemv_encode_fn() {
+    static EncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(ptr);
+    });
+    return fn;
+}
+
+// The staged axpy kernel (S = 8 or 16, Big 16-byte aligned with a leading
+// dimension that is a multiple of 4).  Returns false when it cannot run, so
+// that the caller launches the register-staged kernel instead.
+template <int SM>
+bool launch_axpy_tma(const gemv::Params &p, cudaStream_t s, int *status) {
+    EncodeFn enc = gemv_encode_fn();
+    if (!enc) return false;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.P, (cuuint64_t)p.K};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.big_ld * sizeof(float)};
+    const cuuint32_t box[2] = {(cuuint32_t)gemv::AX_P, (cuuint32_t)gemv::TX_KS};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(p.big), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    auto kern = gemv::gemv_axpy_tma_kernel<SM>;
+    const int smem = gemv::tx_smem_bytes<SM>();
+    static uint64_t attr_done = 0;   // bit d: the opt-in is set on device d
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { *status = SGEMM_ERR_CUDA; return true; }
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
+    }
+    dim3 grid((p.P + gemv::AX_P - 1) / gemv::AX_P, p.ksplit);
+    kern<<<grid, gemv::TX_THREADS, smem, s>>>(map, p);
+    *status = SGEMM_OK;
+    return true;
+}
+
 int last_cuda_status() {
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }
@@ -361,6 +604,19 @@ Geometry geometry(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
 }
 
 }  // namespace
+
+void gemv_set_wait_limit(uint64_t ns) {
+    std::lock_guard<std::mutex> lk(g_gemv_mu);
+    g_gemv_wait_ns = ns ? ns : 2000000000ull;
+}
+
+int gemv_take_device_error() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, gemv::g_error, sizeof(v)) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(gemv::g_error, &zero, sizeof(zero)) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return v == 0 ? SGEMM_OK : (int)v;
+}
 
 int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
     return geometry(ta, tb, M, N, std::max<int64_t>(K, 1), sms).ctas;
@@ -426,8 +682,16 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
         p.partial = static_cast<float *>(ws);
     }
     const bool vec = al16(p.big) && p.big_ld % 4 == 0;
+    {
+        std::lock_guard<std::mutex> lk(g_gemv_mu);
+        p.wait_ns = g_gemv_wait_ns;
+    }
     timing_mark(s, true);
-    int st = vec ? launch_axpy_s<true>(p, s) : launch_axpy_s<false>(p, s);
+    int st = SGEMM_OK;
+    bool staged = false;
+    if (vec && p.S > 4)
+        staged = p.S <= 8 ? launch_axpy_tma<8>(p, s, &st) : launch_axpy_tma<16>(p, s, &st);
+    if (!staged) st = vec ? launch_axpy_s<true>(p, s) : launch_axpy_s<false>(p, s);
     timing_mark(s, false);
     if (st != SGEMM_OK) return st;
     if (p.ksplit > 1) {

@@ -14,6 +14,12 @@ constexpr int64_t kGemvMaxSmall = 16;
 // CTAs of the main GEMV launch for this problem (what run_gemv launches).
 int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms);
 
+// Bounded-wait limit of the staged kernel (ns; 0 = the default 2 s).
+void gemv_set_wait_limit(uint64_t ns);
+
+// Reads and clears the current device's sticky error word of this path.
+int gemv_take_device_error();
+
 // Arguments already validated (check_args), M, N, K > 0, alpha != 0.
 int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
              int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,

@@ -327,11 +327,15 @@ extern "C" const char *sgemm_status_string(int status) {
 extern "C" int sgemm_device_error(sgemm_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SGEMM_ERR_CUDA;
-    return tc_take_device_error();
+    // both words are read (and cleared); the tensor cores' is reported first
+    const int t = tc_take_device_error();
+    const int g = gemv_take_device_error();
+    return t != SGEMM_OK ? t : g;
 }
 
 extern "C" int sgemm_set_wait_limit(uint64_t nanoseconds) {
     tc_set_wait_limit(nanoseconds);
+    gemv_set_wait_limit(nanoseconds);
     return SGEMM_OK;
 }
 

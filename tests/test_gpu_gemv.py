@@ -123,3 +123,32 @@ def test_gemv_forced_on_a_wide_problem_is_refused():
     st = sg.sgemm_ex("N", "N", 64, 64, 64, 1.0, x.data_ptr(), 64, x.data_ptr(), 64, 0.0,
                      x.data_ptr(), 64, torch.cuda.current_stream(), sg.PATH_GEMV, 0)
     assert st == sg.SGEMM_ERR_UNSUPPORTED
+
+
+def test_staged_axpy_timeout_reports_and_recovers(oracle_mod):
+    """The thin-problem kernel that stages the large operand through shared
+    memory with TMA (S = 16, large operand K x N row-major): a 1 ns wait limit
+    makes its bounded waits run out; the call raises SGEMM_ERR_TIMEOUT through
+    the device error word and the next call computes the right result."""
+    import torch
+    M, N, K = 16, 4096, 4096
+    A = gi.random_matrix(61, M, K)
+    B = gi.random_matrix(62, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), device="cuda")
+    s = torch.cuda.current_stream()
+    assert sg.sgemm_device_error(s) == 0
+    assert sg.sgemm_set_wait_limit(1) == 0
+    try:
+        st = sg.sgemm_ex("N", "N", M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                         dC.data_ptr(), N, s, sg.PATH_GEMV, 0)
+        assert st == 0
+        assert sg.sgemm_device_error(s) == sg.SGEMM_ERR_TIMEOUT
+        assert sg.sgemm_device_error(s) == 0          # read-and-clear
+    finally:
+        sg.sgemm_set_wait_limit(0)
+    st = sg.sgemm_ex("N", "N", M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                     dC.data_ptr(), N, s, sg.PATH_GEMV, 0)
+    assert st == 0 and sg.sgemm_device_error(s) == 0
+    ref, bound = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    assert oracle_mod.compare(dC.cpu().numpy(), ref, bound, K, 1.0)["pass"]
