@@ -417,6 +417,12 @@ def gpu_arm(args):
         ref, bound = oracle.gemm_f64(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A, lda, B, ldb,
                                      w.beta, C, ldc, points=(rows_s, cols_s))
     wanted = set(args.paths.split(","))
+    # The per-path timings start from an idle GPU (the power-capped clock of the
+    # tensor-core steps above does not carry over into them), and each records
+    # the SM clock samples taken while it ran.
+    path_clocks = ClockSampler(local)
+    path_clocks.start()
+    time.sleep(1.0)
     for name, pid in (("ffma", sg.PATH_FFMA), ("3xtf32", sg.PATH_3XTF32), ("tf32", sg.PATH_TF32)):
         if name not in wanted:
             continue
@@ -427,7 +433,8 @@ def gpu_arm(args):
             continue
         torch.cuda.synchronize(dev)
         ms = []
-        for _ in range(max(3, args.path_reps)):
+        t_pb = time.perf_counter()
+        for _ in range(max(20 if name == "ffma" else 3, args.path_reps)):
             flush.fill_(0.5)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -436,12 +443,18 @@ def gpu_arm(args):
             e1.record(stream)
             ms.append((e0, e1))
         torch.cuda.synchronize(dev)
+        t_pe = time.perf_counter()
         t = statistics.median([a.elapsed_time(b) for a, b in ms])
         tfl = w.flops / (t / 1e3) / 1e12
         ent = {"ms": t, "tflops": tfl}
+        time.sleep(0.05)
+        ck = path_clocks.summary(t_pb, t_pe + 0.025) if path_clocks.proc else path_clocks.summary()
+        ent["clocks"] = {"sm_mhz": ck["sm_mhz"], "reasons": ck["reasons"], "samples": ck["samples"]}
         if name == "ffma":
             ent["frac_ffma_peak_max_clock"] = tfl / ffma_peak
             ent["frac_ffma_peak_median_clock"] = tfl / ffma_peak_med
+            if ck["sm_mhz"]:
+                ent["frac_ffma_peak_sampled_clock"] = tfl / (sms * FP32_LANES_PER_SM * 2 * ck["sm_mhz"] * 1e6 / 1e12)
         else:
             mult = 3 if name == "3xtf32" else 1
             ent["tensor_tflops"] = mult * tfl
@@ -453,6 +466,7 @@ def gpu_arm(args):
             ent.update({"oracle_pass": rep["pass"], "max_err_over_bound": rep["max_err_over_bound"],
                         "max_rel": rep["max_rel"]})
         paths[name] = ent
+    path_clocks.stop()
 
     # ---- every workload through the selector, against its path's roofline
     workloads = None
