@@ -209,7 +209,8 @@ const char *sgemm_status_string(int status);
 
 /*
  * sgemm_device_error - synchronises `stream`, then returns and clears the
- * library's sticky device error word on the current device: SGEMM_OK, or
+ * library's sticky device error words on the current device (one per path
+ * with device-side waits; the tensor cores' is reported first): SGEMM_OK, or
  * SGEMM_ERR_TIMEOUT when a bounded device-side wait gave up (the kernel
  * then stopped early and its C is undefined).  SGEMM_ERR_CUDA if the
  * synchronisation itself failed.
@@ -218,9 +219,10 @@ int sgemm_device_error(sgemm_stream_t stream);
 
 /*
  * sgemm_set_wait_limit - spin limit for the device-side waits of the
- * tensor-core path, in nanoseconds of %globaltimer (0 restores the default
- * of 2 s).  A test hook: a tiny limit makes a wait run out on purpose so that
- * the timeout path can be checked without hanging anything.
+ * tensor-core path and of the thin-problem kernel that stages its large
+ * operand through shared memory, in nanoseconds of %globaltimer (0 restores
+ * the default of 2 s).  A test hook: a tiny limit makes a wait run out on
+ * purpose so that the timeout path can be checked without hanging anything.
  */
 int sgemm_set_wait_limit(uint64_t nanoseconds);
 
