@@ -395,6 +395,7 @@ template <bool A_KMAJOR, bool B_KMAJOR, bool VEC>
 __global__ void __launch_bounds__(THREADS, 2) ffma_gemm_kernel(const Params p) {
     __shared__ __align__(16) float sA[2][BK * BM];
     __shared__ __align__(16) float sB[2][BK * BN];
+    pdl_trigger();   // the stream-K fixup may launch; it waits for this grid
     if ((int)blockIdx.x < p.dp_tiles) {
         run_share<A_KMAJOR, B_KMAJOR, VEC>(p, sA, sB, blockIdx.x, 0, p.kt, 0);
         return;
@@ -427,6 +428,7 @@ constexpr int FIX_MAX_SHARES = 64;
 __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
     __shared__ int slots[FIX_MAX_SHARES];
     __shared__ int nslots;
+    pdl_wait();   // the main kernel's partial blocks are complete and visible
     const int u = blockIdx.x;
     const int64_t x0 = (int64_t)u * p.kt;
     const int c_lo = share_owner(p.sk_iters, p.sk_ctas, x0);

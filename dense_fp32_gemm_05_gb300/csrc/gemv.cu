@@ -159,6 +159,7 @@ constexpr int ax_smem_floats() { return WARPS * SM * AX_P + AX_KC * SM; }
 
 template <int SM, bool VEC>
 __global__ void __launch_bounds__(THREADS, 2) gemv_axpy_kernel(const Params p) {
+    pdl_trigger();   // the K-split sum may launch; it waits for this grid
     extern __shared__ __align__(16) float smem_f[];
     float *red = smem_f;                               // [WARPS][SM][AX_P]
     float *smt = smem_f + WARPS * SM * AX_P;           // Small chunk, [AX_KC][SM]
@@ -302,6 +303,7 @@ __device__ __forceinline__ bool tx_wait(uint32_t bar, uint32_t ph, uint64_t limi
 template <int SM>
 __global__ void __launch_bounds__(TX_THREADS, 2)
     gemv_axpy_tma_kernel(const __grid_constant__ CUtensorMap big_map, const Params p) {
+    pdl_trigger();   // the K-split sum may launch; it waits for this grid
     extern __shared__ __align__(16) float tx_smem[];
     // the ring on a 128-byte boundary (TMA destination), as an element offset
     // from the shared array so that every access stays a shared-memory one
@@ -429,6 +431,7 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
 
 // The K-split CTAs' partial sums, added in K order, then the epilogue.
 __global__ void __launch_bounds__(THREADS) gemv_ksum_kernel(const Params p) {
+    pdl_wait();   // the K-split CTAs' partial sums are complete and visible
     const int64_t n = (int64_t)p.S * p.P;
     for (int64_t o = blockIdx.x * (int64_t)THREADS + threadIdx.x; o < n;
          o += (int64_t)gridDim.x * THREADS) {
@@ -697,7 +700,7 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
     if (p.ksplit > 1) {
         const int64_t n = (int64_t)p.S * p.P;
         const int blocks = (int)std::min<int64_t>((n + gemv::THREADS - 1) / gemv::THREADS, 4 * sms);
-        gemv::gemv_ksum_kernel<<<blocks, gemv::THREADS, 0, s>>>(p);
+        launch_dependent(gemv::gemv_ksum_kernel, dim3(blocks), dim3(gemv::THREADS), 0, s, p);
     }
     return last_cuda_status();
 }

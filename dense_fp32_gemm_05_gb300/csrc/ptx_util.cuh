@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace sgemm_gb300 {
@@ -40,6 +41,41 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Programmatic dependent launch (griddepcontrol).  A kernel launched by
+// launch_dependent() may start while the kernel before it in the stream is
+// still running.  pdl_wait() returns once that kernel has completed and its
+// memory operations are visible, so a dependent kernel calls it before it
+// touches global memory; for a kernel launched the ordinary way it returns at
+// once.  pdl_trigger() lets the dependent kernel start launching as soon as
+// every CTA of this grid has called it or exited; it changes nothing about
+// when this grid's writes become visible.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// kern<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization: only the library's own second and third kernels of one call
+// are launched this way, each of which starts with pdl_wait().
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                           size_t smem, cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace sgemm_gb300

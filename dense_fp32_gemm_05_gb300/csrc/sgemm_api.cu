@@ -195,7 +195,8 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
     timing_mark(s, false);
     if (st != SGEMM_OK) return st;
     if (partials) {
-        ffma::sk_fixup_kernel<<<dim3(ffma_fix_tiles(p), ffma::FIX_PARTS), 256, 0, s>>>(p);
+        launch_dependent(ffma::sk_fixup_kernel, dim3(ffma_fix_tiles(p), ffma::FIX_PARTS), dim3(256), 0,
+                         s, p);
         st = launch_status();
     }
     return st;
@@ -476,7 +477,8 @@ extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, in
     st = launch_ffma(p, transA, transB, pl.vector != 0, s);
     if (st != SGEMM_OK) return st;
     if (partials) {
-        ffma::sk_fixup_kernel<<<dim3(ffma_fix_tiles(p), ffma::FIX_PARTS), 256, 0, s>>>(p);
+        launch_dependent(ffma::sk_fixup_kernel, dim3(ffma_fix_tiles(p), ffma::FIX_PARTS), dim3(256), 0,
+                         s, p);
         st = launch_status();
     }
     return st;

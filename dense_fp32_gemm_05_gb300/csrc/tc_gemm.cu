@@ -641,6 +641,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched after the split pre-pass, the setup above ran while the
+    // pre-pass finished; its outputs are read only after this wait.  The
+    // stream-K fixup may start launching now (it waits for this grid).
+    pdl_wait();
+    pdl_trigger();
 
     const uint64_t lim = p.wait_ns;
     // A CTA that splits A into TMEM has one accumulator (the A slots take
@@ -959,6 +964,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // floor(c * T / G) <= x.
 template <int BN, int TM>
 __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
+    pdl_wait();   // the main kernel's partial sums are complete and visible
     const long long T = p.sk_iters, G = p.sk_ctas;
     const int t = p.sk_tile0 + (int)blockIdx.x;
     const long long first = (long long)blockIdx.x * p.num_kb, last = first + p.num_kb - 1;
@@ -1051,6 +1057,7 @@ __device__ __forceinline__ void split_store4(const SplitJob &j, int64_t o, float
 // around through shared memory so that reads and writes are both coalesced.
 template <bool THREE>
 __global__ void __launch_bounds__(256) split_pair_kernel(const SplitJob j0, const SplitJob j1) {
+    pdl_trigger();   // the main kernel may launch; it waits for this grid's writes
     __shared__ float tile[32][33];
     const bool second = (int)blockIdx.x >= j0.blocks;
     const SplitJob &j = second ? j1 : j0;
@@ -1177,8 +1184,11 @@ static void launch_split_pair(bool three, const tc::SplitJob &a, const tc::Split
     else tc::split_pair_kernel<false><<<blocks, 256, 0, s>>>(a, b);
 }
 
+// dep: the split pre-pass was launched just before, so this launch is its
+// programmatic dependent (the kernel's setup overlaps the pre-pass's tail).
 template <int BN, bool THREE, bool PAIR, bool WIDE = false>
-static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, cudaStream_t s) {
+static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, cudaStream_t s,
+                       bool dep) {
     using K_ = tc::Cfg<BN, THREE, PAIR, WIDE>;
     auto kern = tc::tc_gemm_kernel<BN, THREE, PAIR, WIDE>;
     // the shared-memory opt-in is a per-device function attribute
@@ -1200,14 +1210,19 @@ static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, c
         cfg.blockDim = dim3(tc::THREADS);
         cfg.dynamicSmemBytes = K_::SMEM;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = dep ? 2 : 1;
         cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    } else if (dep) {
+        launch_dependent(kern, dim3(grid), dim3(tc::THREADS), K_::SMEM, s, maps[0], maps[1],
+                         maps[2], maps[3], maps[4], maps[5], p);
     } else {
         kern<<<grid, tc::THREADS, K_::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                    maps[5], p);
@@ -1218,9 +1233,9 @@ static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, c
 
 template <int BN, bool THREE>
 static int launch_main_any(bool pair, const CUtensorMap *maps, const tc::Params &p, int grid,
-                           cudaStream_t s) {
-    return pair ? launch_main<BN, THREE, true>(maps, p, grid, s)
-                : launch_main<BN, THREE, false>(maps, p, grid, s);
+                           cudaStream_t s, bool dep) {
+    return pair ? launch_main<BN, THREE, true>(maps, p, grid, s, dep)
+                : launch_main<BN, THREE, false>(maps, p, grid, s, dep);
 }
 
 // 2-D map over a caller's K-contiguous fp32 operand (`rows` rows of K values,
@@ -1294,6 +1309,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     if (!fuse_a) ja = split_job(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, three ? a_lo : nullptr);
     if (!fuse_b) jb = split_job(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, three ? b_lo : nullptr);
     launch_split_pair(three, ja, jb, s);
+    const bool dep = ja.blocks + jb.blocks > 0;
     int st = last_status();
     if (st != SGEMM_OK) return st;
 
@@ -1368,30 +1384,30 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     const int grid = groups * (pair ? 2 : 1);
     int st2;
     if (BN == 256)
-        st2 = three ? launch_main_any<256, true>(pair, maps, p, grid, s)
-                    : launch_main_any<256, false>(pair, maps, p, grid, s);
+        st2 = three ? launch_main_any<256, true>(pair, maps, p, grid, s, dep)
+                    : launch_main_any<256, false>(pair, maps, p, grid, s, dep);
     else if (BN == 128 && wide)
-        st2 = launch_main<128, true, false, true>(maps, p, grid, s);
+        st2 = launch_main<128, true, false, true>(maps, p, grid, s, dep);
     else if (BN == 128)
-        st2 = three ? launch_main_any<128, true>(pair, maps, p, grid, s)
-                    : launch_main_any<128, false>(pair, maps, p, grid, s);
+        st2 = three ? launch_main_any<128, true>(pair, maps, p, grid, s, dep)
+                    : launch_main_any<128, false>(pair, maps, p, grid, s, dep);
     else if (wide)
-        st2 = launch_main<64, true, false, true>(maps, p, grid, s);
+        st2 = launch_main<64, true, false, true>(maps, p, grid, s, dep);
     else
-        st2 = three ? launch_main_any<64, true>(pair, maps, p, grid, s)
-                    : launch_main_any<64, false>(pair, maps, p, grid, s);
+        st2 = three ? launch_main_any<64, true>(pair, maps, p, grid, s, dep)
+                    : launch_main_any<64, false>(pair, maps, p, grid, s, dep);
     if (st2 != SGEMM_OK || sk_ctas == 0) return st2;
     // the shared tiles' partial sums, added in k order, then the epilogue
     const dim3 fgrid((unsigned)sk_tiles, (unsigned)(TM * BN / 1024));   // one float4 per thread
-    if (pair) {
-        if (BN == 256) tc::sk_fixup_kernel<256, 256><<<fgrid, 256, 0, s>>>(p);
-        else if (BN == 128) tc::sk_fixup_kernel<128, 256><<<fgrid, 256, 0, s>>>(p);
-        else tc::sk_fixup_kernel<64, 256><<<fgrid, 256, 0, s>>>(p);
-    } else {
-        if (BN == 256) tc::sk_fixup_kernel<256, 128><<<fgrid, 256, 0, s>>>(p);
-        else if (BN == 128) tc::sk_fixup_kernel<128, 128><<<fgrid, 256, 0, s>>>(p);
-        else tc::sk_fixup_kernel<64, 128><<<fgrid, 256, 0, s>>>(p);
-    }
+    // a programmatic dependent of the main kernel: it launches while the
+    // main kernel runs and waits for it in pdl_wait()
+    auto fix = pair ? (BN == 256   ? tc::sk_fixup_kernel<256, 256>
+                       : BN == 128 ? tc::sk_fixup_kernel<128, 256>
+                                   : tc::sk_fixup_kernel<64, 256>)
+                    : (BN == 256   ? tc::sk_fixup_kernel<256, 128>
+                       : BN == 128 ? tc::sk_fixup_kernel<128, 128>
+                                   : tc::sk_fixup_kernel<64, 128>);
+    launch_dependent(fix, fgrid, dim3(256), 0, s, p);
     return last_status();
 }
 
