@@ -127,11 +127,14 @@ def test_plan_auto_path_choice(lib):
     # odd leading dimensions do not matter to the tensor-core path (pre-pass)
     st, p = sg.sgemm_plan("T", "T", 4095, 3073, 1537, 4095, 1537, 3073)
     assert st == 0 and p["path"] == sg.PATH_3XTF32
-    # small problems and short K stay on the CUDA cores
-    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256)
-    assert st == 0 and p["path"] == sg.PATH_FFMA
-    st, p = sg.sgemm_plan("N", "N", 8192, 8192, 16, 16, 8192, 8192)
-    assert st == 0 and p["path"] == sg.PATH_FFMA
+    # small problems too, as long as K >= 32
+    for shp in [(256, 256, 256), (128, 128, 128), (17, 17, 32), (128, 128, 2048)]:
+        st, p = sg.sgemm_plan("N", "N", *shp, shp[2], shp[1], shp[1])
+        assert st == 0 and p["path"] == sg.PATH_3XTF32, shp
+    # short K stays on the CUDA cores
+    for shp in [(8192, 8192, 16), (256, 256, 31), (17, 17, 1)]:
+        st, p = sg.sgemm_plan("N", "N", *shp, shp[2], shp[1], shp[1])
+        assert st == 0 and p["path"] == sg.PATH_FFMA, shp
     # TF32 is never chosen automatically
     for shp in [(4096, 4096, 4096), (1024, 1024, 1024), (300, 300, 40)]:
         st, p = sg.sgemm_plan("N", "N", *shp, shp[2], shp[1], shp[1])
@@ -224,17 +227,18 @@ def test_plan_ffma_stream_k_tail(lib):
 
 
 def test_plan_split_k_for_small_grids(lib):
+    F = sg.PATH_FFMA
     # 256^3: 4 tiles for 304 CTA slots -> the K loop is split
-    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152)
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152, path=F)
     assert st == 0 and p["split"] > 1
     # 16384 x 64 x 8192 skinny on the FFMA path: 128 tiles, long K -> split
     st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152,
                           path=sg.PATH_FFMA)
     assert st == 0 and p["split"] > 1
     # forced split is honoured, forced 1 disables it
-    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=1)
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=1, path=F)
     assert p["split"] == 1
-    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=3)
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, split=3, path=F)
     assert p["split"] == 3
 
 
