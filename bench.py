@@ -366,6 +366,7 @@ def gpu_arm(args):
     # the library records its main kernel's launches on the same stream
     sg.sgemm_timing_enable(args.steps)
     barrier()
+    launches0 = sg.sgemm_launch_count()
     t_wall = time.perf_counter()
     t_begin = t_wall
     for i in range(args.steps):
@@ -375,6 +376,7 @@ def gpu_arm(args):
         ends[i].record(stream)
     barrier()
     t_end = time.perf_counter()
+    launches = sg.sgemm_launch_count() - launches0
     t_wall = t_end - t_wall
     time.sleep(0.05)                # the last in-region sample reaches the reader
     sampler.stop()
@@ -390,16 +392,6 @@ def gpu_arm(args):
     # ---- plan of the timed call: which kernels ran
     st, plan = sg.sgemm_plan(w.transA, w.transB, w.M, w.N, w.K, lda, ldb, ldc, True, True, True,
                              sg.PATH_AUTO, 0, sms)
-    # our kernels per timed call: FFMA (+ fixup when tiles are shared); tensor
-    # cores: the main kernel + one split pre-pass launch unless both operands
-    # are split in it (A in the kernel when N <= 2048 and A is K-contiguous,
-    # B when M <= 2048 and B is K-contiguous; see the selector)
-    if plan["path"] == sg.PATH_FFMA:
-        launches_per_step = 1 + (1 if plan["split"] > 1 else 0)
-    else:
-        fuse_a = w.N <= 2048 and w.transA.upper() == "N"
-        fuse_b = w.M <= 2048 and w.transB.upper() == "T"
-        launches_per_step = 1 + (0 if (fuse_a and fuse_b) else 1)
 
     # ---- per-path timings on the same workload (outside the timed region)
     peaks, peak_src = measured_peaks()
@@ -545,7 +537,7 @@ def gpu_arm(args):
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"], "samples": clocks["samples"]},
             "plan": plan, "paths": paths, "workloads": workloads, "ffma_peak_tflops": ffma_peak,

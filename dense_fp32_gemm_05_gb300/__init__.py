@@ -19,7 +19,7 @@ __all__ = [
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
     "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
-    "sgemm_timing_read", "gemm", "exported_symbols",
+    "sgemm_timing_read", "sgemm_launch_count", "gemm", "exported_symbols",
 ]
 
 SGEMM_OK = 0
@@ -85,6 +85,8 @@ def _declare(lib):
     lib.sgemm_timing_enable.restype = i32
     lib.sgemm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i32]
     lib.sgemm_timing_read.restype = i32
+    lib.sgemm_launch_count.argtypes = []
+    lib.sgemm_launch_count.restype = i64
     lib.sgemm_ffma_static_scratch.argtypes = gemm_args + [i32]
     lib.sgemm_ffma_static_scratch.restype = i32
 
@@ -109,7 +111,8 @@ def exported_symbols(lib=None):
     """Names of the entry points this binding declares, for export checks."""
     return ["sgemm", "sgemm_ex", "sgemm_epilogue", "sgemm_host", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
             "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
-            "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read"]
+            "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read",
+            "sgemm_launch_count"]
 
 
 def _b(t: str) -> bytes:
@@ -187,6 +190,11 @@ def sgemm_version() -> int:
 def sgemm_timing_enable(n: int) -> int:
     """Record event pairs around the main kernel of the next n launches."""
     return load().sgemm_timing_enable(n)
+
+
+def sgemm_launch_count() -> int:
+    """Kernels the library has launched in this process (all paths)."""
+    return int(load().sgemm_launch_count())
 
 
 def sgemm_timing_read(capacity: int = 4096):

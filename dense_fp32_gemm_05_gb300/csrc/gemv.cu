@@ -448,6 +448,7 @@ namespace {
 template <int SM, int PB, bool VEC>
 void launch_dot(const gemv::Params &p, cudaStream_t s) {
     const int rows_per_cta = gemv::WARPS * PB;
+    count_launch();
     gemv::gemv_dot_kernel<SM, PB, VEC><<<(p.P + rows_per_cta - 1) / rows_per_cta, gemv::THREADS, 0, s>>>(p);
 }
 
@@ -477,6 +478,7 @@ int launch_axpy(const gemv::Params &p, cudaStream_t s) {
         return SGEMM_ERR_CUDA;
     }
     dim3 grid((p.P + gemv::AX_P - 1) / gemv::AX_P, p.ksplit);
+    count_launch();
     kern<<<grid, gemv::THREADS, smem, s>>>(p);
     return SGEMM_OK;
 }
@@ -544,6 +546,7 @@ bool launch_axpy_tma(const gemv::Params &p, cudaStream_t s, int *status) {
         __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
     }
     dim3 grid((p.P + gemv::AX_P - 1) / gemv::AX_P, p.ksplit);
+    count_launch();
     kern<<<grid, gemv::TX_THREADS, smem, s>>>(map, p);
     *status = SGEMM_OK;
     return true;

@@ -59,6 +59,9 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Counts one kernel launch of the library (sgemm_launch_count reads the total).
+void count_launch();
+
 // kern<<<grid, block, smem, s>>>(args...) with programmatic stream
 // serialization: only the library's own second and third kernels of one call
 // are launched this way, each of which starts with pdl_wait().
@@ -75,6 +78,7 @@ static inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, di
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    count_launch();
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <map>
@@ -91,6 +92,10 @@ struct TimingRing {
 };
 static TimingRing g_timing;
 
+// Kernel launches made by the library in this process (every path).
+static std::atomic<long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 void timing_mark(cudaStream_t s, bool begin) {
     std::lock_guard<std::mutex> lk(g_mu);
     TimingRing &t = g_timing;
@@ -124,6 +129,7 @@ static int grid_for(int64_t total, int sms) {
 // ------------------------------------------------------------ FFMA launch
 template <bool AK, bool BK_, bool V>
 static void launch_ffma_t(const ffma::Params &p, int grid, cudaStream_t s) {
+    count_launch();
     ffma::ffma_gemm_kernel<AK, BK_, V><<<grid, ffma::THREADS, 0, s>>>(p);
 }
 
@@ -219,6 +225,7 @@ int gemm_impl(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
 
     if (K == 0 || alpha == 0.0f) {
         if (beta == 1.0f && !epi.bias && epi.act == SGEMM_ACT_NONE) return SGEMM_OK;
+        count_launch();
         ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc,
                                                                      epi.bias, epi.act);
         return launch_status();
@@ -340,6 +347,10 @@ extern "C" int sgemm_set_wait_limit(uint64_t nanoseconds) {
     return SGEMM_OK;
 }
 
+extern "C" int64_t sgemm_launch_count(void) {
+    return g_launches.load(std::memory_order_relaxed);
+}
+
 extern "C" int sgemm_timing_enable(int n) {
     if (n < 0 || n > 100000) return -1;
     int dev = 0;
@@ -452,6 +463,7 @@ extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, in
     if (!(d->cc_major == 10 && d->cc_minor == 3)) return SGEMM_ERR_UNSUPPORTED;
     if (K == 0 || alpha == 0.0f) {
         if (beta == 1.0f) return SGEMM_OK;
+        count_launch();
         ffma::scale_c_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>((int)M, (int)N, beta, C, ldc,
                                                                      nullptr, SGEMM_ACT_NONE);
         return launch_status();

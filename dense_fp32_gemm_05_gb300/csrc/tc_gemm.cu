@@ -1180,6 +1180,7 @@ static void launch_split_pair(bool three, const tc::SplitJob &a, const tc::Split
                               cudaStream_t s) {
     const int blocks = a.blocks + b.blocks;
     if (blocks == 0) return;
+    count_launch();
     if (three) tc::split_pair_kernel<true><<<blocks, 256, 0, s>>>(a, b);
     else tc::split_pair_kernel<false><<<blocks, 256, 0, s>>>(a, b);
 }
@@ -1219,11 +1220,13 @@ static int launch_main(const CUtensorMap *maps, const tc::Params &p, int grid, c
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = dep ? 2 : 1;
+        count_launch();
         cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     } else if (dep) {
         launch_dependent(kern, dim3(grid), dim3(tc::THREADS), K_::SMEM, s, maps[0], maps[1],
                          maps[2], maps[3], maps[4], maps[5], p);
     } else {
+        count_launch();
         kern<<<grid, tc::THREADS, K_::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                    maps[5], p);
     }

@@ -240,13 +240,22 @@ int sgemm_set_wait_limit(uint64_t nanoseconds);
 int sgemm_timing_enable(int n);
 int sgemm_timing_read(float *ms, int capacity);
 
+/*
+ * sgemm_launch_count - the number of GPU kernels this library has launched in
+ * this process, on every device and path: split pre-passes, main kernels,
+ * stream-K and K-split reductions, and the C = beta*C quick return.  A
+ * measurement hook: the difference of two readings counts the launches in
+ * between.  Never fails.
+ */
+int64_t sgemm_launch_count(void);
+
 /* Free the current device's workspace (synchronises the device). */
 int sgemm_release_workspace(void);
 
 /*
  * sgemm_ffma_static_scratch - the FFMA path (SGEMM_PATH_FFMA) for callers
- * that cannot allocate device memory.  The paper has no counterpart: this
- * entry point exists only for the library's users.
+ * that cannot allocate device memory.  The GEMM write-ups this library
+ * follows have no counterpart: this entry point exists only for its users.
  *
  * Who needs it: code that runs where cudaMalloc/cudaMallocAsync must not be
  * called - a host framework that owns the whole device memory pool and
