@@ -157,6 +157,42 @@ constexpr int AX_U = 8;                // consecutive k per warp step (row loads
 template <int SM>
 constexpr int ax_smem_floats() { return WARPS * SM * AX_P + AX_KC * SM; }
 
+// Small(s, kc .. kc+kn-1) -> smt[k][s] by NT threads (this one is tid),
+// reading along Small's contiguous dimension.  Element t = tid + j NT, j <
+// PER, sits at (slow, fast) = (t / major, t % major); both advance by NT
+// with one carry.  Every load is issued before the first store: a chunk
+// costs one L2 round trip, not one per element of the thread.
+template <int SM, int NT, int PER>
+__device__ __forceinline__ void stage_small(const Params &p, float *smt, int kc, int kn,
+                                            int tid) {
+    const bool s_fast = p.small_ss == 1;               // Small's stored rows run along s
+    const int major = s_fast ? SM : kn;
+    const int dq = NT / major, dr = NT % major;
+    const int total = kn * SM;
+    float v[PER];
+    int q = tid / major, r = tid % major;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int s = s_fast ? r : q, kk = s_fast ? q : r;
+        v[j] = (tid + j * NT < total && s < p.S)
+                   ? __ldg(p.small + (int64_t)s * p.small_ss + (int64_t)(kc + kk) * p.small_sk)
+                   : 0.0f;
+        q += dq;
+        r += dr;
+        if (r >= major) { r -= major; ++q; }
+    }
+    q = tid / major;
+    r = tid % major;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int s = s_fast ? r : q, kk = s_fast ? q : r;
+        if (tid + j * NT < total) smt[kk * SM + s] = v[j];
+        q += dq;
+        r += dr;
+        if (r >= major) { r -= major; ++q; }
+    }
+}
+
 template <int SM, bool VEC>
 __global__ void __launch_bounds__(THREADS, 2) gemv_axpy_kernel(const Params p) {
     pdl_trigger();   // the K-split sum may launch; it waits for this grid
@@ -174,19 +210,12 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_axpy_kernel(const Params p) {
 #pragma unroll
     for (int s = 0; s < SM; ++s) acc[s][0] = acc[s][1] = make_float2(0.0f, 0.0f);
     const bool whole = VEC && pc + 3 < p.P;
-    const bool s_fast = p.small_ss == 1;               // Small's stored rows run along s
     constexpr int U = AX_U;
     for (int kc = k0; kc < k1; kc += AX_KC) {
         const int kn = min(AX_KC, k1 - kc);
         __syncthreads();                               // the previous chunk is consumed
-        // Small(s, kc .. kc+kn) -> smt[k][s], reading along its contiguous dimension
-        for (int i = threadIdx.x; i < kn * SM; i += THREADS) {
-            const int s = s_fast ? i % SM : i / kn;
-            const int kk = s_fast ? i / SM : i % kn;
-            smt[kk * SM + s] = s < p.S ? __ldg(p.small + (int64_t)s * p.small_ss +
-                                               (int64_t)(kc + kk) * p.small_sk)
-                                       : 0.0f;
-        }
+        stage_small<SM, THREADS, (AX_KC * SM + THREADS - 1) / THREADS>(p, smt, kc, kn,
+                                                                      threadIdx.x);
         __syncthreads();
         // warp w takes U consecutive k at a time (k = kc + (w + 8 i) U ..):
         // all U row loads are issued before the first FMA
@@ -287,8 +316,25 @@ __device__ __forceinline__ bool tx_try(uint32_t bar, uint32_t ph) {
                  "selp.u32 %0, 1, 0, q;\n\t}" : "=r"(ok) : "r"(bar), "r"(ph) : "memory");
     return ok != 0;
 }
+// The same with the suspension bounded by `ns` nanoseconds instead of the
+// hardware's own window.
+__device__ __forceinline__ bool tx_try_for(uint32_t bar, uint32_t ph, uint32_t ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}" : "=r"(ok) : "r"(bar), "r"(ph), "r"(ns) : "memory");
+    return ok != 0;
+}
 // Bounded wait; on expiry the device error word is raised and false returned.
+// A limit below 100 us (only the test hook sets one) is one try_wait whose
+// suspension it bounds: %globaltimer does not tick every nanosecond, and
+// try_wait on its own suspends a thread for a hardware-chosen while, so such
+// a limit could otherwise outlast a wait of a microsecond or two.
 __device__ __forceinline__ bool tx_wait(uint32_t bar, uint32_t ph, uint64_t limit_ns) {
+    if (limit_ns < 100000u) {
+        if (tx_try_for(bar, ph, (uint32_t)limit_ns)) return true;
+        atomicExch(&g_error, (unsigned)SGEMM_ERR_TIMEOUT);
+        return false;
+    }
     if (tx_try(bar, ph)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!tx_try(bar, ph)) {
@@ -361,7 +407,6 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     float2 acc[SM][2];
 #pragma unroll
     for (int s = 0; s < SM; ++s) acc[s][0] = acc[s][1] = make_float2(0.0f, 0.0f);
-    const bool s_fast = p.small_ss == 1;
     // A failed wait stops the compute and the empty-slot arrivals (the
     // producer then times out too), but never a barrier: every consumer
     // thread runs the same sequence of named-barrier syncs.
@@ -370,13 +415,7 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     for (int kc = k0; kc < k1; kc += TX_KC) {
         const int kn = min(TX_KC, k1 - kc);
         asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");   // previous chunk consumed
-        for (int t = threadIdx.x; t < kn * SM; t += TX_CT) {
-            const int s = s_fast ? t % SM : t / kn;
-            const int kk = s_fast ? t / SM : t % kn;
-            smt[kk * SM + s] = s < p.S ? __ldg(p.small + (int64_t)s * p.small_ss +
-                                               (int64_t)(kc + kk) * p.small_sk)
-                                       : 0.0f;
-        }
+        stage_small<SM, TX_CT, (TX_KC * SM + TX_CT - 1) / TX_CT>(p, smt, kc, kn, threadIdx.x);
         asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
         // the stages of this chunk (TX_KC is a multiple of TX_KS)
         for (; i < nst && k0 + i * TX_KS < kc + kn; ++i) {

@@ -223,6 +223,9 @@ int sgemm_device_error(sgemm_stream_t stream);
  * operand through shared memory, in nanoseconds of %globaltimer (0 restores
  * the default of 2 s).  A test hook: a tiny limit makes a wait run out on
  * purpose so that the timeout path can be checked without hanging anything.
+ * In the staged thin-problem kernel a limit below 100 us bounds a single
+ * mbarrier try_wait's suspension instead, so that a wait not complete within
+ * it runs out whatever the timer's resolution.
  */
 int sgemm_set_wait_limit(uint64_t nanoseconds);
 
