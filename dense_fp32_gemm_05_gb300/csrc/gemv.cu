@@ -99,8 +99,15 @@ __global__ void __launch_bounds__(THREADS) gemv_dot_kernel(const Params p) {
     for (int b = 0; b < PB; ++b)
         rows[b] = p.big + (int64_t)min(p0 + b, p.P - 1) * p.big_ld;   // clamped: a row past P is read, never stored
     int k = lane * 4;
+    // k-steps unrolled (their row loads issued together).  Measured on GB300,
+    // S x 16384 x 8192 NT, unrolled 2 -> this: S = 4 208 -> 124 us and S = 8
+    // 563 -> 282 us with 8; S = 16 438 -> 414 us with 4 (8 spills there,
+    // 676 us); S <= 2 unchanged at 2.  Two rows per warp instead of four for
+    // S > 8 was slower still (1888 us): each warp then reads Small twice as
+    // often per byte of Big.
+    constexpr int DOT_UNROLL = SM >= 16 ? 4 : SM >= 4 ? 8 : 2;
     if (VEC) {
-#pragma unroll 2
+#pragma unroll DOT_UNROLL
         for (; k + 3 < p.K; k += 128) {
             float4 bv[PB];
 #pragma unroll
