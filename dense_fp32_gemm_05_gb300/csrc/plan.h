@@ -64,8 +64,16 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
     Plan pl;
     // Thin problems (min(M, N) <= 16, "Matmul II", section 8: decode's
     // M = 1 to a few dozen) stream their large operand once on the CUDA
-    // cores; the tile paths would compute mostly padding.
-    if (path == SGEMM_PATH_GEMV || (path == SGEMM_PATH_AUTO && std::min(M, N) <= 16)) {
+    // cores; the tile paths would compute mostly padding.  Except when the
+    // large operand's rows run along K (the dot form: weights stored [N][K])
+    // and more than 4 outputs share each of its elements: there the
+    // tensor-core path, which splits both operands inside its kernel, is
+    // ahead despite the padding (measured on GB300, S x 16384 x 8192 NT:
+    // S = 8 279 -> 165 us, S = 16 418 -> 166 us; S = 4 stays at 124 us).
+    const int64_t thin = std::min(M, N);
+    const bool big_kcontig = M <= N ? !is_notrans(tb) : is_notrans(ta);
+    const bool thin_on_tc = thin > 4 && big_kcontig && K >= 32;
+    if (path == SGEMM_PATH_GEMV || (path == SGEMM_PATH_AUTO && thin <= 16 && !thin_on_tc)) {
         if (std::min(M, N) > 16) return SGEMM_ERR_UNSUPPORTED;
         pl.path = SGEMM_PATH_GEMV;
         pl.tile_m = (int)std::min(M, N);

@@ -244,10 +244,25 @@ def test_plan_split_k_for_small_grids(lib):
 
 def test_plan_thin_problems_take_the_gemv_path(lib):
     # min(M, N) <= 16 ("Matmul II", section 8: decode's M = 1 to a few dozen)
-    for (M, N, K) in [(1, 16384, 8192), (16, 4096, 4096), (16384, 8, 8192), (5, 5, 5)]:
-        st, p = sg.sgemm_plan("N", "T", M, N, K, K, K, N)
-        assert st == 0 and p["path"] == sg.PATH_GEMV, (M, N, K)
+    for (ta, tb, M, N, K) in [("N", "T", 1, 16384, 8192), ("N", "T", 4, 4096, 4096),
+                              ("N", "N", 16, 4096, 4096), ("T", "N", 16384, 8, 8192),
+                              ("N", "T", 5, 5, 5), ("N", "T", 16, 4096, 16)]:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, p = sg.sgemm_plan(ta, tb, M, N, K, lda, ldb, N)
+        assert st == 0 and p["path"] == sg.PATH_GEMV, (ta, tb, M, N, K)
         assert p["tile_m"] == min(M, N)
+    # large operand K-contiguous (weights stored [N][K]) and S > 4: the
+    # tensor cores are ahead there
+    for (ta, tb, M, N, K) in [("N", "T", 16, 16384, 8192), ("N", "T", 8, 4096, 4096),
+                              ("N", "N", 16384, 8, 8192), ("N", "T", 5, 4096, 32)]:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, p = sg.sgemm_plan(ta, tb, M, N, K, lda, ldb, N)
+        assert st == 0 and p["path"] == sg.PATH_3XTF32, (ta, tb, M, N, K)
+    # forced, the thin path still takes them
+    st, p = sg.sgemm_plan("N", "T", 16, 16384, 8192, 8192, 8192, 16384, path=sg.PATH_GEMV)
+    assert st == 0 and p["path"] == sg.PATH_GEMV
     # 17 and up: the tile paths
     st, p = sg.sgemm_plan("N", "N", 17, 4096, 4096, 4096, 4096, 4096)
     assert st == 0 and p["path"] != sg.PATH_GEMV

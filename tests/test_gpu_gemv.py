@@ -91,8 +91,9 @@ def test_gemv_random_within_bound(oracle_mod, t, S, P, K, ta, tb, thin):
 
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_gemv_is_the_selectors_choice(ta, tb):
-    # min(M, N) <= 16: sgemm() (AUTO) runs this path, bit for bit
-    M, N, K = 8, 3000, 777
+    # min(M, N) <= 4: sgemm() (AUTO) runs this path in every layout, bit for
+    # bit (from 5 up, a K-contiguous large operand goes to the tensor cores)
+    M, N, K = 4, 3000, 777
     A = stored(gi.random_matrix(31, M, K), ta)
     B = stored(gi.random_matrix(32, K, N), tb)
     st1, out1 = gh.run(ta, tb, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, None, N,
