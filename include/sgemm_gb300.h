@@ -96,8 +96,11 @@ typedef enum {
                               FMAs streaming the large operand once, no tiles
                               ("Matmul II", section 8: dedicated GEMV kernels
                               for decode's M = 1 to a few dozen).  AUTO takes
-                              it whenever min(M, N) <= 16; forced on a larger
-                              problem it returns SGEMM_ERR_UNSUPPORTED.       */
+                              it whenever min(M, N) <= 16, except with K >= 32,
+                              min(M, N) > 4 and the large operand's rows along
+                              K (weights stored [N][K]): those go to 3xTF32.
+                              Forced on a larger problem it returns
+                              SGEMM_ERR_UNSUPPORTED.                          */
 } sgemm_path;
 
 /*
