@@ -70,9 +70,13 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
     // tensor-core path, which splits both operands inside its kernel, is
     // ahead despite the padding (measured on GB300, S x 16384 x 8192 NT:
     // S = 8 279 -> 165 us, S = 16 418 -> 166 us; S = 4 stays at 124 us).
+    // The large operand must also allow the in-kernel split (16-byte base,
+    // leading dimension a multiple of 4); otherwise the pre-pass would copy it
+    // twice over and the thin path stays ahead.
     const int64_t thin = std::min(M, N);
     const bool big_kcontig = M <= N ? !is_notrans(tb) : is_notrans(ta);
-    const bool thin_on_tc = thin > 4 && big_kcontig && K >= 32;
+    const bool big_al = M <= N ? (b_al && ldb % 4 == 0) : (a_al && lda % 4 == 0);
+    const bool thin_on_tc = thin > 4 && big_kcontig && big_al && K >= 32;
     if (path == SGEMM_PATH_GEMV || (path == SGEMM_PATH_AUTO && thin <= 16 && !thin_on_tc)) {
         if (std::min(M, N) > 16) return SGEMM_ERR_UNSUPPORTED;
         pl.path = SGEMM_PATH_GEMV;

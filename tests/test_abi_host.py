@@ -263,6 +263,11 @@ def test_plan_thin_problems_take_the_gemv_path(lib):
     # forced, the thin path still takes them
     st, p = sg.sgemm_plan("N", "T", 16, 16384, 8192, 8192, 8192, 16384, path=sg.PATH_GEMV)
     assert st == 0 and p["path"] == sg.PATH_GEMV
+    # a large operand the tensor-core kernel cannot split itself stays thin
+    st, p = sg.sgemm_plan("N", "T", 16, 16384, 8191, 8191, 8191, 16384)
+    assert st == 0 and p["path"] == sg.PATH_GEMV
+    st, p = sg.sgemm_plan("N", "T", 16, 16384, 8192, 8192, 8192, 16384, True, False, True)
+    assert st == 0 and p["path"] == sg.PATH_GEMV
     # 17 and up: the tile paths
     st, p = sg.sgemm_plan("N", "N", 17, 4096, 4096, 4096, 4096, 4096)
     assert st == 0 and p["path"] != sg.PATH_GEMV
