@@ -73,7 +73,9 @@ typedef enum {
 } sgemm_activation;
 
 /* Arithmetic path.  AUTO lets the per-shape selector choose among the
-   fp32-accurate paths (FFMA and 3xTF32); TF32 is never chosen by AUTO. */
+   fp32-accurate paths: GEMV for min(M, N) <= 16 (see below for the one
+   exception), else 3xTF32 for K >= 32 and FFMA for K < 32.  TF32 is never
+   chosen by AUTO. */
 typedef enum {
     SGEMM_PATH_AUTO = 0,
     SGEMM_PATH_FFMA = 1,   /* CUDA-core fp32 FMA, 128x128 block tiles, 8x16
