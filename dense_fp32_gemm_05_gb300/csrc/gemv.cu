@@ -30,6 +30,10 @@
 //     ring with TMA instead (gemv_axpy_tma_kernel).
 // Every sum is a fixed order of fp32 FMAs and adds: deterministic, and, as
 // any summation order, inside the 4 K 2^-24 bound.
+//
+// The selector sends dot-form problems with S > 4 and K >= 32 (and a Big
+// the tensor-core kernel can split itself) to the 3xTF32 path, which is
+// faster there despite its padded tiles; forced, this path still runs them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
