@@ -16,7 +16,7 @@ __all__ = [
     "SGEMM_OK", "SGEMM_ERR_CUDA", "SGEMM_ERR_TIMEOUT", "SGEMM_ERR_NOMEM",
     "SGEMM_ERR_UNSUPPORTED", "SGEMM_ERR_ARG", "SGEMM_ERR_SCRATCH", "PATH_AUTO", "PATH_FFMA",
     "PATH_3XTF32", "PATH_TF32", "PATH_GEMV", "ACT_NONE", "ACT_RELU", "sgemm_epilogue", "SgemmError", "library_path", "load",
-    "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_status_string",
+    "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_plan_detail", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
     "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
     "sgemm_timing_read", "sgemm_launch_count", "gemm", "exported_symbols",
@@ -52,6 +52,13 @@ class SgemmError(RuntimeError):
         super().__init__(f"{where}: status {status} ({sgemm_status_string(status)})")
 
 
+class PlanInfo(ctypes.Structure):
+    """sgemm_plan_info of the C header, field for field."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "path", "tile_m", "tile_n", "vector", "ctas", "split", "dp_tiles", "pair", "fuse_a",
+        "fuse_b", "wide", "accumulators", "k_block", "tail_nsplit", "sk_ctas", "sk_tail")]
+
+
 def library_path() -> str:
     return os.path.join(_HERE, _LIB_NAME)
 
@@ -71,6 +78,9 @@ def _declare(lib):
     lib.sgemm_plan.argtypes = [c, c, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, i32, i32,
                                ip, ip, ip, ip, ip, ip]
     lib.sgemm_plan.restype = i32
+    lib.sgemm_plan_detail.argtypes = [c, c, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, i32,
+                                      i32, ctypes.POINTER(PlanInfo)]
+    lib.sgemm_plan_detail.restype = i32
     lib.sgemm_status_string.argtypes = [i32]
     lib.sgemm_status_string.restype = ctypes.c_char_p
     lib.sgemm_device_error.argtypes = [vp]
@@ -109,7 +119,8 @@ def load():
 
 def exported_symbols(lib=None):
     """Names of the entry points this binding declares, for export checks."""
-    return ["sgemm", "sgemm_ex", "sgemm_epilogue", "sgemm_host", "sgemm_plan", "sgemm_status_string", "sgemm_device_error",
+    return ["sgemm", "sgemm_ex", "sgemm_epilogue", "sgemm_host", "sgemm_plan", "sgemm_plan_detail",
+            "sgemm_status_string", "sgemm_device_error",
             "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
             "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read",
             "sgemm_launch_count"]
@@ -165,6 +176,17 @@ def sgemm_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned=True, b_aligned
                            *[ctypes.byref(o) for o in outs])
     keys = ("path", "split", "tile_m", "tile_n", "vector", "ctas")
     return st, {k: o.value for k, o in zip(keys, outs)}
+
+
+def sgemm_plan_detail(transA, transB, M, N, K, lda, ldb, ldc, a_aligned=True, b_aligned=True,
+                      c_aligned=True, path=PATH_AUTO, split=0, num_sms=152):
+    """The selector's decision down to the kernel variant, without a GPU:
+    (status, dict of sgemm_plan_info's fields)."""
+    info = PlanInfo()
+    st = load().sgemm_plan_detail(_b(transA), _b(transB), M, N, K, lda, ldb, ldc, int(a_aligned),
+                                  int(b_aligned), int(c_aligned), path, split, num_sms,
+                                  ctypes.byref(info))
+    return st, {name: getattr(info, name) for name, _ in PlanInfo._fields_}
 
 
 def sgemm_status_string(status: int) -> str:

@@ -266,4 +266,32 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
     return 0;
 }
 
+// The tensor-core kernel variant a plan runs (run_tc launches exactly this).
+struct TcVariant {
+    bool fuse_a = false;   // A split in the kernel (into tensor memory)
+    bool fuse_b = false;   // B split in the kernel (in shared memory)
+    bool sk = false;       // stream-K over every tile, single SMs
+    bool pair = false;     // 256-row tiles on SM pairs (cta_group::2)
+    bool sk_tail = false;  // the tiles after the last full wave shared by all CTAs
+    bool wide = false;     // 3xTF32 with 32-wide k-blocks, A_hi in TMEM and A_lo in shared memory
+    int nacc = 1;          // accumulators per tile, summed by the epilogue
+    int bk = 32;           // k-block width in floats
+};
+
+inline TcVariant tc_variant(const Plan &pl) {
+    TcVariant v;
+    const bool three = pl.path == SGEMM_PATH_3XTF32;
+    v.fuse_a = pl.fuse_a != 0;
+    v.fuse_b = pl.fuse_b != 0;
+    v.sk = pl.tc_sk > 0;
+    // the pair kernel takes pre-split operands only; stream-K over every
+    // tile runs on single SMs, stream-K over the last wave on either
+    v.pair = pl.pair != 0 && !v.fuse_a && !v.fuse_b && !v.sk;
+    v.sk_tail = !v.sk && pl.tc_sk_tail != 0 && !v.fuse_a && !v.fuse_b;
+    v.wide = three && pl.tile_n <= 128 && v.fuse_a && !v.pair;
+    v.nacc = (pl.tile_n == 64 && !v.pair) ? (three ? 3 : 2) : (v.wide ? 3 : 1);
+    v.bk = (v.wide || !three) ? 32 : 16;
+    return v;
+}
+
 }  // namespace sgemm_gb300

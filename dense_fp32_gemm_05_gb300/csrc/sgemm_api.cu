@@ -318,6 +318,38 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
     return SGEMM_OK;
 }
 
+extern "C" int sgemm_plan_detail(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldc, int a_aligned,
+                                 int b_aligned, int c_aligned, int path, int split, int num_sms,
+                                 sgemm_plan_info *out) {
+    if (out == nullptr) return -15;
+    sgemm_plan_info info{};
+    int st = sgemm_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned, b_aligned, c_aligned,
+                        path, split, num_sms, &info.path, &info.split, &info.tile_m,
+                        &info.tile_n, &info.vector, &info.ctas);
+    if (st != SGEMM_OK) return st;
+    Plan pl;
+    make_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned != 0, b_aligned != 0,
+              c_aligned != 0, path, split, num_sms, &pl);
+    info.dp_tiles = pl.path == SGEMM_PATH_GEMV ? 0 : pl.dp_tiles;
+    if (pl.path == SGEMM_PATH_3XTF32 || pl.path == SGEMM_PATH_TF32) {
+        const TcVariant v = tc_variant(pl);
+        info.pair = v.pair;
+        info.fuse_a = v.fuse_a;
+        info.fuse_b = v.fuse_b;
+        info.wide = v.wide;
+        info.accumulators = v.nacc;
+        info.k_block = v.bk;
+        info.tail_nsplit = (v.sk || v.sk_tail) ? 1 : pl.tail_nsplit;
+        info.sk_ctas = v.sk ? pl.tc_sk : 0;
+        info.sk_tail = v.sk_tail;
+    } else if (pl.path == SGEMM_PATH_FFMA) {
+        info.k_block = ffma::BK;
+    }
+    *out = info;
+    return SGEMM_OK;
+}
+
 extern "C" const char *sgemm_status_string(int status) {
     if (status < 0) return "invalid argument (the negated value is its 1-based position)";
     switch (status) {
@@ -420,7 +452,7 @@ constexpr size_t kStaticPartialFloats =
 
 // Every GPU that loads the library holds this array until the process exits.
 // It holds 2 slots per CTA of the stream-K decomposition (a CTA's first and
-// last partial tile), so plans with up to 128 CTAs fit.
+// last partial tile), so plans with up to 128 sharing CTAs fit.
 static __device__ __align__(256) float g_static_partials[kStaticPartialFloats];
 
 // Device address of g_static_partials per device, looked up once with that
@@ -476,11 +508,10 @@ extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, in
     bool partials = ffma_has_partials(p);
     if (partials && 2LL * p.sk_ctas > kStaticPartialTiles) {
         if (split != 0) return SGEMM_ERR_SCRATCH;    // the caller's split does not fit
-        // the selector's choice does not fit: every tile whole needs no scratch
-        p.dp_tiles = p.tiles_m * p.tiles_n;
-        p.sk_ctas = 0;
-        p.sk_iters = 0;
-        partials = false;
+        // the selector's stream-K share does not fit: the same iterations
+        // shared by as many CTAs as the array holds slots for
+        p.sk_ctas = kStaticPartialTiles / 2;
+        partials = ffma_has_partials(p);
     }
     if (partials) {
         st = static_partials(&p.partial);

@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -129,6 +130,14 @@ struct Cfg {
 // this way (sk_tile0 = 0, single SMs), or the CTAs first compute the first
 // dp_units tiles whole, one wave after another, and share only the rest: the
 // last, partly filled wave.
+// The caller's operands as given (for the fp32 redo of NaN sums).
+struct RawOps {
+    const float *A, *B;
+    int64_t lda, ldb;
+    int ta_n, tb_n;             // transA / transB is 'N'
+    int K;
+};
+
 struct Params {
     float *C;
     int64_t ldc;
@@ -149,6 +158,8 @@ struct Params {
     int sk_tile0;               // stream-K: first shared tile
     long long sk_iters;         // stream-K: shared tiles * num_kb
     float *partial;             // stream-K: 2 * sk_ctas tiles of TM x BN floats
+    RawOps raw;                 // the caller's A and B
+    unsigned long long gen;     // this call's stamp (see g_inf_gen)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -369,28 +380,93 @@ __device__ __forceinline__ float tf32_round(float x) {
     return __uint_as_float(r);
 }
 
+__device__ __forceinline__ float f32_inf() { return __uint_as_float(0x7f800000u); }
+
+// The two parts of one operand value x = hi + lo (+ a residual of about
+// 2^-22 |x|), both TF32.  hi = rna_tf32(x), except where that rounding
+// overflows a finite x (|x| >= (2 - 2^-11) 2^127): there hi is x with its low
+// 13 bits cleared, so no finite input becomes infinite.  lo = rna_tf32(x - hi)
+// (x - hi is exact in fp32) when hi is finite; an infinite or NaN x is
+// carried by hi alone (lo = 0, not inf - inf).  `inf` is raised when x is
+// infinite.
+__device__ __forceinline__ float split_hi(float x, bool &inf) {
+    float h = tf32_round(x);
+    if (fabsf(h) == f32_inf()) {
+        inf |= fabsf(x) == f32_inf();
+        h = __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+    }
+    return h;
+}
+
+__device__ __forceinline__ float split_lo(float x, float h) {
+    const float l = tf32_round(__fsub_rn(x, h));
+    return fabsf(h) < f32_inf() ? l : 0.0f;
+}
+
+// Infinite operand values and the NaN they can cause.  A sum that meets an
+// infinite input is infinite or NaN in fp32 arithmetic; on the tensor cores
+// the cross terms hi*lo multiply an infinity by its partner's low part, which
+// may be zero or of the other sign, so an infinite sum can come out NaN.  A
+// call that meets an infinite operand value therefore redoes, in fp32 with
+// fused multiply-adds in ascending k (the naive loop), every output whose sum
+// came out NaN; that gives the IEEE result.  g_inf_gen holds the largest
+// call stamp (Params::gen, increasing per call) whose split met an infinity;
+// a call's kernels compare it with their own stamp, so the word never needs
+// clearing, and a later call's stamp can only cause a redundant redo.
+__device__ unsigned long long g_inf_gen;
+
+__device__ __forceinline__ void note_inf(unsigned long long gen) { atomicMax(&g_inf_gen, gen); }
+
+__device__ __forceinline__ bool inf_seen(unsigned long long gen) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&g_inf_gen) : "memory");
+    return v >= gen;
+}
+
+// sum_k op(A)(row, k) * op(B)(k, col) in fp32, fused multiply-adds in
+// ascending k from 0, straight from the caller's operands.
+__device__ __noinline__ float dot_fp32(const RawOps o, int row, int col) {
+    float acc = 0.0f;
+    for (int k = 0; k < o.K; ++k) {
+        const float a = o.ta_n ? o.A[(int64_t)row * o.lda + k] : o.A[(int64_t)k * o.lda + row];
+        const float b = o.tb_n ? o.B[(int64_t)k * o.ldb + col] : o.B[(int64_t)col * o.ldb + k];
+        acc = __fmaf_rn(a, b, acc);
+    }
+    return acc;
+}
+
+// Redoes the NaN sums of one row of 32 staged accumulator values (columns
+// col0..col0+31 of output row `row`).
+__device__ __noinline__ void redo_nan_row(float *vals, const RawOps o, int M, int N, int row,
+                                          int col0) {
+    if (row >= M) return;
+    for (int j = 0; j < 32 && col0 + j < N; ++j)
+        if (vals[j] != vals[j]) vals[j] = dot_fp32(o, row, col0 + j);
+}
+
 // In-place split of `n16` 16-byte groups of a shared tile: hi = round(x)
 // written over x, lo = round(x - hi) written to the twin tile (THREE only).
 // The WORKERS split threads stride through the tile together.
+// Returns whether an infinite value was met.
 template <bool THREE>
-__device__ __forceinline__ void split_tile(uint32_t hi, uint32_t lo, int n16, int ct) {
+__device__ __forceinline__ bool split_tile(uint32_t hi, uint32_t lo, int n16, int ct) {
+    bool inf = false;
     for (int i = ct; i < n16; i += WORKERS) {
         float4 v;
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(hi + 16u * i));
-        const float4 h = make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z),
-                                     tf32_round(v.w));
+        const float4 h = make_float4(split_hi(v.x, inf), split_hi(v.y, inf), split_hi(v.z, inf),
+                                     split_hi(v.w, inf));
         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                      :: "r"(hi + 16u * i), "f"(h.x), "f"(h.y), "f"(h.z), "f"(h.w) : "memory");
         if (THREE) {
-            const float4 l = make_float4(tf32_round(__fsub_rn(v.x, h.x)),
-                                         tf32_round(__fsub_rn(v.y, h.y)),
-                                         tf32_round(__fsub_rn(v.z, h.z)),
-                                         tf32_round(__fsub_rn(v.w, h.w)));
+            const float4 l = make_float4(split_lo(v.x, h.x), split_lo(v.y, h.y),
+                                         split_lo(v.z, h.z), split_lo(v.w, h.w));
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                          :: "r"(lo + 16u * i), "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w) : "memory");
         }
     }
+    return inf;
 }
 
 // Split of this thread's row of a raw A tile (TMA-swizzled, rows of BK
@@ -400,8 +476,9 @@ __device__ __forceinline__ void split_tile(uint32_t hi, uint32_t lo, int n16, in
 // index by bits 1-2 of the row, its 128-byte swizzle (BK_ = 32) by bits 0-2.
 // `taddr` is the warp's lane quarter and column tslot of tensor memory.
 template <bool THREE, int BK_>
-__device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, int q, int half,
+__device__ __forceinline__ bool split_a_to_tmem(uint32_t raw, uint32_t taddr, int q, int half,
                                                 int lane) {
+    bool inf = false;
     constexpr int KH = BK_ / 2;                       // k values per thread: 8 or 16
     const int r = q * 32 + lane;
     const uint32_t sw = BK_ == 16 ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
@@ -419,14 +496,15 @@ __device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, in
             const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                hi[4 * c + e] = tf32_round(x[e]);
-                if (THREE) lo[4 * c + e] = tf32_round(__fsub_rn(x[e], hi[4 * c + e]));
+                hi[4 * c + e] = split_hi(x[e], inf);
+                if (THREE) lo[4 * c + e] = split_lo(x[e], hi[4 * c + e]);
             }
         }
         const uint32_t col = (uint32_t)(half * KH + g * 8);
         tmem_st8(taddr + col, hi);
         if (THREE) tmem_st8(taddr + (uint32_t)BK_ + col, lo);
     }
+    return inf;
 }
 
 // WIDE tiles: this thread's row of the raw A tile (128-byte swizzle), split
@@ -434,8 +512,9 @@ __device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, in
 // k); lo = round(x - hi) is stored in the A_lo tile at x's own swizzled
 // position, the layout the shared-memory MMA reads.
 template <int BK_>
-__device__ __forceinline__ void split_a_hi_lo(uint32_t raw, uint32_t lo_tile, uint32_t taddr, int q,
+__device__ __forceinline__ bool split_a_hi_lo(uint32_t raw, uint32_t lo_tile, uint32_t taddr, int q,
                                               int half, int lane) {
+    bool inf = false;
     constexpr int KH = BK_ / 2;                       // k values per thread
     const int r = q * 32 + lane;
     const uint32_t sw = BK_ == 16 ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
@@ -454,14 +533,15 @@ __device__ __forceinline__ void split_a_hi_lo(uint32_t raw, uint32_t lo_tile, ui
             float lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                hi[4 * c + e] = tf32_round(x[e]);
-                lo[e] = tf32_round(__fsub_rn(x[e], hi[4 * c + e]));
+                hi[4 * c + e] = split_hi(x[e], inf);
+                lo[e] = split_lo(x[e], hi[4 * c + e]);
             }
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                          :: "r"(lo_tile + o), "f"(lo[0]), "f"(lo[1]), "f"(lo[2]), "f"(lo[3]) : "memory");
         }
         tmem_st8(taddr + (uint32_t)(half * KH + g * 8), hi);
     }
+    return inf;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -836,17 +916,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(full_bar(s), ph, lim)) { ok = false; break; }
+                    bool inf = false;
                     if (p.fuse_a) {
                         // A's hi and lo go to tensor memory, where the MMA reads
                         // them: no shared-memory traffic for A in the MMAs
                         const uint32_t slot = tmem + ((uint32_t)(q * 32) << 16) +
                                               (uint32_t)(K_::A_TMEM_COL + s * K_::A_SLOT_COLS);
-                        if (WIDE) split_a_hi_lo<BK>(a_hi(s), a_lo(s), slot, q, half, lane);
-                        else split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
+                        if (WIDE) inf = split_a_hi_lo<BK>(a_hi(s), a_lo(s), slot, q, half, lane);
+                        else inf = split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
                         tmem_st_wait();
                         tc_fence_before();
                     }
-                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s, b_rows), b_rows * BK * 4 / 16, ct);
+                    if (p.fuse_b)
+                        inf |= split_tile<THREE>(b_hi(s), b_lo(s, b_rows), b_rows * BK * 4 / 16, ct);
+                    // noted before this stage's split arrival, which orders the
+                    // note before the epilogue's read (below)
+                    if (inf) note_inf(p.gen);
                     if (p.fuse_b || (WIDE && p.fuse_a)) {
                         // generic-proxy stores must be visible to the tensor core's reads
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -860,6 +945,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool ready = mbar_wait(accf_bar(b), (uint32_t)(j / nbuf) & 1u, lim);
             tc_fence_after();
             if (!ready) break;
+            // A whole tile of a call that met an infinite operand value redoes
+            // its NaN sums in fp32 (see g_inf_gen; shared tiles are redone by
+            // the fixup).  Operands split by the pre-pass noted theirs before
+            // this grid started; this CTA's split warps noted theirs before
+            // arriving on a stage's split barrier, so waiting for the piece's
+            // last such barrier orders every note before the read.
+            bool redo = false;
+            if (pc.slot < 0) {
+                if (fused && g > 0) {
+                    const int64_t gl = g - 1;
+                    mbar_wait(conv_bar((int)(gl % K_::STAGES)), (uint32_t)(gl / K_::STAGES) & 1u,
+                              lim);
+                }
+                redo = inf_seen(p.gen);
+            }
             const float alpha = p.alpha, beta = p.beta;
             const int row0 = m0 + (int)rank * BM + q * 32;
             const int rows_here = min(32, p.M - row0);
@@ -889,6 +989,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = f[jj];
                 }
+                if (redo) redo_nan_row(stg + lane * EPI_LD, p.raw, p.M, p.N, row0 + lane, n0 + c * 32);
                 __syncwarp();
                 const int col = n0 + c * 32 + lane;
                 if (pc.slot >= 0) {
@@ -965,6 +1066,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int BN, int TM>
 __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
     pdl_wait();   // the main kernel's partial sums are complete and visible
+    const bool redo = inf_seen(p.gen);   // NaN sums redone in fp32 (see g_inf_gen)
     const long long T = p.sk_iters, G = p.sk_ctas;
     const int t = p.sk_tile0 + (int)blockIdx.x;
     const long long first = (long long)blockIdx.x * p.num_kb, last = first + p.num_kb - 1;
@@ -1001,7 +1103,11 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
                 v.w = __fadd_rn(v.w, x[u].w);
             }
         }
-        const float vs[4] = {v.x, v.y, v.z, v.w};
+        float vs[4] = {v.x, v.y, v.z, v.w};
+        if (redo) {
+            for (int q = 0; q < 4 && col + q < p.N; ++q)
+                if (vs[q] != vs[q]) vs[q] = dot_fp32(p.raw, row, col + q);
+        }
         float *dst = p.C + (int64_t)row * p.ldc + col;
         const float a_r = epi_alpha(p.alpha, p.row_scale, row);
 #pragma unroll
@@ -1015,15 +1121,9 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
 }
 
 // ---------------------------------------------------------------- split pre-pass
-__device__ __forceinline__ float rna_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
 // One operand of the split pre-pass: out[r][k] (r < rows, k < Kp, row stride
-// Kp) = op value at (r, k) for k < K, 0 for K <= k < Kp; hi = rna_tf32(x),
-// lo = rna_tf32(x - hi).  trans: the source is stored k-major
+// Kp) = op value at (r, k) for k < K, 0 for K <= k < Kp; hi and lo as
+// split_hi / split_lo.  trans: the source is stored k-major
 // (src[k*ld + r]), else src[r*ld + k]; vec: the source rows are 16-byte
 // aligned (base aligned, ld % 4 == 0).
 struct SplitJob {
@@ -1033,6 +1133,7 @@ struct SplitJob {
     float *hi, *lo;
     int trans, vec;
     int blocks;                 // CTAs of this job
+    unsigned long long gen;     // the call's stamp, noted when an infinity is met
 };
 
 __host__ __device__ inline int split_blocks(int rows, int Kp, bool trans) {
@@ -1043,12 +1144,15 @@ __host__ __device__ inline int split_blocks(int rows, int Kp, bool trans) {
 
 template <bool THREE>
 __device__ __forceinline__ void split_store4(const SplitJob &j, int64_t o, float4 x) {
-    const float4 h = make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
+    bool inf = false;
+    const float4 h = make_float4(split_hi(x.x, inf), split_hi(x.y, inf), split_hi(x.z, inf),
+                                 split_hi(x.w, inf));
     *reinterpret_cast<float4 *>(j.hi + o) = h;
     if (THREE)
         *reinterpret_cast<float4 *>(j.lo + o) =
-            make_float4(rna_tf32(__fsub_rn(x.x, h.x)), rna_tf32(__fsub_rn(x.y, h.y)),
-                        rna_tf32(__fsub_rn(x.z, h.z)), rna_tf32(__fsub_rn(x.w, h.w)));
+            make_float4(split_lo(x.x, h.x), split_lo(x.y, h.y), split_lo(x.z, h.z),
+                        split_lo(x.w, h.w));
+    if (inf) note_inf(j.gen);
 }
 
 // Both operands in one launch: CTAs [0, j0.blocks) do j0, the rest j1.
@@ -1143,6 +1247,8 @@ static bool make_map(CUtensorMap *m, const float *base, int rows, int Kp, int bo
 
 static std::mutex g_tc_mu;
 static uint64_t g_wait_ns = tc::kDefaultWaitNs;
+// Call stamps for tc::g_inf_gen: increasing, never 0 (the word's initial value).
+static std::atomic<unsigned long long> g_call_gen{0};
 
 void tc_set_wait_limit(uint64_t ns) {
     std::lock_guard<std::mutex> lk(g_tc_mu);
@@ -1268,14 +1374,14 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // An operand whose rows already run along K in memory, 16-byte aligned
     // with a leading dimension that is a multiple of 4, is read raw by TMA and
     // split in shared memory; any other goes through the split pre-pass into
-    // the canonical K-contiguous workspace layout.
-    const bool fuse_a = pl.fuse_a && is_notrans(ta) && aligned16(A) && lda % 4 == 0;
-    const bool fuse_b = pl.fuse_b && !is_notrans(tb) && aligned16(B) && ldb % 4 == 0;
-    // the pair kernel takes pre-split operands only; stream-K over every tile
-    // runs on single SMs, stream-K over the last wave on either
-    const bool sk = pl.tc_sk > 0;
-    const bool pair = pl.pair != 0 && !fuse_a && !fuse_b && !sk;
-    const bool sk_tail = !sk && pl.tc_sk_tail != 0 && !fuse_a && !fuse_b;
+    // the canonical K-contiguous workspace layout.  (The plan decided this
+    // from the same pointers; the checks here only guard the TMA rules.)
+    const TcVariant v = tc_variant(pl);
+    if ((v.fuse_a && !(is_notrans(ta) && aligned16(A) && lda % 4 == 0)) ||
+        (v.fuse_b && !(!is_notrans(tb) && aligned16(B) && ldb % 4 == 0)))
+        return SGEMM_ERR_UNSUPPORTED;
+    const bool fuse_a = v.fuse_a, fuse_b = v.fuse_b;
+    const bool sk = v.sk, pair = v.pair, sk_tail = v.sk_tail;
     const int TM = pair ? 2 * tc::BM : tc::BM;          // tile rows
     const int bdiv = pair ? 2 : 1;                      // B rows per CTA = tile columns / bdiv
     auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
@@ -1285,7 +1391,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // stream-K: the iterations of the shared tiles (at full width) and their
     // sharing -- every tile, or those after the last full wave
     const int64_t tiles_all = ((M + TM - 1) / TM) * ((N + BN - 1) / BN);
-    const int nkb_all = Kp / ((three && !(BN <= 128 && fuse_a)) ? tc::KBlock<true>::BK : 32);
+    const int nkb_all = Kp / v.bk;
     const int slots = pair ? std::max(sms / 2, 1) : std::max(sms, 1);
     const int64_t sk_tile0 = sk_tail ? std::min<int64_t>(pl.dp_tiles, tiles_all) : 0;
     const int64_t sk_tiles = (sk || sk_tail) ? tiles_all - sk_tile0 : 0;
@@ -1308,9 +1414,11 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // canonical K-major operands: A as [M][Kp], B as [N][Kp]
     const bool a_trans = !is_notrans(ta);   // A stored K x M
     const bool b_trans = is_notrans(tb);    // B stored K x N
+    const unsigned long long gen = g_call_gen.fetch_add(1, std::memory_order_relaxed) + 1;
     tc::SplitJob ja{}, jb{};
     if (!fuse_a) ja = split_job(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, three ? a_lo : nullptr);
     if (!fuse_b) jb = split_job(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, three ? b_lo : nullptr);
+    ja.gen = jb.gen = gen;
     launch_split_pair(three, ja, jb, s);
     const bool dep = ja.blocks + jb.blocks > 0;
     int st = last_status();
@@ -1321,8 +1429,8 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // HBM: 32-wide k-blocks (128-byte rows) there (16384 x 64 x 8192: 2.3 ->
     // 4.5 TB/s of A in the TF32 mode, which always has them; 16384 x 128 x
     // 8192 3xTF32: 142 -> 170 TFLOP/s)
-    const bool wide = three && BN <= 128 && fuse_a && !pair;
-    const int bk = (wide || !three) ? 32 : tc::KBlock<true>::BK;
+    const bool wide = v.wide;
+    const int bk = v.bk;
     CUtensorMap maps[6];
     bool ok;
     if (fuse_a) {
@@ -1359,6 +1467,8 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.row_scale = epi.row_scale;
     p.bias = epi.bias;
     p.act = epi.act;
+    p.raw = tc::RawOps{A, B, lda, ldb, is_notrans(ta) ? 1 : 0, is_notrans(tb) ? 1 : 0, (int)K};
+    p.gen = gen;
     p.units = p.dp_tiles + (p.tiles_m * p.tiles_n - p.dp_tiles) * nsplit;
     p.dp_units = p.units;
     if (sk_ctas > 0) {

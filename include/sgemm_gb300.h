@@ -41,6 +41,16 @@
  * Quick returns (BLAS rules): M == 0 or N == 0 does nothing.  K == 0 or
  * alpha == 0 sets C = beta*C without reading A or B, and C = 0 when
  * beta == 0 (C is not read, so NaN in C does not propagate).
+ *
+ * Infinities and NaN in A or B give, on every path, the result of IEEE fp32
+ * arithmetic: a sum that meets an infinity is that infinity (sign of the
+ * product), or NaN where an infinity meets zero or one of the other sign; NaN
+ * propagates.  The tensor-core paths split each value into two TF32 parts,
+ * and their cross products can turn such an infinite sum into NaN; so a call
+ * whose operands hold an infinity recomputes every output that came out NaN
+ * with fp32 fused multiply-adds in ascending k, straight from A and B (the
+ * FFMA path's arithmetic).  Finite values keep finite parts, also above
+ * (2 - 2^-11) * 2^127 where rounding to TF32 would overflow.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -209,6 +219,45 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
                int *out_path, int *out_split, int *out_tile_m, int *out_tile_n,
                int *out_vector, int *out_ctas);
 
+/*
+ * The selector's whole decision for one problem, down to the kernel variant
+ * (filled by sgemm_plan_detail).  Fields that do not apply to the chosen
+ * path are 0.
+ */
+typedef struct {
+    int path;          /* sgemm_path actually run                               */
+    int tile_m;        /* tile rows: 128, or 256 on an SM pair; GEMV: min(M, N)  */
+    int tile_n;        /* tile columns: 64, 128 or 256 (FFMA: 128; GEMV: 0)     */
+    int vector;        /* FFMA / GEMV: 16-byte operand loads (else 4-byte)      */
+    int ctas;          /* CTAs of the main kernel, as sgemm_plan's out_ctas     */
+    int split;         /* as sgemm_plan's out_split                             */
+    int dp_tiles;      /* tiles computed whole before any shared or narrowed one */
+    /* tensor cores only: */
+    int pair;          /* 256-row tiles on a pair of SMs (tcgen05 cta_group::2) */
+    int fuse_a;        /* A split inside the kernel, into tensor memory         */
+    int fuse_b;        /* B split inside the kernel, in shared memory           */
+    int wide;          /* 3xTF32 with 32-wide k-blocks: A_hi in tensor memory,
+                          A_lo in shared memory, one MMA over [B_hi | B_lo]     */
+    int accumulators;  /* independent accumulators per tile, summed by the
+                          epilogue (1, 2 or 3)                                  */
+    int k_block;       /* k-block width of a pipeline stage, in floats          */
+    int tail_nsplit;   /* column slices of each tile after the last full wave   */
+    int sk_ctas;       /* stream-K over every tile: CTAs sharing the k-blocks   */
+    int sk_tail;       /* 1: the tiles after the last full wave are shared in k
+                          by all CTAs (pairs)                                   */
+} sgemm_plan_info;
+
+/*
+ * sgemm_plan_detail - sgemm_plan's decision with the kernel variant spelled
+ * out (sgemm_plan_info), for tests and tools that must know which kernel a
+ * shape reaches.  Same arguments and checks as sgemm_plan; `out` must not be
+ * NULL (-15).  Touches no GPU.
+ */
+int sgemm_plan_detail(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc,
+                      int a_aligned, int b_aligned, int c_aligned,
+                      int path, int split, int num_sms, sgemm_plan_info *out);
+
 /* Static description of a status code (never NULL). */
 const char *sgemm_status_string(int status);
 
@@ -276,10 +325,10 @@ int sgemm_release_workspace(void);
  * `split` = 0 letting the selector choose.  The partial sums of tiles shared
  * by several CTAs go to a file-scope static __device__ array of 16 MiB (256
  * partial tiles of 128 x 128 floats, two per CTA) that every GPU which loads
- * the library holds until the process exits.  With split = 0 a plan that
- * would need more falls back to computing every tile whole (no scratch);
- * a forced split that needs more returns SGEMM_ERR_SCRATCH and launches
- * nothing (split = 1 never needs scratch).
+ * the library holds until the process exits.  With split = 0, where the
+ * selector would share k-tiles among more than 128 CTAs, the same k-tiles
+ * are shared among 128 CTAs; a forced split that needs more returns
+ * SGEMM_ERR_SCRATCH and launches nothing (split = 1 never needs scratch).
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call

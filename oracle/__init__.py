@@ -186,6 +186,27 @@ def compare_bound(candidate, ref, bound):
             "n_bad": int(np.count_nonzero(~(err <= bound))), "n": int(cand.size)}
 
 
+def compare_ieee(candidate, ref, bound):
+    """Elementwise check for inputs that may hold infinities or NaN.
+
+    Where the fp64 reference is not finite the candidate must be the same:
+    NaN, or an infinity of the same sign.  IEEE arithmetic gives that class
+    in fp32 as in fp64 (inf * finite = inf with the product's sign, inf * 0
+    and inf - inf = NaN, NaN propagates) as long as no finite partial sum
+    overflows fp32.  Elsewhere |cand - ref| <= bound, as in compare().
+    """
+    cand = np.asarray(candidate, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = np.asarray(bound, dtype=np.float64)
+    fin = np.isfinite(ref)
+    same_class = np.where(np.isnan(ref), np.isnan(cand), cand == ref)
+    with np.errstate(invalid="ignore"):
+        within = np.abs(cand - ref) <= bound
+    good = np.where(fin, within, same_class)
+    return {"pass": bool(good.all()), "n_bad": int(np.count_nonzero(~good)),
+            "n_nonfinite": int(np.count_nonzero(~fin)), "n": int(cand.size)}
+
+
 def compare(candidate, ref, bound, K, alpha):
     """Elementwise check of a candidate fp32 result against (ref, bound).
 

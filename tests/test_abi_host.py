@@ -281,3 +281,45 @@ def test_plan_thin_problems_take_the_gemv_path(lib):
 def test_plan_forced_tensor_core_path(lib):
     st, p = sg.sgemm_plan("N", "N", 1024, 1024, 1024, 1024, 1024, 1024, path=sg.PATH_3XTF32)
     assert st == 0 and p["path"] == sg.PATH_3XTF32
+
+
+def test_plan_detail_agrees_with_plan(lib):
+    """sgemm_plan_detail repeats sgemm_plan's fields and spells out the
+    tensor-core variant; NULL output is rejected."""
+    shapes = [("N", "N", 4096, 4096, 4096), ("T", "N", 513, 64, 2000), ("N", "T", 16384, 64, 8192),
+              ("N", "N", 300, 200, 16), ("N", "T", 4, 5000, 300), ("T", "T", 4095, 3073, 1537)]
+    for ta, tb, M, N, K in shapes:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, p = sg.sgemm_plan(ta, tb, M, N, K, lda, ldb, N)
+        st2, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N)
+        assert st == st2 == 0
+        for k in p:
+            assert d[k] == p[k], (ta, tb, M, N, K, k)
+        if d["path"] in (sg.PATH_3XTF32, sg.PATH_TF32):
+            assert d["k_block"] in (16, 32) and d["accumulators"] in (1, 2, 3)
+            assert not (d["pair"] and (d["fuse_a"] or d["fuse_b"]))
+            assert not (d["wide"] and not d["fuse_a"])
+        else:
+            assert d["pair"] == d["fuse_a"] == d["fuse_b"] == d["wide"] == 0
+    assert lib.sgemm_plan_detail(b"N", b"N", 8, 8, 8, 8, 8, 8, 1, 1, 1, 0, 0, 152, None) == -15
+
+
+def test_plan_detail_reaches_every_pinned_variant(lib):
+    """The shapes of the GPU 3xTF32 variant pins reach the variants they are
+    named for (152 SMs), so a selector change cannot empty those pins."""
+    from tests.test_gpu_3xtf32_variants import VARIANTS
+    seen = set()
+    for name, ta, tb, M, N, K, split, want in VARIANTS:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N, path=sg.PATH_3XTF32,
+                                     split=split, num_sms=152)
+        assert st == 0
+        assert {k: d[k] for k in want} == want, (name, d)
+        seen.add((d["tile_n"], d["pair"], d["fuse_a"], d["fuse_b"], d["wide"],
+                  d["sk_ctas"] > 0, d["sk_tail"], d["tail_nsplit"] > 1))
+    # every kernel template of the 3xTF32 path is among them
+    templates = {(t, p, w) for t, p, _, _, w, _, _, _ in seen}
+    assert templates >= {(256, 1, 0), (128, 1, 0), (64, 1, 0), (256, 0, 0), (128, 0, 0),
+                         (64, 0, 0), (128, 0, 1), (64, 0, 1)}

@@ -329,6 +329,51 @@ def test_compare_detects_errors(oracle_mod):
     assert not oracle_mod.compare(bad, ref, bound, K, 1.0)["pass"]
 
 
+# ------------------------------------------------------------ non-finite inputs
+def test_nonfinite_hand_worked(oracle_mod):
+    """IEEE classes by hand: an infinity times a positive value keeps its
+    sign, times a negative one flips it, times zero is NaN; +inf and -inf in
+    one sum give NaN; NaN propagates; a value near FLT_MAX times a small one
+    stays finite.  Both oracle functions, every layout."""
+    inf, big = np.float32(np.inf), np.float32(3.4e38)
+    rows = [
+        ([inf, 1.0], [1.0, 1.0], np.inf),
+        ([inf, 2.0], [-1.0, 1.0], -np.inf),
+        ([inf, -inf], [1.0, 1.0], np.nan),
+        ([inf, 1.0], [0.0, 1.0], np.nan),
+        ([np.nan, 1.0], [1.0, 1.0], np.nan),
+        ([big, 1.0], [2.0 ** -100, 2.0], float(big) * 2.0 ** -100 + 2.0),
+    ]
+    for a, b, want in rows:
+        opA = np.array([a], np.float32)
+        opB = np.array(b, np.float32).reshape(2, 1)
+        for ta, tb in LAYOUTS:
+            ref, bound = run_f64(oracle_mod, ta, tb, opA, opB, 1.0, 0.0)
+            f32 = run_f32(oracle_mod, ta, tb, opA, opB, 1.0, 0.0)
+            if np.isnan(want):
+                assert np.isnan(ref[0, 0]) and np.isnan(f32[0, 0])
+            elif np.isinf(want):
+                assert ref[0, 0] == want and f32[0, 0] == want
+            else:
+                assert abs(ref[0, 0] - want) <= 2.0 ** -52 * abs(want)
+                assert abs(f32[0, 0] - want) <= bound[0, 0]
+
+
+def test_compare_ieee_classes(oracle_mod):
+    """compare_ieee: non-finite reference entries need the same class,
+    finite ones the bound; a wrong sign, NaN for inf, a finite value for inf
+    and an error beyond the bound each fail."""
+    ref = np.array([np.inf, -np.inf, np.nan, 1.0])
+    bound = np.array([np.inf, np.inf, np.nan, 1e-6])
+    good = np.array([np.inf, -np.inf, np.nan, 1.0], np.float32)
+    assert oracle_mod.compare_ieee(good, ref, bound)["pass"]
+    for i, v in [(0, -np.inf), (0, np.nan), (1, 3.0), (2, np.inf), (3, 1.1), (3, np.nan)]:
+        bad = good.copy()
+        bad[i] = v
+        rep = oracle_mod.compare_ieee(bad, ref, bound)
+        assert not rep["pass"] and rep["n_bad"] == 1, (i, v)
+
+
 # ------------------------------------------------------------ fused epilogue
 # D = act(alpha * s_i * (op(A) op(B))_ij + beta * C_ij + bias_j): each term
 # pinned against something other than the epilogue oracle itself.
