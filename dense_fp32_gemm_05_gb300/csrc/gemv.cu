@@ -377,7 +377,9 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     const int k1 = min(p.K, k0 + p.kchunk);
     const int nst = (k1 - k0 + TX_KS - 1) / TX_KS;      // stages of this CTA
     const uint64_t lim = p.wait_ns;
+    __shared__ int gave_up;                             // a consumer's wait ran out
     if (threadIdx.x == 0) {
+        gave_up = 0;
         for (int st = 0; st < TX_ST; ++st) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(full(st)) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(empty(st)), "r"(TX_CW) : "memory");
@@ -460,8 +462,13 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(empty(st)) : "memory");
         }
     }
-    // all consumers are past the ring before it is reused for the reduction
+    // all consumers are past the ring before it is reused for the reduction.
+    // If any consumer's wait ran out, copies the producer issued may still
+    // land in the ring: then no consumer touches it again and nothing is
+    // stored (the error word is raised; the producer drains its copies).
+    if (!ok) gave_up = 1;
     asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
+    if (gave_up) return;
     float *red = ring;                                  // [TX_CW][SM][AX_P]
 #pragma unroll
     for (int s = 0; s < SM; ++s)

@@ -1,7 +1,9 @@
 """sgemm_host: the GEMM on host buffers with the copies pipelined against the
-computation in row blocks.  Checked against the oracle (within the fp32
-bound) for every layout, beta != 0, odd leading dimensions, page-locked and
-pageable buffers, and shapes that make one, several and ragged row blocks."""
+computation in K-chunks and row blocks.  Checked against the oracle (within
+the fp32 bound) for every layout, beta != 0, odd leading dimensions,
+page-locked and pageable buffers, shapes that make one, several and ragged
+row blocks, and K long enough for 2 to 4 chunks (each chunk after the first
+adds into C with beta = 1; the last chunk may be shorter)."""
 import numpy as np
 import pytest
 
@@ -34,6 +36,10 @@ def stored(op_mat, trans, pad):
     (300, 260, 200, 1.0, 0.0, 0, True),          # one row block, small: FFMA
     (2100, 520, 700, 1.5, 0.5, 3, True),         # four ragged row blocks, 3xTF32
     (1537, 1025, 333, -1.0, 1.0, 1, False),      # pageable buffers
+    # K in chunks, each chunk's GEMM adding into C (beta = 1 after the first):
+    (2100, 520, 2050, 1.0, 0.5, 3, True),        # 4 chunks of 544, 544, 544, 418
+    (1537, 1025, 1500, -1.0, 1.0, 1, False),     # 2 chunks (768, 732), pageable
+    (700, 300, 1024, 1.0, 0.0, 0, True),         # 2 equal chunks, beta = 0 over NaN
 ])
 def test_host_api_matches_oracle(oracle_mod, ta, tb, M, N, K, alpha, beta, pad, pinned):
     import torch

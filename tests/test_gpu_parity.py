@@ -230,31 +230,42 @@ def test_special_cases(path):
 
 
 # ------------------------------------------------------------ full-size configs
+# Workloads up to this many flop are compared on every output entry (the
+# oracle runs at ~10 GFLOP/s on the GPU host's cores); larger ones on seeded
+# sample points.
+FULL_COMPARE_FLOPS = 4.0e10
+
+
 @pytest.mark.parametrize("name", list(gi.WORKLOADS))
-def test_workload_full_size_sampled(oracle_mod, name):
+def test_workload_full_size(oracle_mod, name):
     """Every measured workload at full size through sgemm() (the call the
-    benchmark times), checked on seeded sample points (corners, last row and
-    column, uniform points) against the fp64 oracle within the bound."""
+    benchmark times) and, where every entry is compared, through the forced
+    FFMA path too; against the fp64 oracle within the bound.  Workloads up to
+    FULL_COMPARE_FLOPS are compared on every entry of C, larger ones on
+    seeded sample points (corners, last row and column, uniform points)."""
     import torch
 
     w = gi.WORKLOADS[name]
     A, B, C = gi.make_inputs(w)
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
-    dC = torch.from_numpy(C).cuda() if C is not None else torch.full((w.M, w.N), float("nan"),
-                                                                      device="cuda")
-    st = sg.sgemm(w.transA, w.transB, w.M, w.N, w.K, w.alpha, dA.data_ptr(), A.shape[1],
-                  dB.data_ptr(), B.shape[1], w.beta, dC.data_ptr(), w.N,
-                  torch.cuda.current_stream())
-    torch.cuda.synchronize()
-    assert st == 0
-    out = dC.cpu().numpy()
-    rows, cols = gi.sample_points(w.M, w.N, 4096, seed=w.seed)
+    full = w.flops <= FULL_COMPARE_FLOPS
+    points = None if full else gi.sample_points(w.M, w.N, 4096, seed=w.seed)
     ref, bound = oracle_mod.gemm_f64(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A, A.shape[1],
-                                     B, B.shape[1], w.beta, C, w.N, points=(rows, cols))
-    rep = oracle_mod.compare(out[rows, cols], ref, bound, w.K, w.alpha)
-    assert rep["pass"], rep
-    assert np.all(np.isfinite(out))
+                                     B, B.shape[1], w.beta, C, w.N, points=points)
+    for path in ((sg.PATH_AUTO, sg.PATH_FFMA) if full else (sg.PATH_AUTO,)):
+        dC = (torch.from_numpy(C).cuda() if C is not None
+              else torch.full((w.M, w.N), float("nan"), device="cuda"))
+        st = sg.sgemm_ex(w.transA, w.transB, w.M, w.N, w.K, w.alpha, dA.data_ptr(), A.shape[1],
+                         dB.data_ptr(), B.shape[1], w.beta, dC.data_ptr(), w.N,
+                         torch.cuda.current_stream(), path, 0)
+        torch.cuda.synchronize()
+        assert st == 0
+        out = dC.cpu().numpy()
+        assert np.all(np.isfinite(out))
+        rep = oracle_mod.compare(out if full else out[points], ref, bound, w.K, w.alpha)
+        assert rep["pass"], (path, rep)
+        del dC
 
 
 @pytest.mark.parametrize("name", ["sq4096_nn", "ragged_tn", "skinny_nt", "sq1024_nn"])

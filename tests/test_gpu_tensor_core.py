@@ -62,22 +62,34 @@ def test_tf32_within_its_own_bound(oracle_mod, ta, tb):
     assert rep["normwise_rel"] < 1e-3
 
 
+# At K = 4096 the fp32 bound is loose enough that single-pass TF32 meets it
+# (max err/bound ~0.026 on this workload); 3xTF32 measures ~0.002.  A
+# threshold between the two, checked against TF32 on the same samples, makes
+# the full-size test fail if the split's lo terms were lost.
+SPLIT_THRESHOLD = 0.006
+
+
 def test_3xtf32_headline_size_error_budget(oracle_mod):
     """3xTF32 at 4096^3 (the measured workload): every sampled entry within
-    the fp32 bound, with room to spare."""
+    the fp32 bound, and the worst err/bound below a threshold that
+    single-pass TF32 exceeds on the same samples."""
     import torch
     w = gi.WORKLOADS["sq4096_nn"]
     A, B, _ = gi.make_inputs(w)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
-    dC = torch.empty((w.M, w.N), device="cuda")
-    st = sg.sgemm_ex("N", "N", w.M, w.N, w.K, 1.0, dA.data_ptr(), w.K, dB.data_ptr(), w.N, 0.0,
-                     dC.data_ptr(), w.N, torch.cuda.current_stream(), sg.PATH_3XTF32, 0)
-    assert st == 0 and sg.sgemm_device_error(torch.cuda.current_stream()) == 0
     rows, cols = gi.sample_points(w.M, w.N, 3000, seed=11)
     ref, bound = oracle_mod.gemm_f64("N", "N", w.M, w.N, w.K, 1.0, A, w.K, B, w.N, 0.0, None,
                                      w.N, points=(rows, cols))
-    rep = oracle_mod.compare(dC.cpu().numpy()[rows, cols], ref, bound, w.K, 1.0)
-    assert rep["pass"] and rep["max_err_over_bound"] < 0.25, rep
+    reps = {}
+    for path in (sg.PATH_3XTF32, sg.PATH_TF32):
+        dC = torch.empty((w.M, w.N), device="cuda")
+        st = sg.sgemm_ex("N", "N", w.M, w.N, w.K, 1.0, dA.data_ptr(), w.K, dB.data_ptr(), w.N,
+                         0.0, dC.data_ptr(), w.N, torch.cuda.current_stream(), path, 0)
+        assert st == 0 and sg.sgemm_device_error(torch.cuda.current_stream()) == 0
+        reps[path] = oracle_mod.compare(dC.cpu().numpy()[rows, cols], ref, bound, w.K, 1.0)
+    three, tf32 = reps[sg.PATH_3XTF32], reps[sg.PATH_TF32]
+    assert three["pass"] and three["max_err_over_bound"] < SPLIT_THRESHOLD, three
+    assert tf32["max_err_over_bound"] > SPLIT_THRESHOLD, tf32
 
 
 @pytest.mark.parametrize("path", [sg.PATH_3XTF32, sg.PATH_TF32])
