@@ -7,11 +7,16 @@ beta = 0, A and B uniform[-1, 1] from seed 3, inputs resident in HBM.  L2 is
 flushed between steps by writing a 256 MB buffer; the flush is outside the
 CUDA events that time each step.
 
-Prints ONE JSON line (rank 0).  Keys beyond the base contract:
-  roofline      dominant kernel: achieved / peak (FFMA: "alu" bound, peak =
-                SMs x 128 lanes x 2 flop x max SM clock; also at the median
-                clock sampled during the run), DRAM traffic from the
-                committed ncu summary when it matches the current kernel.
+Prints ONE JSON line (rank 0).  The headline value comes from K steps with
+nothing but the calls in them.  Keys beyond the base contract:
+  roofline      dominant kernel: achieved / peak, its launches timed by the
+                library's CUDA event pair on the launching stream over a
+                second region of the same K steps (FFMA: "alu" bound, peak =
+                SMs x 128 lanes x 2 flop x max SM clock; tensor cores: the
+                measured bf16 peak x 1.1/2.25, and beside it SMs x the
+                measured kind::tf32 MAC rate per clock (library probe) x 2 x
+                SM clock), DRAM traffic from the committed ncu summary when
+                it matches the current kernel.
   cpu_baseline  the CPU oracle (fp64 triple loop) timed on a bounded sample
                 of the same workload on the host cores.
   e2e           the same metric through sgemm_host() on pinned host
@@ -19,6 +24,10 @@ Prints ONE JSON line (rank 0).  Keys beyond the base contract:
                 of C (pipelined in row blocks), all inside the timed region.
   paths         every GPU path timed on the same workload (TFLOP/s, fraction
                 of its roofline, error vs the oracle on sample points).
+  workloads     every workload through sgemm(): flushed median and min,
+                unflushed median, roofline fraction, and the CPU oracle's
+                GFLOP/s on a bounded row sample (all cores; one core for the
+                small square ones) with the GPU/oracle speed-up.
   clocks        nvidia-smi SM clock samples during the timed region.
 
 --impl reference times the CPU oracle itself (the reference arm).
@@ -245,12 +254,56 @@ def reference_arm(args):
     return 0
 
 
-def workload_table(dev, stream, flush, ffma_peak, tf32_peak, hbm_gbs, reps=5):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def event_times(call, stream, flush, reps, flushed):
+    """CUDA-event durations (ms) of `reps` calls on `stream`; with `flushed`
+    L2 is flushed before each call, outside its events."""
+    import torch
+    ev = []
+    for i in range(reps):
+        if flushed:
+            flush.fill_(0.25 + i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+# 1-core oracle timings for these workloads (the small square ones)
+ONE_CORE = ("sq256_nn", "sq1024_nn", "sq2048_nn_ab")
+
+
+def workload_table(dev, stream, flush, ffma_peak, tf32_peak, hbm_gbs, reps=5, oracle_s=1.0):
     """Every workload through sgemm() (the selector's path), device-timed with
-    L2 flushed between calls, against the roofline of the path that ran:
-    attainable = min(the path's compute peak, arithmetic intensity x HBM).
-    Inputs are drawn on the device (seeded, the workload's distribution):
-    this table times; the parity tests check."""
+    L2 flushed between calls (median and min) and without flushing (median),
+    against the roofline of the path that ran: attainable = min(the path's
+    compute peak, arithmetic intensity x HBM).  Inputs are drawn on the device
+    (seeded, the workload's distribution): this table times; the parity tests
+    check.  With oracle_s > 0 the CPU oracle is timed beside each workload on
+    a bounded sample of whole rows of C (its own numpy draw), on all host
+    cores and, for the small square workloads, on one core."""
     import torch
     import dense_fp32_gemm_05_gb300 as sg
 
@@ -278,29 +331,42 @@ def workload_table(dev, stream, flush, ffma_peak, tf32_peak, hbm_gbs, reps=5):
                 raise sg.SgemmError(st)
         call()
         torch.cuda.synchronize(dev)
-        ev = []
-        for _ in range(reps):
-            flush.fill_(0.25)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            call()
-            e1.record(stream)
-            ev.append((e0, e1))
-        torch.cuda.synchronize(dev)
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        flushed = event_times(call, stream, flush, reps, True)
+        warm = event_times(call, stream, flush, reps, False)
+        ms = statistics.median(flushed)
         tfl = w.flops / (ms / 1e3) / 1e12
         gbs = w.compulsory_bytes() / (ms / 1e3) / 1e9
         compute = {"ffma": ffma_peak, "gemv": ffma_peak, "3xtf32": tf32_peak / 3.0,
                    "tf32": tf32_peak}.get(path, ffma_peak)
         hbm_roof = w.flops / w.compulsory_bytes() * hbm_gbs / 1e3
         attain = min(compute, hbm_roof)
-        table[name] = {"path": path, "ms": round(ms, 4), "tflops": round(tfl, 3),
-                       "gbs": round(gbs, 1),
-                       "bound": "hbm" if hbm_roof < compute else
-                                ("tensor" if path in ("3xtf32", "tf32") else "alu"),
-                       "attainable_tflops": round(attain, 3), "frac": round(tfl / attain, 4)}
+        ent = {"path": path, "ms": round(ms, 4), "ms_min": round(min(flushed), 4),
+               "ms_unflushed": round(statistics.median(warm), 4),
+               "tflops": round(tfl, 3),
+               "tflops_unflushed": round(w.flops / (statistics.median(warm) / 1e3) / 1e12, 3),
+               "gbs": round(gbs, 1),
+               "bound": "hbm" if hbm_roof < compute else
+                        ("tensor" if path in ("3xtf32", "tf32") else "alu"),
+               "attainable_tflops": round(attain, 3), "frac": round(tfl / attain, 4)}
         del dA, dB, dC
+        if oracle_s > 0:
+            A, B, C = gi.make_inputs(w)
+            v, rows, dt, threads = oracle_sample(w, A, B, C, seconds_target=oracle_s)
+            ent["oracle"] = {"gflops": round(v / 1e9, 3), "threads": threads, "rows": rows,
+                             "seconds": round(dt, 2)}
+            ent["speedup_vs_oracle"] = round(tfl * 1e12 / v, 1)
+            if name in ONE_CORE:
+                import oracle
+                n = oracle.num_threads()
+                oracle.set_num_threads(1)
+                try:
+                    v1, rows1, dt1, _ = oracle_sample(w, A, B, C, seconds_target=oracle_s)
+                finally:
+                    oracle.set_num_threads(n)
+                ent["oracle_1core"] = {"gflops": round(v1 / 1e9, 3), "rows": rows1,
+                                       "seconds": round(dt1, 2)}
+            del A, B, C
+        table[name] = ent
     torch.cuda.empty_cache()
     return table
 
@@ -351,6 +417,18 @@ def gpu_arm(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    def timed_steps(n):
+        """n steps, L2 flushed before each outside its events: per-step ms."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        barrier()
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
     # ---- warm-up
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -358,49 +436,58 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
 
     # ---- timed region: K steps, per-step CUDA events on the launching stream
+    # (nothing else in the calls: the kernel timing hook is off here)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    # the library records its main kernel's launches on the same stream
-    sg.sgemm_timing_enable(args.steps)
     barrier()
     launches0 = sg.sgemm_launch_count()
-    t_wall = time.perf_counter()
-    t_begin = t_wall
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        starts[i].record(stream)
-        call()
-        ends[i].record(stream)
-    barrier()
+    t_begin = time.perf_counter()
+    step_ms = timed_steps(args.steps)
     t_end = time.perf_counter()
     launches = sg.sgemm_launch_count() - launches0
-    t_wall = t_end - t_wall
-    time.sleep(0.05)                # the last in-region sample reaches the reader
-    sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kernel_ms = sg.sgemm_timing_read(args.steps)
-    sg.sgemm_timing_enable(0)
+    t_wall = t_end - t_begin
     total_ms, value = job_throughput(sum(step_ms), args.steps, w.flops, device=dev)
     ms_per_step = total_ms / args.steps
+
+    # ---- roofline region: the same K steps again, now with the library's
+    # CUDA event pair around each launch of the main kernel (on the launching
+    # stream).  The events sit between the call's kernels, so this region's
+    # call times are not the headline; its kernel times are the roofline's.
+    sg.sgemm_timing_enable(args.steps)
+    t_rbegin = time.perf_counter()
+    hooked_ms = timed_steps(args.steps)
+    t_rend = time.perf_counter()
+    kernel_ms = sg.sgemm_timing_read(args.steps)
+    sg.sgemm_timing_enable(0)
+    time.sleep(0.05)                # the last in-region sample reaches the reader
+    sampler.stop()
     # samples that arrived while the timed steps ran (nvidia-smi prints each
     # shortly after taking it: a 25 ms allowance at the end)
     clocks = sampler.summary(t_begin, t_end + 0.025)
+    roof_clocks = sampler.summary(t_rbegin, t_rend + 0.025)
 
     # ---- plan of the timed call: which kernels ran
-    st, plan = sg.sgemm_plan(w.transA, w.transB, w.M, w.N, w.K, lda, ldb, ldc, True, True, True,
-                             sg.PATH_AUTO, 0, sms)
+    st, plan = sg.sgemm_plan_detail(w.transA, w.transB, w.M, w.N, w.K, lda, ldb, ldc, True, True,
+                                    True, sg.PATH_AUTO, 0, sms)
 
-    # ---- per-path timings on the same workload (outside the timed region)
+    # ---- peaks
     peaks, peak_src = measured_peaks()
     max_mhz = clocks["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
     med_mhz = clocks["sm_mhz"] or max_mhz
+    roof_mhz = roof_clocks["sm_mhz"] or med_mhz
     ffma_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
     ffma_peak_med = sms * FP32_LANES_PER_SM * 2 * med_mhz * 1e6 / 1e12
-    # TF32 tensor peak: measured bf16 (burst) x nominal tf32/bf16 ratio (1.1/2.25)
+    # TF32 tensor peak, the recipe's rule: measured bf16 (burst) x nominal
+    # tf32/bf16 ratio (1.1/2.25); and from the tensor pipe's measured
+    # kind::tf32 rate (library probe) x SMs x 2 flop x SM clock
     tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
+    pst, mac_rate = sg.sgemm_probe_tf32_rate(4096)
+    if pst != 0:
+        mac_rate = None
+    tf32_rate_peak = (lambda mhz: sms * mac_rate * 2 * mhz * 1e6 / 1e12) if mac_rate else None
+
+    # ---- per-path timings on the same workload (outside the timed region)
     paths = {}
     rows_s, cols_s = gi.sample_points(w.M, w.N, 2048, seed=w.seed)
     ref = bound = None
@@ -424,21 +511,14 @@ def gpu_arm(args):
             paths[name] = {"status": e.status, "note": sg.sgemm_status_string(e.status)}
             continue
         torch.cuda.synchronize(dev)
-        ms = []
         t_pb = time.perf_counter()
-        for _ in range(max(20 if name == "ffma" else 3, args.path_reps)):
-            flush.fill_(0.5)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            call(pid)
-            e1.record(stream)
-            ms.append((e0, e1))
-        torch.cuda.synchronize(dev)
+        ms = event_times(lambda: call(pid), stream, flush,
+                         max(20 if name == "ffma" else 3, args.path_reps), True)
         t_pe = time.perf_counter()
-        t = statistics.median([a.elapsed_time(b) for a, b in ms])
+        warm = event_times(lambda: call(pid), stream, flush, 5, False)
+        t = statistics.median(ms)
         tfl = w.flops / (t / 1e3) / 1e12
-        ent = {"ms": t, "tflops": tfl}
+        ent = {"ms": t, "ms_min": min(ms), "ms_unflushed": statistics.median(warm), "tflops": tfl}
         time.sleep(0.05)
         ck = path_clocks.summary(t_pb, t_pe + 0.025) if path_clocks.proc else path_clocks.summary()
         ent["clocks"] = {"sm_mhz": ck["sm_mhz"], "reasons": ck["reasons"], "samples": ck["samples"]}
@@ -451,6 +531,10 @@ def gpu_arm(args):
             mult = 3 if name == "3xtf32" else 1
             ent["tensor_tflops"] = mult * tfl
             ent["frac_tf32_tensor_peak"] = mult * tfl / tf32_peak
+            if tf32_rate_peak:
+                ent["frac_tf32_rate_peak_max_clock"] = mult * tfl / tf32_rate_peak(max_mhz)
+                if ck["sm_mhz"]:
+                    ent["frac_tf32_rate_peak_sampled_clock"] = mult * tfl / tf32_rate_peak(ck["sm_mhz"])
         if ref is not None:
             import oracle
             out = dC.cpu().numpy()[rows_s, cols_s]
@@ -463,13 +547,12 @@ def gpu_arm(args):
     # ---- every workload through the selector, against its path's roofline
     workloads = None
     if rank == 0 and not args.no_workloads:
-        workloads = workload_table(dev, stream, flush, ffma_peak, tf32_peak, peaks["hbm_gbs"])
+        workloads = workload_table(dev, stream, flush, ffma_peak, tf32_peak, peaks["hbm_gbs"],
+                                   oracle_s=0.0 if (args.no_cpu or world > 1) else args.workload_oracle_s)
 
-    # ---- dominant kernel of the timed call: its launches measured alone
+    # ---- dominant kernel of the timed call, from the roofline region
     main_name = {sg.PATH_FFMA: "ffma", sg.PATH_3XTF32: "3xtf32", sg.PATH_TF32: "tf32",
                  sg.PATH_GEMV: "gemv"}[plan["path"]]
-    # the dominant kernel's own launches inside the timed region (library
-    # timing hook: events around the main kernel only)
     k_ms = statistics.mean(kernel_ms) if kernel_ms else ms_per_step
     mult = 3 if main_name == "3xtf32" else 1
     achieved = w.flops / (k_ms / 1e3) / 1e12          # useful flop rate of the kernel
@@ -487,9 +570,23 @@ def gpu_arm(args):
                     "peak_basis": f"{peak_src} bf16 {peaks['bf16_tflops']} TFLOP/s x 1.1/2.25 "
                                   "(nominal tf32/bf16 ratio)",
                     "kernel": "tc_gemm_kernel"}
+        if tf32_rate_peak:
+            roofline.update({
+                "tf32_mac_per_clock_per_sm": mac_rate,
+                "peak_tf32_rate_sampled_clock": tf32_rate_peak(roof_mhz),
+                "frac_tf32_rate_sampled_clock": tt / tf32_rate_peak(roof_mhz),
+                "peak_tf32_rate_max_clock": tf32_rate_peak(max_mhz),
+                "frac_tf32_rate_max_clock": tt / tf32_rate_peak(max_mhz),
+                "tf32_rate_basis": f"{sms} SMs x {mac_rate:.0f} MAC/clock/SM (measured, "
+                                   "tcgen05.mma kind::tf32 128x256x8 issue loop) x 2 flop x SM "
+                                   f"clock ({roof_mhz:.0f} MHz median in the roofline region; "
+                                   f"{max_mhz:.0f} MHz max)"})
     roofline["traffic"] = traffic_from_profiles(roofline["kernel"] + ":" + w.name)
     roofline["kernel_ms"] = k_ms
     roofline["kernel_launches_timed"] = len(kernel_ms)
+    roofline["timing"] = ("library CUDA event pair around each main-kernel launch, on the "
+                          "launching stream, over a second region of the same steps")
+    roofline["call_ms_with_events"] = statistics.mean(hooked_ms)
     if main_name != "ffma":
         roofline["useful_tflops"] = achieved
 
@@ -519,6 +616,13 @@ def gpu_arm(args):
     e2e_val = world * e_steps * w.flops / e_dt / 1e12
     h2d = A.nbytes + B.nbytes + (C.nbytes if C is not None else 0)
     d2h = w.M * w.N * 4
+    e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "entry_point": "sgemm_host"}
+    if ref is not None and w.beta == 0:
+        import oracle
+        rep = oracle.compare(hC.numpy()[rows_s, cols_s], ref, bound, w.K, w.alpha)
+        e2e.update({"oracle_pass": rep["pass"], "max_err_over_bound": rep["max_err_over_bound"],
+                    "oracle_points": int(rows_s.size)})
 
     # ---- CPU oracle baseline (rank 0, N == 1 only)
     cpu = None
@@ -526,20 +630,22 @@ def gpu_arm(args):
         v, rows, dt, threads = oracle_sample(w, A, B, C, seconds_target=args.ref_seconds)
         cpu = {"value": v / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"rows 0..{rows - 1} of C ({rows} x {w.N} outputs, "
-                         f"{2 * rows * w.N * w.K:.3e} flop), {dt:.1f} s"}
+                         f"{2 * rows * w.N * w.K:.3e} flop), {dt:.1f} s",
+               "cpu_model": cpu_model()}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "ms_per_step_min": min(step_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": workload_config(w),
-            "roofline": roofline, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"], "samples": clocks["samples"]},
+            "roofline_clocks": {"sm_mhz": roof_clocks["sm_mhz"], "reasons": roof_clocks["reasons"],
+                                "samples": roof_clocks["samples"]},
             "plan": plan, "paths": paths, "workloads": workloads, "ffma_peak_tflops": ffma_peak,
             "wall_s_timed": t_wall, "peaks_source": peak_src,
         }
@@ -600,6 +706,8 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the oracle sample check")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (every workload through sgemm)")
+    ap.add_argument("--workload-oracle-s", type=float, default=1.0,
+                    help="seconds of CPU oracle time per workload in the table (0: none)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)

@@ -19,7 +19,8 @@ __all__ = [
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan", "sgemm_plan_detail", "sgemm_status_string",
     "sgemm_device_error", "sgemm_set_wait_limit", "sgemm_release_workspace",
     "sgemm_version", "sgemm_ffma_static_scratch", "sgemm_timing_enable",
-    "sgemm_timing_read", "sgemm_launch_count", "gemm", "exported_symbols",
+    "sgemm_timing_read", "sgemm_launch_count", "sgemm_probe_tf32_rate", "gemm",
+    "exported_symbols",
 ]
 
 SGEMM_OK = 0
@@ -95,6 +96,8 @@ def _declare(lib):
     lib.sgemm_timing_enable.restype = i32
     lib.sgemm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i32]
     lib.sgemm_timing_read.restype = i32
+    lib.sgemm_probe_tf32_rate.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
+    lib.sgemm_probe_tf32_rate.restype = i32
     lib.sgemm_launch_count.argtypes = []
     lib.sgemm_launch_count.restype = i64
     lib.sgemm_ffma_static_scratch.argtypes = gemm_args + [i32]
@@ -123,7 +126,7 @@ def exported_symbols(lib=None):
             "sgemm_status_string", "sgemm_device_error",
             "sgemm_set_wait_limit", "sgemm_release_workspace", "sgemm_version",
             "sgemm_ffma_static_scratch", "sgemm_timing_enable", "sgemm_timing_read",
-            "sgemm_launch_count"]
+            "sgemm_launch_count", "sgemm_probe_tf32_rate"]
 
 
 def _b(t: str) -> bytes:
@@ -212,6 +215,13 @@ def sgemm_version() -> int:
 def sgemm_timing_enable(n: int) -> int:
     """Record event pairs around the main kernel of the next n launches."""
     return load().sgemm_timing_enable(n)
+
+
+def sgemm_probe_tf32_rate(reps: int = 4096):
+    """Measured tcgen05 kind::tf32 rate: (status, multiply-adds per clock per SM)."""
+    v = ctypes.c_double(0.0)
+    st = load().sgemm_probe_tf32_rate(reps, ctypes.byref(v))
+    return st, v.value
 
 
 def sgemm_launch_count() -> int:

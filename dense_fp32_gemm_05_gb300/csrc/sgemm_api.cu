@@ -383,6 +383,16 @@ extern "C" int64_t sgemm_launch_count(void) {
     return g_launches.load(std::memory_order_relaxed);
 }
 
+extern "C" int sgemm_probe_tf32_rate(int reps, double *mac_per_clock) {
+    if (reps < 64 || reps > (1 << 20)) return -1;
+    if (mac_per_clock == nullptr) return -2;
+    DeviceState *d = nullptr;
+    int st = device_state(&d);
+    if (st != SGEMM_OK) return st;
+    if (!(d->cc_major == 10 && d->cc_minor == 3)) return SGEMM_ERR_UNSUPPORTED;
+    return tc_probe_tf32_rate(reps, mac_per_clock);
+}
+
 extern "C" int sgemm_timing_enable(int n) {
     if (n < 0 || n > 100000) return -1;
     int dev = 0;

@@ -47,6 +47,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "ptx_util.cuh"
 #include "tc_gemm.h"
@@ -1207,6 +1208,58 @@ __global__ void __launch_bounds__(256) split_pair_kernel(const SplitJob j0, cons
     }
 }
 
+// ---------------------------------------------------------------- MMA rate probe
+// The tensor pipe's kind::tf32 rate, measured: one CTA per SM (the dynamic
+// shared memory admits one), one thread issues `reps` MMAs of 128 x 256 x 8
+// back to back from zeroed shared-memory operands into one TMEM accumulator,
+// commits them to a barrier and waits (bounded).  clock64 around the issue
+// loop and the wait gives that SM's cycles for `reps` MMAs (0 on a timeout).
+constexpr int PROBE_SMEM = 120 * 1024;
+__device__ unsigned long long g_probe_cycles[1024];
+
+__global__ void __launch_bounds__(128, 1) tf32_rate_probe_kernel(int reps, unsigned long long wait_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tslot;
+    // A: 128 rows x 64 bytes, B: 256 rows x 64 bytes (K = 16 floats per row)
+    for (int i = threadIdx.x; i < (128 + 256) * 64 / 16; i += blockDim.x)
+        reinterpret_cast<float4 *>(base)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the zero stores are read by the tensor core (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (threadIdx.x < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;"
+                     :: "r"(smem_u32(&tslot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    if (threadIdx.x == 0) {
+        const uint32_t idesc = idesc_tf32(256);
+        const uint64_t a = smem_desc<64>(smem_u32(base));
+        const uint64_t b = smem_desc<64>(smem_u32(base + 128 * 64));
+        const long long t0 = clock64();
+        for (int i = 0; i < reps; ++i) umma_tf32(tmem, a, b, idesc, i > 0 ? 1u : 0u);
+        umma_commit(smem_u32(&bar));
+        const bool ok = mbar_wait(smem_u32(&bar), 0, wait_ns);
+        const long long t1 = clock64();
+        if (blockIdx.x < 1024) g_probe_cycles[blockIdx.x] = ok ? (unsigned long long)(t1 - t0) : 0ull;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" :: "r"(tmem) : "memory");
+    }
+}
+
 }  // namespace tc
 
 // ---------------------------------------------------------------- host side
@@ -1269,6 +1322,34 @@ static int last_status() {
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
         return SGEMM_ERR_UNSUPPORTED;
     return SGEMM_ERR_CUDA;
+}
+
+int tc_probe_tf32_rate(int reps, double *mac_per_clock) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    sms = std::min(sms, 1024);
+    if (cudaFuncSetAttribute(tc::tf32_rate_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::PROBE_SMEM) != cudaSuccess)
+        return last_status();
+    std::vector<unsigned long long> cyc((size_t)sms);
+    for (int run = 0; run < 2; ++run) {            // the first run warms up
+        count_launch();
+        tc::tf32_rate_probe_kernel<<<sms, 128, tc::PROBE_SMEM>>>(reps, tc::kDefaultWaitNs);
+        int st = last_status();
+        if (st != SGEMM_OK) return st;
+        if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+    }
+    if (cudaMemcpyFromSymbol(cyc.data(), tc::g_probe_cycles, cyc.size() * sizeof(cyc[0])) !=
+        cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    for (unsigned long long c : cyc)
+        if (c == 0) return SGEMM_ERR_TIMEOUT;
+    std::sort(cyc.begin(), cyc.end());
+    const double per_mma = (double)cyc[cyc.size() / 2] / reps;   // median SM
+    *mac_per_clock = 128.0 * 256.0 * 8.0 / per_mma;
+    return SGEMM_OK;
 }
 
 static tc::SplitJob split_job(const float *src, int64_t ld, bool trans, int rows, int K, int Kp,

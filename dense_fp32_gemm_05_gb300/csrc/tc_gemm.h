@@ -15,6 +15,10 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
            const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
            int64_t ldc, cudaStream_t s, int sms, const Epilogue &epi = Epilogue{});
 
+// Measures the tensor pipe's kind::tf32 MMA rate on the current device
+// (MAC per clock per SM, median over the SMs); synchronises the device.
+int tc_probe_tf32_rate(int reps, double *mac_per_clock);
+
 // Reads and clears the current device's sticky device error word.
 int tc_take_device_error();
 

@@ -298,6 +298,20 @@ int sgemm_timing_enable(int n);
 int sgemm_timing_read(float *ms, int capacity);
 
 /*
+ * sgemm_probe_tf32_rate - the tensor pipe's measured rate for the MMAs of the
+ * tensor-core paths, the denominator of their roofline: one CTA per SM issues
+ * `reps` (64 .. 2^20) tcgen05.mma kind::tf32 instructions of 128 x 256 x 8
+ * back to back from zeroed shared-memory operands into tensor memory, timed
+ * with the SM's cycle counter.  Writes the median over the SMs of the
+ * multiply-adds per clock per SM to *mac_per_clock; the TF32 peak is then
+ * SMs x *mac_per_clock x 2 flop x SM clock.  A measurement hook: launches
+ * on the legacy default stream and synchronises the device.  Returns
+ * SGEMM_OK, -1 / -2 for a bad argument, SGEMM_ERR_TIMEOUT when a probe's
+ * bounded wait ran out, SGEMM_ERR_UNSUPPORTED off compute capability 10.3.
+ */
+int sgemm_probe_tf32_rate(int reps, double *mac_per_clock);
+
+/*
  * sgemm_launch_count - the number of GPU kernels this library has launched in
  * this process, on every device and path: split pre-passes, main kernels,
  * stream-K and K-split reductions, and the C = beta*C quick return.  A

@@ -65,6 +65,8 @@ def _load():
             lib.oracle_gemm_epilogue_f64.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -72,6 +74,12 @@ def _load():
 def num_threads() -> int:
     """Threads the oracle's OpenMP loops use."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Sets the threads of the oracle's OpenMP loops (results are unchanged:
+    every entry is computed by one thread in a fixed order)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _ptr(a):

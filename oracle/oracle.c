@@ -98,6 +98,16 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads for the following calls (n >= 1); the results do not depend on it. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /*
  * ref[p], bound[p] for every output point p.  With rows == NULL the points
  * are all (i, j) in row-major order and ref/bound are M*N arrays; otherwise

@@ -323,3 +323,11 @@ def test_plan_detail_reaches_every_pinned_variant(lib):
     templates = {(t, p, w) for t, p, _, _, w, _, _, _ in seen}
     assert templates >= {(256, 1, 0), (128, 1, 0), (64, 1, 0), (256, 0, 0), (128, 0, 0),
                          (64, 0, 0), (128, 0, 1), (64, 0, 1)}
+
+
+def test_tf32_rate_probe_argument_errors(lib):
+    """The rate probe rejects its arguments before touching a device."""
+    v = ctypes.c_double(0.0)
+    assert lib.sgemm_probe_tf32_rate(10, ctypes.byref(v)) == -1
+    assert lib.sgemm_probe_tf32_rate(1 << 21, ctypes.byref(v)) == -1
+    assert lib.sgemm_probe_tf32_rate(4096, None) == -2

@@ -119,3 +119,14 @@ def test_bounded_wait_timeout_reports_and_recovers(oracle_mod, path):
     assert st == 0 and sg.sgemm_device_error(s) == 0
     ref, bound = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
     assert oracle_mod.compare(dC.cpu().numpy(), ref, bound, K, 1.0)["pass"]
+
+
+def test_tf32_rate_probe():
+    """The tensor pipe's kind::tf32 rate (the tensor-core roofline's
+    denominator) is measured and physically sensible: a 128 x 256 x 8 MMA
+    takes at least 128 cycles on one SM (2048 MAC per clock), and no SM
+    takes more than twice that."""
+    st, rate = sg.sgemm_probe_tf32_rate(4096)
+    assert st == sg.SGEMM_OK, sg.sgemm_status_string(st)
+    assert 1024.0 < rate <= 2048.0 * 1.01, rate
+    assert sg.sgemm_device_error(None) == sg.SGEMM_OK

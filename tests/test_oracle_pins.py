@@ -465,3 +465,23 @@ def test_epilogue_rejects_unknown_activation(oracle_mod):
     with pytest.raises(oracle_mod.OracleArgError):
         oracle_mod.gemm_epilogue_f64("N", "N", 2, 2, 2, 1.0, np.ones((2, 2), np.float32), 2,
                                      np.ones((2, 2), np.float32), 2, 0.0, None, 2, act=7)
+
+
+def test_thread_count_does_not_change_results(oracle_mod):
+    """Every entry is summed by one thread in a fixed order: one thread and
+    all threads give the same bits."""
+    M, N, K = 37, 29, 301
+    A = gi.random_matrix(81, M, K)
+    B = gi.random_matrix(82, K, N)
+    n = oracle_mod.num_threads()
+    try:
+        oracle_mod.set_num_threads(1)
+        assert oracle_mod.num_threads() == 1
+        r1, b1 = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+        f1 = oracle_mod.gemm_f32_seq("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    finally:
+        oracle_mod.set_num_threads(n)
+    r2, b2 = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    f2 = oracle_mod.gemm_f32_seq("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    assert np.array_equal(r1, r2) and np.array_equal(b1, b2)
+    assert np.array_equal(f1.view(np.uint32), f2.view(np.uint32))
