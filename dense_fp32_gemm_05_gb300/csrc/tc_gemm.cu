@@ -44,7 +44,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -131,7 +130,7 @@ struct Cfg {
 // this way (sk_tile0 = 0, single SMs), or the CTAs first compute the first
 // dp_units tiles whole, one wave after another, and share only the rest: the
 // last, partly filled wave.
-// The caller's operands as given (for the fp32 redo of NaN sums).
+// The caller's operands as given.
 struct RawOps {
     const float *A, *B;
     int64_t lda, ldb;
@@ -159,8 +158,8 @@ struct Params {
     int sk_tile0;               // stream-K: first shared tile
     long long sk_iters;         // stream-K: shared tiles * num_kb
     float *partial;             // stream-K: 2 * sk_ctas tiles of TM x BN floats
-    RawOps raw;                 // the caller's A and B
-    unsigned long long gen;     // this call's stamp (see g_inf_gen)
+    RawOps raw;                 // the caller's A and B (for the fp32 redo of non-finite sums)
+    int three;                  // 3xTF32 (else single-pass TF32)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -381,93 +380,96 @@ __device__ __forceinline__ float tf32_round(float x) {
     return __uint_as_float(r);
 }
 
+// Non-finite inputs.  The split is exact (up to lo's rounding) for every
+// finite x whose rounding to TF32 stays finite.  An infinite x (hi = inf,
+// lo = inf - inf = NaN), or a finite one that rounds to infinity (|x| above
+// (2 - 2^-11) 2^127: lo = x - inf), makes every 3xTF32 sum it enters NaN,
+// where fp32 arithmetic gives an infinity, NaN or, in the rounding case, a
+// finite value; in single-pass TF32 such a sum is infinite or NaN.  Those
+// sums are redone in fp32 after the fact: the epilogue checks its outputs
+// (one packed FMA by zero per two outputs finds any NaN or infinity), and a
+// block with a NaN sum (3xTF32) or a non-finite one (TF32) has those outputs
+// recomputed by the warp straight from A and B.  A sum whose true value is
+// infinite or NaN comes out of the redo the same, so the result is the IEEE
+// fp32 one on this path too; the split itself pays nothing.
 __device__ __forceinline__ float f32_inf() { return __uint_as_float(0x7f800000u); }
 
-// The two parts of one operand value x = hi + lo (+ a residual of about
-// 2^-22 |x|), both TF32.  hi = rna_tf32(x), except where that rounding
-// overflows a finite x (|x| >= (2 - 2^-11) 2^127): there hi is x with its low
-// 13 bits cleared, so no finite input becomes infinite.  lo = rna_tf32(x - hi)
-// (x - hi is exact in fp32) when hi is finite; an infinite or NaN x is
-// carried by hi alone (lo = 0, not inf - inf).  `inf` is raised when x is
-// infinite.
-__device__ __forceinline__ float split_hi(float x, bool &inf) {
-    float h = tf32_round(x);
-    if (fabsf(h) == f32_inf()) {
-        inf |= fabsf(x) == f32_inf();
-        h = __uint_as_float(__float_as_uint(x) & 0xffffe000u);
-    }
-    return h;
+template <bool THREE>
+__device__ __forceinline__ bool needs_redo(float v) {
+    return THREE ? v != v : !(fabsf(v) < f32_inf());
 }
 
-__device__ __forceinline__ float split_lo(float x, float h) {
-    const float l = tf32_round(__fsub_rn(x, h));
-    return fabsf(h) < f32_inf() ? l : 0.0f;
-}
-
-// Infinite operand values and the NaN they can cause.  A sum that meets an
-// infinite input is infinite or NaN in fp32 arithmetic; on the tensor cores
-// the cross terms hi*lo multiply an infinity by its partner's low part, which
-// may be zero or of the other sign, so an infinite sum can come out NaN.  A
-// call that meets an infinite operand value therefore redoes, in fp32 with
-// fused multiply-adds in ascending k (the naive loop), every output whose sum
-// came out NaN; that gives the IEEE result.  g_inf_gen holds the largest
-// call stamp (Params::gen, increasing per call) whose split met an infinity;
-// a call's kernels compare it with their own stamp, so the word never needs
-// clearing, and a later call's stamp can only cause a redundant redo.
-__device__ unsigned long long g_inf_gen;
-
-__device__ __forceinline__ void note_inf(unsigned long long gen) { atomicMax(&g_inf_gen, gen); }
-
-__device__ __forceinline__ bool inf_seen(unsigned long long gen) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&g_inf_gen) : "memory");
-    return v >= gen;
-}
-
-// sum_k op(A)(row, k) * op(B)(k, col) in fp32, fused multiply-adds in
-// ascending k from 0, straight from the caller's operands.
-__device__ __noinline__ float dot_fp32(const RawOps o, int row, int col) {
+// sum_k op(A)(row, k) * op(B)(k, col) in fp32 by the whole warp: lane l adds
+// k = l, l + 32, ... with fused multiply-adds, then a butterfly adds the lanes.
+// Every lane returns the sum.
+__device__ __noinline__ float dot_fp32_warp(const RawOps o, int row, int col, int lane) {
     float acc = 0.0f;
-    for (int k = 0; k < o.K; ++k) {
+    for (int k = lane; k < o.K; k += 32) {
         const float a = o.ta_n ? o.A[(int64_t)row * o.lda + k] : o.A[(int64_t)k * o.lda + row];
         const float b = o.tb_n ? o.B[(int64_t)k * o.ldb + col] : o.B[(int64_t)col * o.ldb + k];
         acc = __fmaf_rn(a, b, acc);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
     return acc;
 }
 
-// Redoes the NaN sums of one row of 32 staged accumulator values (columns
-// col0..col0+31 of output row `row`).
-__device__ __noinline__ void redo_nan_row(float *vals, const RawOps o, int M, int N, int row,
-                                          int col0) {
-    if (row >= M) return;
-    for (int j = 0; j < 32 && col0 + j < N; ++j)
-        if (vals[j] != vals[j]) vals[j] = dot_fp32(o, row, col0 + j);
+// Warp-collective: the 32 x 32 block of sums staged at `stg` (row stride ld;
+// lane l's row is row0 + l, columns col0..col0+31) has its NaN (3xTF32) or
+// non-finite (TF32) entries inside M x N recomputed with dot_fp32_warp.
+template <bool THREE>
+__device__ __noinline__ void redo_block(float *stg, int ld, const RawOps o, int M, int N, int row0,
+                                        int col0, int lane) {
+    uint32_t mask = 0;
+    if (row0 + lane < M)
+        for (int jj = 0; jj < 32 && col0 + jj < N; ++jj)
+            if (needs_redo<THREE>(stg[lane * ld + jj])) mask |= 1u << jj;
+    while (true) {
+        const uint32_t lanes = __ballot_sync(0xffffffffu, mask != 0);
+        if (lanes == 0) break;
+        const int src = __ffs(lanes) - 1;
+        const int jj = __ffs(__shfl_sync(0xffffffffu, mask, src)) - 1;
+        const float v = dot_fp32_warp(o, row0 + src, col0 + jj, lane);
+        if (lane == src) {
+            stg[lane * ld + jj] = v;
+            mask &= ~(1u << jj);
+        }
+    }
+    __syncwarp();
+}
+
+// Any NaN or infinity among 32 values (a packed FMA by zero keeps the sum 0
+// unless one is).
+__device__ __forceinline__ bool any_nonfinite32(const float (&v)[32]) {
+    float2 z = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) z = __ffma2_rn(make_float2(v[j], v[j + 1]), make_float2(0.0f, 0.0f), z);
+    const float s = __fadd_rn(z.x, z.y);
+    return s != s;
 }
 
 // In-place split of `n16` 16-byte groups of a shared tile: hi = round(x)
 // written over x, lo = round(x - hi) written to the twin tile (THREE only).
 // The WORKERS split threads stride through the tile together.
-// Returns whether an infinite value was met.
 template <bool THREE>
-__device__ __forceinline__ bool split_tile(uint32_t hi, uint32_t lo, int n16, int ct) {
-    bool inf = false;
+__device__ __forceinline__ void split_tile(uint32_t hi, uint32_t lo, int n16, int ct) {
     for (int i = ct; i < n16; i += WORKERS) {
         float4 v;
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(hi + 16u * i));
-        const float4 h = make_float4(split_hi(v.x, inf), split_hi(v.y, inf), split_hi(v.z, inf),
-                                     split_hi(v.w, inf));
+        const float4 h = make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z),
+                                     tf32_round(v.w));
         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                      :: "r"(hi + 16u * i), "f"(h.x), "f"(h.y), "f"(h.z), "f"(h.w) : "memory");
         if (THREE) {
-            const float4 l = make_float4(split_lo(v.x, h.x), split_lo(v.y, h.y),
-                                         split_lo(v.z, h.z), split_lo(v.w, h.w));
+            const float4 l = make_float4(tf32_round(__fsub_rn(v.x, h.x)),
+                                         tf32_round(__fsub_rn(v.y, h.y)),
+                                         tf32_round(__fsub_rn(v.z, h.z)),
+                                         tf32_round(__fsub_rn(v.w, h.w)));
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                          :: "r"(lo + 16u * i), "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w) : "memory");
         }
     }
-    return inf;
 }
 
 // Split of this thread's row of a raw A tile (TMA-swizzled, rows of BK
@@ -477,9 +479,8 @@ __device__ __forceinline__ bool split_tile(uint32_t hi, uint32_t lo, int n16, in
 // index by bits 1-2 of the row, its 128-byte swizzle (BK_ = 32) by bits 0-2.
 // `taddr` is the warp's lane quarter and column tslot of tensor memory.
 template <bool THREE, int BK_>
-__device__ __forceinline__ bool split_a_to_tmem(uint32_t raw, uint32_t taddr, int q, int half,
+__device__ __forceinline__ void split_a_to_tmem(uint32_t raw, uint32_t taddr, int q, int half,
                                                 int lane) {
-    bool inf = false;
     constexpr int KH = BK_ / 2;                       // k values per thread: 8 or 16
     const int r = q * 32 + lane;
     const uint32_t sw = BK_ == 16 ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
@@ -497,15 +498,14 @@ __device__ __forceinline__ bool split_a_to_tmem(uint32_t raw, uint32_t taddr, in
             const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                hi[4 * c + e] = split_hi(x[e], inf);
-                if (THREE) lo[4 * c + e] = split_lo(x[e], hi[4 * c + e]);
+                hi[4 * c + e] = tf32_round(x[e]);
+                if (THREE) lo[4 * c + e] = tf32_round(__fsub_rn(x[e], hi[4 * c + e]));
             }
         }
         const uint32_t col = (uint32_t)(half * KH + g * 8);
         tmem_st8(taddr + col, hi);
         if (THREE) tmem_st8(taddr + (uint32_t)BK_ + col, lo);
     }
-    return inf;
 }
 
 // WIDE tiles: this thread's row of the raw A tile (128-byte swizzle), split
@@ -513,9 +513,8 @@ __device__ __forceinline__ bool split_a_to_tmem(uint32_t raw, uint32_t taddr, in
 // k); lo = round(x - hi) is stored in the A_lo tile at x's own swizzled
 // position, the layout the shared-memory MMA reads.
 template <int BK_>
-__device__ __forceinline__ bool split_a_hi_lo(uint32_t raw, uint32_t lo_tile, uint32_t taddr, int q,
+__device__ __forceinline__ void split_a_hi_lo(uint32_t raw, uint32_t lo_tile, uint32_t taddr, int q,
                                               int half, int lane) {
-    bool inf = false;
     constexpr int KH = BK_ / 2;                       // k values per thread
     const int r = q * 32 + lane;
     const uint32_t sw = BK_ == 16 ? (uint32_t)((r >> 1) & 3) : (uint32_t)(r & 7);
@@ -534,15 +533,14 @@ __device__ __forceinline__ bool split_a_hi_lo(uint32_t raw, uint32_t lo_tile, ui
             float lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                hi[4 * c + e] = split_hi(x[e], inf);
-                lo[e] = split_lo(x[e], hi[4 * c + e]);
+                hi[4 * c + e] = tf32_round(x[e]);
+                lo[e] = tf32_round(__fsub_rn(x[e], hi[4 * c + e]));
             }
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                          :: "r"(lo_tile + o), "f"(lo[0]), "f"(lo[1]), "f"(lo[2]), "f"(lo[3]) : "memory");
         }
         tmem_st8(taddr + (uint32_t)(half * KH + g * 8), hi);
     }
-    return inf;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -917,22 +915,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int s = (int)(g % K_::STAGES);
                     const uint32_t ph = (uint32_t)(g / K_::STAGES) & 1u;
                     if (!mbar_wait(full_bar(s), ph, lim)) { ok = false; break; }
-                    bool inf = false;
                     if (p.fuse_a) {
                         // A's hi and lo go to tensor memory, where the MMA reads
                         // them: no shared-memory traffic for A in the MMAs
                         const uint32_t slot = tmem + ((uint32_t)(q * 32) << 16) +
                                               (uint32_t)(K_::A_TMEM_COL + s * K_::A_SLOT_COLS);
-                        if (WIDE) inf = split_a_hi_lo<BK>(a_hi(s), a_lo(s), slot, q, half, lane);
-                        else inf = split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
+                        if (WIDE) split_a_hi_lo<BK>(a_hi(s), a_lo(s), slot, q, half, lane);
+                        else split_a_to_tmem<THREE, BK>(a_hi(s), slot, q, half, lane);
                         tmem_st_wait();
                         tc_fence_before();
                     }
-                    if (p.fuse_b)
-                        inf |= split_tile<THREE>(b_hi(s), b_lo(s, b_rows), b_rows * BK * 4 / 16, ct);
-                    // noted before this stage's split arrival, which orders the
-                    // note before the epilogue's read (below)
-                    if (inf) note_inf(p.gen);
+                    if (p.fuse_b) split_tile<THREE>(b_hi(s), b_lo(s, b_rows), b_rows * BK * 4 / 16, ct);
                     if (p.fuse_b || (WIDE && p.fuse_a)) {
                         // generic-proxy stores must be visible to the tensor core's reads
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -946,21 +939,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool ready = mbar_wait(accf_bar(b), (uint32_t)(j / nbuf) & 1u, lim);
             tc_fence_after();
             if (!ready) break;
-            // A whole tile of a call that met an infinite operand value redoes
-            // its NaN sums in fp32 (see g_inf_gen; shared tiles are redone by
-            // the fixup).  Operands split by the pre-pass noted theirs before
-            // this grid started; this CTA's split warps noted theirs before
-            // arriving on a stage's split barrier, so waiting for the piece's
-            // last such barrier orders every note before the read.
-            bool redo = false;
-            if (pc.slot < 0) {
-                if (fused && g > 0) {
-                    const int64_t gl = g - 1;
-                    mbar_wait(conv_bar((int)(gl % K_::STAGES)), (uint32_t)(gl / K_::STAGES) & 1u,
-                              lim);
-                }
-                redo = inf_seen(p.gen);
-            }
             const float alpha = p.alpha, beta = p.beta;
             const int row0 = m0 + (int)rank * BM + q * 32;
             const int rows_here = min(32, p.M - row0);
@@ -970,9 +948,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) +
                                     (uint32_t)(b * K_::NACC * BN + c * 32);
                 tmem_ld32(ta, r);
+                float v[32];
                 if (K_::NACC == 1) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = __uint_as_float(r[jj]);
+                    for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(r[jj]);
                 } else {
                     // 3xTF32 (lo*hi at 0, hi*hi at BN, hi*lo at 2 BN):
                     // hi*hi + (lo*hi + hi*lo); TF32: even + odd k-slices
@@ -988,10 +967,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int jj = 0; jj < 32; ++jj) f[jj] = __fadd_rn(__uint_as_float(r2[jj]), f[jj]);
                     }
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = f[jj];
+                    for (int jj = 0; jj < 32; ++jj) v[jj] = f[jj];
                 }
-                if (redo) redo_nan_row(stg + lane * EPI_LD, p.raw, p.M, p.N, row0 + lane, n0 + c * 32);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) stg[lane * EPI_LD + jj] = v[jj];
+                // a whole tile's NaN (or, in TF32, non-finite) sums are redone in
+                // fp32 (shared tiles' in the fixup)
+                const bool bad = pc.slot < 0 && __any_sync(0xffffffffu, any_nonfinite32(v));
                 __syncwarp();
+                if (bad) redo_block<THREE>(stg, EPI_LD, p.raw, p.M, p.N, row0, n0 + c * 32, lane);
                 const int col = n0 + c * 32 + lane;
                 if (pc.slot >= 0) {
                     // a share of a tile's k range: the raw sum, tile-local
@@ -1067,7 +1051,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int BN, int TM>
 __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
     pdl_wait();   // the main kernel's partial sums are complete and visible
-    const bool redo = inf_seen(p.gen);   // NaN sums redone in fp32 (see g_inf_gen)
     const long long T = p.sk_iters, G = p.sk_ctas;
     const int t = p.sk_tile0 + (int)blockIdx.x;
     const long long first = (long long)blockIdx.x * p.num_kb, last = first + p.num_kb - 1;
@@ -1082,33 +1065,63 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
     // later CTA's range starts inside the tile: slot 2c.
     const int lo_slot = 2 * c_lo + ((long long)c_lo * T / G >= first ? 0 : 1);
     const float4 *part = reinterpret_cast<const float4 *>(p.partial);
+    const int lane = threadIdx.x & 31;
+    // Every lane of a warp runs the same iterations (ELEMS / 4 and the stride
+    // are multiples of 32), so the redo below can be warp-collective.
     for (int e4 = (int)(blockIdx.y * blockDim.x + threadIdx.x); e4 < ELEMS / 4;
          e4 += (int)(gridDim.y * blockDim.x)) {
         const int e = 4 * e4;
         const int r = e / BN, cc = e - r * BN;
         const int row = m0 + r, col = n0 + cc;
-        if (row >= p.M || col >= p.N) continue;
-        float4 v = part[(int64_t)lo_slot * (ELEMS / 4) + e4];
-        // the later partials four at a time: loads first, then the adds in order
-        for (int c = c_lo + 1; c <= c_hi; c += 4) {
-            float4 x[4];
+        const bool valid = row < p.M && col < p.N;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (valid) {
+            v = part[(int64_t)lo_slot * (ELEMS / 4) + e4];
+            // the later partials four at a time: loads first, then the adds in order
+            for (int c = c_lo + 1; c <= c_hi; c += 4) {
+                float4 x[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (c + u <= c_hi) x[u] = part[(int64_t)(2 * (c + u)) * (ELEMS / 4) + e4];
+                for (int u = 0; u < 4; ++u)
+                    if (c + u <= c_hi) x[u] = part[(int64_t)(2 * (c + u)) * (ELEMS / 4) + e4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (c + u > c_hi) break;
-                v.x = __fadd_rn(v.x, x[u].x);
-                v.y = __fadd_rn(v.y, x[u].y);
-                v.z = __fadd_rn(v.z, x[u].z);
-                v.w = __fadd_rn(v.w, x[u].w);
+                for (int u = 0; u < 4; ++u) {
+                    if (c + u > c_hi) break;
+                    v.x = __fadd_rn(v.x, x[u].x);
+                    v.y = __fadd_rn(v.y, x[u].y);
+                    v.z = __fadd_rn(v.z, x[u].z);
+                    v.w = __fadd_rn(v.w, x[u].w);
+                }
             }
         }
-        float vs[4] = {v.x, v.y, v.z, v.w};
-        if (redo) {
-            for (int q = 0; q < 4 && col + q < p.N; ++q)
-                if (vs[q] != vs[q]) vs[q] = dot_fp32(p.raw, row, col + q);
+        // NaN (3xTF32) or non-finite (TF32) sums redone in fp32 by the warp
+        const float2 z = __ffma2_rn(make_float2(v.x, v.y), make_float2(0.0f, 0.0f),
+                                    __fmul2_rn(make_float2(v.z, v.w), make_float2(0.0f, 0.0f)));
+        const float zs = __fadd_rn(z.x, z.y);
+        if (__any_sync(0xffffffffu, zs != zs)) {
+            uint32_t mask = 0;
+            const float vq[4] = {v.x, v.y, v.z, v.w};
+            if (valid)
+                for (int q = 0; q < 4 && col + q < p.N; ++q)
+                    if (p.three ? vq[q] != vq[q] : !(fabsf(vq[q]) < f32_inf())) mask |= 1u << q;
+            while (true) {
+                const uint32_t lanes = __ballot_sync(0xffffffffu, mask != 0);
+                if (lanes == 0) break;
+                const int src = __ffs(lanes) - 1;
+                const int q = __ffs(__shfl_sync(0xffffffffu, mask, src)) - 1;
+                const int srow = __shfl_sync(0xffffffffu, row, src);
+                const int scol = __shfl_sync(0xffffffffu, col, src) + q;
+                const float d = dot_fp32_warp(p.raw, srow, scol, lane);
+                if (lane == src) {
+                    if (q == 0) v.x = d;
+                    else if (q == 1) v.y = d;
+                    else if (q == 2) v.z = d;
+                    else v.w = d;
+                    mask &= ~(1u << q);
+                }
+            }
         }
+        if (!valid) continue;
+        const float vs[4] = {v.x, v.y, v.z, v.w};
         float *dst = p.C + (int64_t)row * p.ldc + col;
         const float a_r = epi_alpha(p.alpha, p.row_scale, row);
 #pragma unroll
@@ -1123,8 +1136,8 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
 
 // ---------------------------------------------------------------- split pre-pass
 // One operand of the split pre-pass: out[r][k] (r < rows, k < Kp, row stride
-// Kp) = op value at (r, k) for k < K, 0 for K <= k < Kp; hi and lo as
-// split_hi / split_lo.  trans: the source is stored k-major
+// Kp) = op value at (r, k) for k < K, 0 for K <= k < Kp; hi = rna_tf32(x),
+// lo = rna_tf32(x - hi).  trans: the source is stored k-major
 // (src[k*ld + r]), else src[r*ld + k]; vec: the source rows are 16-byte
 // aligned (base aligned, ld % 4 == 0).
 struct SplitJob {
@@ -1134,7 +1147,6 @@ struct SplitJob {
     float *hi, *lo;
     int trans, vec;
     int blocks;                 // CTAs of this job
-    unsigned long long gen;     // the call's stamp, noted when an infinity is met
 };
 
 __host__ __device__ inline int split_blocks(int rows, int Kp, bool trans) {
@@ -1145,15 +1157,13 @@ __host__ __device__ inline int split_blocks(int rows, int Kp, bool trans) {
 
 template <bool THREE>
 __device__ __forceinline__ void split_store4(const SplitJob &j, int64_t o, float4 x) {
-    bool inf = false;
-    const float4 h = make_float4(split_hi(x.x, inf), split_hi(x.y, inf), split_hi(x.z, inf),
-                                 split_hi(x.w, inf));
+    const float4 h = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z),
+                                 tf32_round(x.w));
     *reinterpret_cast<float4 *>(j.hi + o) = h;
     if (THREE)
         *reinterpret_cast<float4 *>(j.lo + o) =
-            make_float4(split_lo(x.x, h.x), split_lo(x.y, h.y), split_lo(x.z, h.z),
-                        split_lo(x.w, h.w));
-    if (inf) note_inf(j.gen);
+            make_float4(tf32_round(__fsub_rn(x.x, h.x)), tf32_round(__fsub_rn(x.y, h.y)),
+                        tf32_round(__fsub_rn(x.z, h.z)), tf32_round(__fsub_rn(x.w, h.w)));
 }
 
 // Both operands in one launch: CTAs [0, j0.blocks) do j0, the rest j1.
@@ -1300,8 +1310,7 @@ static bool make_map(CUtensorMap *m, const float *base, int rows, int Kp, int bo
 
 static std::mutex g_tc_mu;
 static uint64_t g_wait_ns = tc::kDefaultWaitNs;
-// Call stamps for tc::g_inf_gen: increasing, never 0 (the word's initial value).
-static std::atomic<unsigned long long> g_call_gen{0};
+
 
 void tc_set_wait_limit(uint64_t ns) {
     std::lock_guard<std::mutex> lk(g_tc_mu);
@@ -1495,11 +1504,9 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     // canonical K-major operands: A as [M][Kp], B as [N][Kp]
     const bool a_trans = !is_notrans(ta);   // A stored K x M
     const bool b_trans = is_notrans(tb);    // B stored K x N
-    const unsigned long long gen = g_call_gen.fetch_add(1, std::memory_order_relaxed) + 1;
     tc::SplitJob ja{}, jb{};
     if (!fuse_a) ja = split_job(A, lda, a_trans, (int)M, (int)K, Kp, a_hi, three ? a_lo : nullptr);
     if (!fuse_b) jb = split_job(B, ldb, b_trans, (int)N, (int)K, Kp, b_hi, three ? b_lo : nullptr);
-    ja.gen = jb.gen = gen;
     launch_split_pair(three, ja, jb, s);
     const bool dep = ja.blocks + jb.blocks > 0;
     int st = last_status();
@@ -1549,7 +1556,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
     p.bias = epi.bias;
     p.act = epi.act;
     p.raw = tc::RawOps{A, B, lda, ldb, is_notrans(ta) ? 1 : 0, is_notrans(tb) ? 1 : 0, (int)K};
-    p.gen = gen;
+    p.three = three ? 1 : 0;
     p.units = p.dp_tiles + (p.tiles_m * p.tiles_n - p.dp_tiles) * nsplit;
     p.dp_units = p.units;
     if (sk_ctas > 0) {

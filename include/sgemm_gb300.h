@@ -46,11 +46,13 @@
  * arithmetic: a sum that meets an infinity is that infinity (sign of the
  * product), or NaN where an infinity meets zero or one of the other sign; NaN
  * propagates.  The tensor-core paths split each value into two TF32 parts,
- * and their cross products can turn such an infinite sum into NaN; so a call
- * whose operands hold an infinity recomputes every output that came out NaN
- * with fp32 fused multiply-adds in ascending k, straight from A and B (the
- * FFMA path's arithmetic).  Finite values keep finite parts, also above
- * (2 - 2^-11) * 2^127 where rounding to TF32 would overflow.
+ * whose cross products turn a sum that meets an infinity, or a finite value
+ * above (2 - 2^-11) * 2^127 (which rounds to an infinite TF32 part), into
+ * NaN; so every output that comes out NaN (3xTF32) or not finite (TF32) is
+ * recomputed in fp32 straight from A and B, by one warp with fused
+ * multiply-adds.  A sum whose true value is infinite or NaN comes out of the
+ * recomputation the same.  Calls without such values pay one check per
+ * output; calls whose outputs are mostly non-finite run much slower.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H

@@ -9,12 +9,14 @@ oracle.compare_ieee: the same class where the reference is not finite,
 the fp32 bound elsewhere.  The FFMA path without split-K must also equal the
 oracle's fp32 ascending-k evaluation bit for bit (NaN for NaN).
 
-On the tensor cores the 3xTF32 cross terms multiply an infinity by its
-partner's low part, which may be zero or of the other sign; the library
-redoes such NaN sums in fp32, and these cases make it do so: values whose
-low part is zero (1.0, 0.5), zeros, and both signs.  Finite values above
-(2 - 2^-11) 2^127 round to infinity in TF32; their split must stay finite,
-checked with FLT_MAX and -3.4025e38 against small partners.
+On the tensor cores the TF32 parts of an infinity (and of a finite value
+above (2 - 2^-11) 2^127, which rounds to an infinite TF32 part) turn the sums
+they enter into NaN; the library recomputes such outputs in fp32, and these
+cases make it do so: partners whose low part is zero (1.0, 0.5), zeros, both
+signs, +inf and -inf in one sum, and FLT_MAX and -3.4025e38 against small
+partners (finite results).  Whole tiles are fixed in the main kernel, shared
+(stream-K) tiles in the fixup kernel, and the SM-pair kernel's tiles by each
+CTA for its rows.
 """
 import numpy as np
 import pytest
@@ -130,8 +132,9 @@ def test_nonfinite_inputs_follow_ieee(oracle_mod, ta, tb, M, N, K, path, split, 
 
 
 def test_clean_call_after_nonfinite_call(oracle_mod):
-    """A call without infinities right after one with them is unaffected
-    (and correct), on the same stream and shapes."""
+    """A call without infinities right after one with them is correct, on
+    the same stream and shapes (nothing of the first call's recomputation
+    carries over)."""
     M, N, K = 1024, 1024, 1024
     opA, opB = planted(M, N, K, 91)
     run("N", "N", M, N, K, opA, opB, 1.0, 0.0, None, sg.PATH_3XTF32, 0)
