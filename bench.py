@@ -664,11 +664,13 @@ def only_path(args):
 
     sgbuild.build()
     sg.load()
-    w = gi.WORKLOADS[WORKLOAD]
-    A, B, _ = gi.make_inputs(w)
+    w = gi.WORKLOADS[args.workload or WORKLOAD]
+    A, B, C = gi.make_inputs(w)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
-    dC = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
-    pid = {"ffma": sg.PATH_FFMA, "3xtf32": sg.PATH_3XTF32, "tf32": sg.PATH_TF32}[args.only_path]
+    dC = (torch.from_numpy(C).cuda() if C is not None
+          else torch.empty((w.M, w.N), dtype=torch.float32, device="cuda"))
+    pid = {"auto": sg.PATH_AUTO, "ffma": sg.PATH_FFMA, "3xtf32": sg.PATH_3XTF32,
+           "tf32": sg.PATH_TF32}[args.only_path]
     s = torch.cuda.current_stream()
     ev = []
     for i in range(args.warmup + args.steps):
@@ -700,9 +702,11 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--paths", default="ffma,3xtf32,tf32",
                     help="comma list of paths to time beside the main call")
-    ap.add_argument("--only-path", default=None, choices=["ffma", "3xtf32", "tf32"],
+    ap.add_argument("--only-path", default=None, choices=["auto", "ffma", "3xtf32", "tf32"],
                     help="profiling mode: run only W + K calls of this path on the "
                          "workload (no baseline, e2e or oracle) and print their timing")
+    ap.add_argument("--workload", default=None, choices=list(gi.WORKLOADS),
+                    help="profiling mode: the workload (default: the benchmark's)")
     ap.add_argument("--no-check", action="store_true", help="skip the oracle sample check")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (every workload through sgemm)")
