@@ -360,6 +360,7 @@ __device__ __forceinline__ bool tx_wait(uint32_t bar, uint32_t ph, uint64_t limi
 template <int SM>
 __global__ void __launch_bounds__(TX_THREADS, 2)
     gemv_axpy_tma_kernel(const __grid_constant__ CUtensorMap big_map, const Params p) {
+    static_assert(SM % 4 == 0, "Small is read four values (two pairs) at a time");
     pdl_trigger();   // the K-split sum may launch; it waits for this grid
     extern __shared__ __align__(16) float tx_smem[];
     // the ring on a 128-byte boundary (TMA destination), as an element offset
@@ -417,9 +418,15 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     }
 
     // ---------------------------------------------------- consumers (warps 0..TX_CW-1)
-    float2 acc[SM][2];
+    // packed pairs along s: acc[t][e] = (out(2t, p_e), out(2t + 1, p_e)) for the
+    // lane's 4 columns p_e, so that Small's pairs come straight from its 16-byte
+    // loads and only Big's 4 values are duplicated per k (measured on GB300:
+    // ~5 % faster than pairs along p, which duplicated all of Small's values)
+    float2 acc[SM / 2][4];
 #pragma unroll
-    for (int s = 0; s < SM; ++s) acc[s][0] = acc[s][1] = make_float2(0.0f, 0.0f);
+    for (int t = 0; t < SM / 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[t][e] = make_float2(0.0f, 0.0f);
     // A failed wait stops the compute and the empty-slot arrivals (the
     // producer then times out too), but never a barrier: every consumer
     // thread runs the same sequence of named-barrier syncs.
@@ -443,18 +450,17 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
                 if (k >= k1) break;
                 const float4 b = *reinterpret_cast<const float4 *>(rows + r * AX_P + lane * 4);
                 const float *a = smt + (k - kc) * SM;  // the same address in every lane
-                const float2 b01 = make_float2(b.x, b.y);
-                const float2 b23 = make_float2(b.z, b.w);
+                const float2 bb[4] = {make_float2(b.x, b.x), make_float2(b.y, b.y),
+                                      make_float2(b.z, b.z), make_float2(b.w, b.w)};
                 // Small four values at a time: few registers beside the accumulators
 #pragma unroll
                 for (int s = 0; s < SM; s += 4) {
                     const float4 v = *reinterpret_cast<const float4 *>(a + s);
-                    const float av[4] = {v.x, v.y, v.z, v.w};
+                    const float2 a01 = make_float2(v.x, v.y), a23 = make_float2(v.z, v.w);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 a2 = make_float2(av[e], av[e]);
-                        acc[s + e][0] = __ffma2_rn(a2, b01, acc[s + e][0]);
-                        acc[s + e][1] = __ffma2_rn(a2, b23, acc[s + e][1]);
+                        acc[s / 2][e] = __ffma2_rn(a01, bb[e], acc[s / 2][e]);
+                        acc[s / 2 + 1][e] = __ffma2_rn(a23, bb[e], acc[s / 2 + 1][e]);
                     }
                 }
             }
@@ -471,9 +477,12 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     if (gave_up) return;
     float *red = ring;                                  // [TX_CW][SM][AX_P]
 #pragma unroll
-    for (int s = 0; s < SM; ++s)
-        *reinterpret_cast<float4 *>(red + (warp * SM + s) * AX_P + lane * 4) =
-            make_float4(acc[s][0].x, acc[s][0].y, acc[s][1].x, acc[s][1].y);
+    for (int t = 0; t < SM / 2; ++t) {
+        *reinterpret_cast<float4 *>(red + (warp * SM + 2 * t) * AX_P + lane * 4) =
+            make_float4(acc[t][0].x, acc[t][1].x, acc[t][2].x, acc[t][3].x);
+        *reinterpret_cast<float4 *>(red + (warp * SM + 2 * t + 1) * AX_P + lane * 4) =
+            make_float4(acc[t][0].y, acc[t][1].y, acc[t][2].y, acc[t][3].y);
+    }
     asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
     for (int o = threadIdx.x; o < SM * AX_P; o += TX_CT) {
         const int s = o / AX_P, q = o % AX_P;
