@@ -173,6 +173,31 @@ constexpr int ax_smem_floats() { return WARPS * SM * AX_P + AX_KC * SM; }
 // PER, sits at (slow, fast) = (t / major, t % major); both advance by NT
 // with one carry.  Every load is issued before the first store: a chunk
 // costs one L2 round trip, not one per element of the thread.
+// As stage_small, with 4-byte cp.async copies straight into shared memory
+// (no registers; zero-filled for s >= S); the caller commits and waits.
+template <int SM, int NT, int PER>
+__device__ __forceinline__ void stage_small_async(const Params &p, float *smt, int kc, int kn,
+                                                  int tid) {
+    const bool s_fast = p.small_ss == 1;
+    const int major = s_fast ? SM : kn;
+    const int dq = NT / major, dr = NT % major;
+    const int total = kn * SM;
+    int q = tid / major, r = tid % major;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int s = s_fast ? r : q, kk = s_fast ? q : r;
+        if (tid + j * NT < total) {
+            const bool in = s < p.S;
+            const float *src = in ? p.small + (int64_t)s * p.small_ss + (int64_t)(kc + kk) * p.small_sk
+                                  : p.small;
+            cp_async_4(smem_u32(smt + kk * SM + s), src, in ? 4 : 0);
+        }
+        q += dq;
+        r += dr;
+        if (r >= major) { r -= major; ++q; }
+    }
+}
+
 template <int SM, int NT, int PER>
 __device__ __forceinline__ void stage_small(const Params &p, float *smt, int kc, int kn,
                                             int tid) {
@@ -297,7 +322,12 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_axpy_kernel(const Params p) {
 // HBM speed.  This variant moves Big through shared memory instead: one
 // producer warp streams boxes of TX_KS rows x 128 columns of Big with TMA into
 // a ring of TX_ST stages (tensor map over Big: p innermost, row stride
-// big_ld), and TX_CW consumer warps read their rows from there.  Warp w takes
+// big_ld), and TX_CW consumer warps read their rows from there.  Small comes
+// in chunks of TX_KC k, double-buffered in shared memory by 4-byte cp.async
+// copies, so that the next chunk's copies are in flight while this one is
+// consumed (measured: 16 x 16384 x 8192 NN 22.6 -> 24.1 TFLOP/s against
+// staging each chunk through registers between two barriers; the ring gave
+// up its sixth stage to keep 2 CTAs per SM).  Warp w takes
 // rows 4w .. 4w+3 of each stage; the sums per output stay in k order within
 // a warp and the warps are added in warp order, as in the kernel above.  Eight
 // warps per CTA (7 consumers + the producer) keep 2 CTAs per SM at 128
@@ -307,7 +337,7 @@ constexpr int TX_CW = 7;               // consumer warps
 constexpr int TX_CT = TX_CW * 32;      // consumer threads
 constexpr int TX_KS = 4 * TX_CW;       // rows of Big per stage: 4 per consumer warp
 constexpr int TX_KC = 9 * TX_KS;       // rows per Small chunk (9 stages)
-constexpr int TX_ST = 6;               // stages in flight
+constexpr int TX_ST = 5;               // stages in flight
 constexpr int TX_THREADS = TX_CT + 32;     // + the producer warp
 constexpr int TX_STAGE_FLOATS = TX_KS * AX_P;
 
@@ -315,7 +345,7 @@ template <int SM>
 constexpr int tx_smem_bytes() {
     // ring, Small chunk, barriers (the reduction reuses the ring), alignment
     // slack: two CTAs per SM
-    return (TX_ST * TX_STAGE_FLOATS + TX_KC * SM) * 4 + 2 * TX_ST * 8 + 128;
+    return (TX_ST * TX_STAGE_FLOATS + 2 * TX_KC * SM) * 4 + 2 * TX_ST * 8 + 128;
 }
 
 __device__ __forceinline__ uint32_t tx_su32(const void *p) {
@@ -366,8 +396,8 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     // the ring on a 128-byte boundary (TMA destination), as an element offset
     // from the shared array so that every access stays a shared-memory one
     float *ring = tx_smem + (((128u - (tx_su32(tx_smem) & 127u)) & 127u) >> 2);
-    float *smt = ring + TX_ST * TX_STAGE_FLOATS;        // Small chunk, [TX_KC][SM]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smt + TX_KC * SM);
+    float *smt0 = ring + TX_ST * TX_STAGE_FLOATS;       // Small chunks, 2 x [TX_KC][SM]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smt0 + 2 * TX_KC * SM);
     const uint32_t bar0 = tx_su32(bars);
     auto full = [&](int st) { return bar0 + 8u * st; };
     auto empty = [&](int st) { return bar0 + 8u * (TX_ST + st); };
@@ -432,11 +462,26 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
     // thread runs the same sequence of named-barrier syncs.
     bool ok = true;
     int i = 0;                                          // next stage
-    for (int kc = k0; kc < k1; kc += TX_KC) {
+    constexpr int SPER = (TX_KC * SM + TX_CT - 1) / TX_CT;
+    const int nchunks = (k1 - k0 + TX_KC - 1) / TX_KC;
+    if (nchunks > 0)
+        stage_small_async<SM, TX_CT, SPER>(p, smt0, k0, min(TX_KC, k1 - k0), threadIdx.x);
+    cp_async_commit();
+    for (int c = 0; c < nchunks; ++c) {
+        const int kc = k0 + c * TX_KC;
         const int kn = min(TX_KC, k1 - kc);
-        asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");   // previous chunk consumed
-        stage_small<SM, TX_CT, (TX_KC * SM + TX_CT - 1) / TX_CT>(p, smt, kc, kn, threadIdx.x);
-        asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");
+        const float *smt = smt0 + (c & 1) * (TX_KC * SM);
+        if (c + 1 < nchunks) {
+            // the next chunk's copies fly while this one is consumed; its buffer
+            // was released by the barrier that ended chunk c - 1
+            stage_small_async<SM, TX_CT, SPER>(p, smt0 + ((c + 1) & 1) * (TX_KC * SM), kc + TX_KC,
+                                               min(TX_KC, k1 - kc - TX_KC), threadIdx.x);
+            cp_async_commit();
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
+        }
+        asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");   // chunk c in shared memory
         // the stages of this chunk (TX_KC is a multiple of TX_KS)
         for (; i < nst && k0 + i * TX_KS < kc + kn; ++i) {
             const int st = i % TX_ST;
@@ -467,6 +512,7 @@ __global__ void __launch_bounds__(TX_THREADS, 2)
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(empty(st)) : "memory");
         }
+        asm volatile("bar.sync 1, %0;" :: "r"(TX_CT) : "memory");   // chunk c's buffer free
     }
     // all consumers are past the ring before it is reused for the reduction.
     // If any consumer's wait ran out, copies the producer issued may still
