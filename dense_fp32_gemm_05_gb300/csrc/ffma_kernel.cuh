@@ -26,8 +26,11 @@
 //     bits 2-3 of k) keeps the transposing stores and the 16-byte loads free
 //     of bank conflicts ("CuTe-ly writing an SM86 SGEMM", section "swizzles &
 //     shared memory");
-//   * two shared-memory stages: the copy of k-tile t+1 is in flight while
-//     k-tile t is multiplied ("Matmul II", section 7, t3's double buffer);
+//   * three shared-memory stages: the cp.async copies of k-tiles t+1 and t+2
+//     are in flight while k-tile t is multiplied (a register-staged operand
+//     runs one k-tile ahead); "Matmul II", section 7, t3's double buffer with
+//     one stage more (measured on GB300, 4096^3: NN 62.2 -> 62.7, TN 64.2 ->
+//     64.6 TFLOP/s, bit-identical);
 //   * fused alpha/beta epilogue with 16-byte stores where C allows.
 //
 // Work decomposition (data-parallel tiles + "stream-K" remainder): tiles are
@@ -302,26 +305,30 @@ __device__ __forceinline__ void run_share(const Params &p, float (*sA)[BK * BM],
     };
 
     issue_async(j0, 0);
+    if (nkt > 1) issue_async(j0 + 1, 1);
+    else cp_async_commit();
     load_half(j0, H_0{});
     park_half(0, H_0{});
     load_half(j0, H_2{});
     park_half(0, H_2{});
-    cp_async_wait_all();
+    cp_async_wait_group<1>();
     __syncthreads();
 
+    int stage = 0;
     for (int it = 0; it < nkt; ++it) {
-        const int stage = it & 1;
+        const int nxt = stage == 2 ? 0 : stage + 1;
+        const int nxt2 = nxt == 2 ? 0 : nxt + 1;
         const bool has_next = it + 1 < nkt;
-        if (has_next) {
-            issue_async(j0 + it + 1, stage ^ 1);
-            load_half(j0 + it + 1, H_0{});
-        }
+        // the stage two ahead was last read in the previous k-tile (barrier passed)
+        if (it + 2 < nkt) issue_async(j0 + it + 2, nxt2);
+        else cp_async_commit();
+        if (has_next) load_half(j0 + it + 1, H_0{});
         const float *As = sA[stage];
         const float *Bs = sB[stage];
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             if (k == BK / 2 && has_next) {
-                park_half(stage ^ 1, H_0{});
+                park_half(nxt, H_0{});
                 load_half(j0 + it + 1, H_2{});
             }
             const int s = ((k >> 2) & 3) << 3;
@@ -355,11 +362,10 @@ __device__ __forceinline__ void run_share(const Params &p, float (*sA)[BK * BM],
                 }
             }
         }
-        if (has_next) {
-            park_half(stage ^ 1, H_2{});
-            cp_async_wait_all();
-        }
+        if (has_next) park_half(nxt, H_2{});
+        cp_async_wait_group<1>();
         __syncthreads();
+        stage = nxt;
     }
 
     if (nkt != p.kt) {
@@ -393,8 +399,8 @@ __device__ __forceinline__ void run_share(const Params &p, float (*sA)[BK * BM],
 //      dimensions are multiples of 4, so 16-byte loads/copies are legal.
 template <bool A_KMAJOR, bool B_KMAJOR, bool VEC>
 __global__ void __launch_bounds__(THREADS, 2) ffma_gemm_kernel(const Params p) {
-    __shared__ __align__(16) float sA[2][BK * BM];
-    __shared__ __align__(16) float sB[2][BK * BN];
+    __shared__ __align__(16) float sA[3][BK * BM];
+    __shared__ __align__(16) float sB[3][BK * BN];
     pdl_trigger();   // the stream-K fixup may launch; it waits for this grid
     if ((int)blockIdx.x < p.dp_tiles) {
         run_share<A_KMAJOR, B_KMAJOR, VEC>(p, sA, sB, blockIdx.x, 0, p.kt, 0);
