@@ -55,7 +55,21 @@ struct Plan {
     int pair = 0;         // tensor cores: 256-row tiles on a pair of SMs (cta_group::2)
     int tc_sk = 0;        // tensor cores: stream-K CTAs sharing all k-block iterations (0: off)
     int tc_sk_tail = 0;   // tensor cores: the tiles after the last full wave shared by all CTAs
+    int small = 0;        // FFMA: the one-launch small-problem kernel (16 x 16 tiles)
 };
+
+// The small-problem FFMA kernel takes problems of at most kSmallFlops
+// (2 M N K), K <= kSmallMaxK and at most kSmallMaxTiles tiles of 16 x 16
+// when the path is chosen automatically, or forced to FFMA without a split.
+// Measured on GB300 (per call, L2 flushed; small kernel against the
+// tensor-core path): 128^3 8.9 / 13.0 us, 256^3 10.9 / 17.1, 384^3 19.1 /
+// 21.2, 448^3 27.3 / 23.2; 512 x 512 x 128 15.0 / 15.0.  Long K or many
+// tiles lose (one CTA per tile, each 128-k chunk waits for its copies):
+// 256 x 256 x 1024 29.3 / 21.2, 128 x 128 x 2048 49.8 / 21.2, 1024 x 1024 x
+// 32 23.3 / 11.9.
+constexpr double kSmallFlops = 1.2e8;
+constexpr int64_t kSmallMaxK = 512;
+constexpr int64_t kSmallMaxTiles = 1024;
 
 // Chooses path, tile, split and vectorisation.  `path`/`split` 0 = auto.
 inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -84,6 +98,24 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         pl.tile_n = 0;
         pl.split = 1;
         pl.vector = (a_al && b_al && lda % 4 == 0 && ldb % 4 == 0) ? 1 : 0;
+        *out = pl;
+        return 0;
+    }
+    const bool small = 2.0 * (double)M * (double)N * (double)K <= kSmallFlops && K <= kSmallMaxK &&
+                       ((M + 15) / 16) * ((N + 15) / 16) <= kSmallMaxTiles;
+    if ((path == SGEMM_PATH_AUTO || path == SGEMM_PATH_FFMA) && small && split <= 1) {
+        // One launch of 16 x 16 tiles, every output summed in ascending k
+        // (ffma_small.cuh): below the crossover the fixed costs of the
+        // tile kernels (their launches, fill and, on the tensor cores, the
+        // split pre-pass and the fixup) outweigh their throughput.
+        pl.path = SGEMM_PATH_FFMA;
+        pl.small = 1;
+        pl.tile_m = pl.tile_n = 16;
+        pl.split = 1;
+        pl.dp_tiles = (int)(((M + 15) / 16) * ((N + 15) / 16));
+        pl.ctas = 0;
+        pl.vector = 0;
+        pl.c_vector = 0;
         *out = pl;
         return 0;
     }

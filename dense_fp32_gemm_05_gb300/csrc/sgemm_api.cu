@@ -14,6 +14,7 @@
 
 #include "../../include/sgemm_gb300.h"
 #include "ffma_kernel.cuh"
+#include "ffma_small.cuh"
 #include "plan.h"
 #include "gemv.h"
 #include "tc_gemm.h"
@@ -184,9 +185,42 @@ static int launch_ffma(const ffma::Params &p, char ta, char tb, bool vec, cudaSt
     return launch_status();
 }
 
+template <bool AK, bool BK_>
+static void launch_ffma_small_t(const ffma_small::Params &p, unsigned tiles, cudaStream_t s) {
+    count_launch();
+    ffma_small::ffma_small_kernel<AK, BK_><<<tiles, ffma_small::THREADS, 0, s>>>(p);
+}
+
+// The small-problem kernel: one launch, one CTA per 16 x 16 tile.
+static int run_ffma_small(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,
+                          const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                          float *C, int64_t ldc, cudaStream_t s, const Epilogue &epi) {
+    ffma_small::Params p{};
+    p.A = A; p.B = B; p.C = C;
+    p.lda = lda; p.ldb = ldb; p.ldc = ldc;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.alpha = alpha; p.beta = beta;
+    p.tiles_n = (int)((N + ffma_small::TN - 1) / ffma_small::TN);
+    p.row_scale = epi.row_scale;
+    p.bias = epi.bias;
+    p.act = epi.act;
+    const int64_t tiles = ((M + ffma_small::TM - 1) / ffma_small::TM) * p.tiles_n;
+    if (tiles > INT32_MAX) return SGEMM_ERR_UNSUPPORTED;
+    const bool ak = is_notrans(ta), bk = !is_notrans(tb);
+    timing_mark(s, true);
+    if (ak && bk) launch_ffma_small_t<true, true>(p, (unsigned)tiles, s);
+    else if (ak) launch_ffma_small_t<true, false>(p, (unsigned)tiles, s);
+    else if (bk) launch_ffma_small_t<false, true>(p, (unsigned)tiles, s);
+    else launch_ffma_small_t<false, false>(p, (unsigned)tiles, s);
+    timing_mark(s, false);
+    return launch_status();
+}
+
 static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K,
                     float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
                     float beta, float *C, int64_t ldc, cudaStream_t s, const Epilogue &epi) {
+    if (pl.small)
+        return run_ffma_small(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, epi);
     ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi);
     const bool partials = ffma_has_partials(p);
     if (partials) {
@@ -344,7 +378,7 @@ extern "C" int sgemm_plan_detail(char transA, char transB, int64_t M, int64_t N,
         info.sk_ctas = v.sk ? pl.tc_sk : 0;
         info.sk_tail = v.sk_tail;
     } else if (pl.path == SGEMM_PATH_FFMA) {
-        info.k_block = ffma::BK;
+        info.k_block = pl.small ? ffma_small::KC : ffma::BK;
     }
     *out = info;
     return SGEMM_OK;
@@ -514,6 +548,9 @@ extern "C" int sgemm_ffma_static_scratch(char transA, char transB, int64_t M, in
     st = make_plan(transA, transB, M, N, K, lda, ldb, ldc, aligned16(A), aligned16(B),
                    aligned16(C), SGEMM_PATH_FFMA, split, d->sms, &pl);
     if (st != SGEMM_OK) return st;
+    if (pl.small)   // one launch, no partial sums
+        return run_ffma_small(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s,
+                              Epilogue{});
     ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
     bool partials = ffma_has_partials(p);
     if (partials && 2LL * p.sk_ctas > kStaticPartialTiles) {

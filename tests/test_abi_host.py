@@ -127,8 +127,13 @@ def test_plan_auto_path_choice(lib):
     # odd leading dimensions do not matter to the tensor-core path (pre-pass)
     st, p = sg.sgemm_plan("T", "T", 4095, 3073, 1537, 4095, 1537, 3073)
     assert st == 0 and p["path"] == sg.PATH_3XTF32
-    # small problems too, as long as K >= 32
-    for shp in [(256, 256, 256), (128, 128, 128), (17, 17, 32), (128, 128, 2048)]:
+    # small problems run the one-launch 16 x 16 FFMA kernel ...
+    for shp in [(256, 256, 256), (128, 128, 128), (17, 17, 32), (384, 384, 384), (2048, 32, 512)]:
+        st, p = sg.sgemm_plan("N", "N", *shp, shp[2], shp[1], shp[1])
+        assert st == 0 and p["path"] == sg.PATH_FFMA and p["tile_m"] == p["tile_n"] == 16, shp
+        assert p["split"] == 1 and p["ctas"] == ((shp[0] + 15) // 16) * ((shp[1] + 15) // 16)
+    # ... but long K, many tiles or more flops go to the tensor cores when K >= 32
+    for shp in [(128, 128, 2048), (256, 256, 1024), (1024, 1024, 32), (448, 448, 448)]:
         st, p = sg.sgemm_plan("N", "N", *shp, shp[2], shp[1], shp[1])
         assert st == 0 and p["path"] == sg.PATH_3XTF32, shp
     # short K stays on the CUDA cores
@@ -228,9 +233,12 @@ def test_plan_ffma_stream_k_tail(lib):
 
 def test_plan_split_k_for_small_grids(lib):
     F = sg.PATH_FFMA
-    # 256^3: 4 tiles for 304 CTA slots -> the K loop is split
+    # 256 x 256 x 2048: 4 tiles for 304 CTA slots -> the K loop is split
+    st, p = sg.sgemm_plan("N", "N", 256, 256, 2048, 2048, 256, 256, num_sms=152, path=F)
+    assert st == 0 and p["split"] > 1 and p["tile_m"] == 128
+    # 256^3 forced to FFMA without a split: the one-launch small kernel
     st, p = sg.sgemm_plan("N", "N", 256, 256, 256, 256, 256, 256, num_sms=152, path=F)
-    assert st == 0 and p["split"] > 1
+    assert st == 0 and p["split"] == 1 and p["tile_m"] == p["tile_n"] == 16
     # 16384 x 64 x 8192 skinny on the FFMA path: 128 tiles, long K -> split
     st, p = sg.sgemm_plan("N", "T", 16384, 64, 8192, 8192, 8192, 64, num_sms=152,
                           path=sg.PATH_FFMA)
@@ -255,7 +263,7 @@ def test_plan_thin_problems_take_the_gemv_path(lib):
     # large operand K-contiguous (weights stored [N][K]) and S > 4: the
     # tensor cores are ahead there
     for (ta, tb, M, N, K) in [("N", "T", 16, 16384, 8192), ("N", "T", 8, 4096, 4096),
-                              ("N", "N", 16384, 8, 8192), ("N", "T", 5, 4096, 32)]:
+                              ("N", "N", 16384, 8, 8192), ("N", "T", 5, 4096, 1024)]:
         lda = K if ta == "N" else M
         ldb = N if tb == "N" else K
         st, p = sg.sgemm_plan(ta, tb, M, N, K, lda, ldb, N)
@@ -331,3 +339,20 @@ def test_tf32_rate_probe_argument_errors(lib):
     assert lib.sgemm_probe_tf32_rate(10, ctypes.byref(v)) == -1
     assert lib.sgemm_probe_tf32_rate(1 << 21, ctypes.byref(v)) == -1
     assert lib.sgemm_probe_tf32_rate(4096, None) == -2
+
+
+def test_small_kernel_selector_boundaries(lib):
+    """The rule's edges, on the CPU side of the plan: 2MNK <= 1.2e8, K <= 512
+    and at most 1024 tiles of 16 x 16 take the small kernel; a forced split
+    or any edge crossed takes the tile kernels."""
+    def small(M, N, K, path=sg.PATH_AUTO, split=0):
+        st, info = sg.sgemm_plan_detail("N", "N", M, N, K, K, N, N, 1, 1, 1, path, split, 152)
+        assert st == 0
+        return info["tile_m"] == 16
+    assert small(48, 48, 512) and not small(48, 48, 513)
+    assert small(512, 512, 64) and not small(512, 528, 64)        # 1024 / 1056 tiles
+    assert small(384, 384, 384) and not small(400, 400, 400)      # 1.13e8 / 1.28e8 flops
+    assert small(256, 256, 256, sg.PATH_FFMA, 1)
+    assert not small(256, 256, 256, sg.PATH_FFMA, 2)              # forced split-K
+    assert not small(256, 256, 256, sg.PATH_3XTF32)               # forced tensor cores
+    assert not small(8, 256, 256)                                 # thin: GEMV

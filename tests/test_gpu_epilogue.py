@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 
 # (name, path, split, transA, transB, M, N, K): each reaches one kernel variant
 CASES = [
-    ("ffma_whole", sg.PATH_FFMA, 1, "N", "N", 300, 260, 200),
+    ("ffma_small", sg.PATH_FFMA, 1, "N", "N", 300, 260, 200),
+    ("ffma_whole", sg.PATH_FFMA, 1, "N", "T", 300, 260, 700),
     ("ffma_stream_k", sg.PATH_FFMA, 0, "T", "N", 256, 256, 1024),
     ("tc_fused_nn", sg.PATH_3XTF32, 0, "N", "N", 300, 260, 200),
     ("tc_fused_nt", sg.PATH_3XTF32, 0, "N", "T", 200, 136, 300),

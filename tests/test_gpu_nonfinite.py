@@ -97,6 +97,7 @@ CASES = [
     ("N", "N", 1024, 1024, 1024, sg.PATH_3XTF32, 0, "A in TMEM, stream-K + fixup"),
     ("T", "T", 300, 260, 700, sg.PATH_TF32, 0, "single-pass TF32"),
     ("N", "N", 300, 260, 700, sg.PATH_FFMA, 1, "FFMA, whole tiles"),
+    ("T", "T", 100, 77, 300, sg.PATH_AUTO, 0, "FFMA, small-problem kernel"),
     ("T", "N", 300, 260, 700, sg.PATH_FFMA, 3, "FFMA, split-K"),
     ("N", "T", 8, 700, 500, sg.PATH_GEMV, 0, "thin problem, dot form"),
     ("T", "N", 700, 8, 500, sg.PATH_GEMV, 0, "thin problem, axpy form"),

@@ -125,6 +125,7 @@ def test_small_integers_exact(path, ta, tb, misalign):
     (129, 131, 1000, -1.5, 0.5, (3, 1, 2), (0, 0, 0)),
     (256, 128, 64, 1.0, 1.0, (0, 0, 0), (0, 0, 0)),
     (77, 300, 33, 0.75, -2.0, (1, 0, 5), (1, 2, 3)),
+    (520, 300, 700, 1.0, 0.5, (2, 3, 1), (3, 1, 2)),
 ])
 def test_ffma_bitwise_equals_sequential_oracle(oracle_mod, ta, tb, M, N, K, alpha, beta, pad, off):
     opA = gi.random_matrix(11, M, K, dist="normal")
