@@ -101,6 +101,57 @@ def test_identity_and_permutation_exact(path, ta, tb):
     assert st == 0 and same_or_split_exact(out, X[:, sigma], path)
 
 
+RANK1_SHAPES = [(300, 260, 200), (1000, 900, 700)]   # small-problem kernel / tile kernels
+
+
+@pytest.mark.parametrize("path", ACCURATE_PATHS)
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("M,N,K", RANK1_SHAPES)
+def test_rank_one_closed_form_exact(path, ta, tb, M, N, K):
+    """A(i, k) = u_i, B(k, j) = v_j with small integers: C(i, j) = K u_i v_j,
+    exact in fp32 (every partial sum is an integer below 2^24) and in TF32
+    (integers below 2^11 have no lo part)."""
+    rng = np.random.default_rng(17)
+    u = rng.integers(-8, 9, M).astype(np.float32)
+    v = rng.integers(-8, 9, N).astype(np.float32)
+    opA = np.repeat(u[:, None], K, axis=1)
+    opB = np.repeat(v[None, :], K, axis=0)
+    st, out = gh.run(ta, tb, M, N, K, 1.0, stored(opA, ta), ld_of(stored(opA, ta)), stored(opB, tb),
+                     ld_of(stored(opB, tb)), 0.0, None, N, path=path)
+    assert st == 0
+    want = (K * np.outer(u.astype(np.int64), v.astype(np.int64))).astype(np.float64)
+    assert np.array_equal(out.astype(np.float64), want)
+
+
+FLIP = {"N": "T", "T": "N"}
+
+
+@pytest.mark.parametrize("path,split", [(sg.PATH_FFMA, 1), (sg.PATH_3XTF32, 0)])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("M,N,K", [(300, 260, 200), (1000, 900, 700)])
+def test_transpose_symmetry(oracle_mod, path, split, ta, tb, M, N, K):
+    """(op(A) op(B))^T = op(B)^T op(A)^T: the same stored arrays through the
+    swapped, flag-flipped call give C^T.  FFMA without a split sums every
+    output in ascending k on both sides (and a*b = b*a), so the two agree bit
+    for bit; 3xTF32 runs other tiles on the swapped problem and is held to
+    the bound."""
+    opA = gi.random_matrix(41, M, K, dist="normal")
+    opB = gi.random_matrix(42, K, N, dist="normal")
+    A, B = stored(opA, ta), stored(opB, tb)
+    st, c1 = gh.run(ta, tb, M, N, K, 1.0, A, ld_of(A), B, ld_of(B), 0.0, None, N, path=path,
+                    split=split)
+    assert st == 0
+    # op(B)^T is B read with the flipped flag, and likewise A
+    st, c2 = gh.run(FLIP[tb], FLIP[ta], N, M, K, 1.0, B, ld_of(B), A, ld_of(A), 0.0, None, M,
+                    path=path, split=split)
+    assert st == 0
+    if path == sg.PATH_FFMA:
+        assert np.array_equal(c2.T.view(np.uint32), c1.view(np.uint32))
+    else:
+        oracle_check(oracle_mod, FLIP[tb], FLIP[ta], N, M, K, 1.0, B, ld_of(B), A, ld_of(A), 0.0,
+                     None, c2)
+
+
 @pytest.mark.parametrize("path", ACCURATE_PATHS)
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 @pytest.mark.parametrize("misalign", [False, True])
