@@ -783,8 +783,9 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
     const Geometry g = geometry(ta, tb, M, N, K, sms);
     if (g.dot != big_kcontig) return SGEMM_ERR_UNSUPPORTED;   // the two views agree by construction
     if (big_kcontig) {
+        // (with S = 1 Small's row stride is never used)
         const bool vec = al16(p.big) && p.big_ld % 4 == 0 && p.small_sk == 1 && al16(p.small) &&
-                         p.small_ss % 4 == 0;
+                         (p.S == 1 || p.small_ss % 4 == 0);
         timing_mark(s, true);
         if (vec) launch_dot_s<true>(p, g.pb, s);
         else launch_dot_s<false>(p, g.pb, s);
