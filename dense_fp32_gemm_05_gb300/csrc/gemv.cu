@@ -606,6 +606,13 @@ int launch_axpy_s(const gemv::Params &p, cudaStream_t s) {
 
 bool al16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
 
+// The axpy form runs on the tensor cores (tc_thin_kernel) from this S up.
+// Measured on GB300 (S x 16384 x 8192 NN, and its TN twin, us per call,
+// L2 flushed; FFMA staged kernel / tensor cores): S = 8 105 / 154, S = 12
+// 176 / 154, S = 16 179 / 155.  Below it each element of Big feeds too few
+// FMAs for the CUDA cores to be the bound.
+constexpr int kThinTcMinS = 12;
+
 std::mutex g_gemv_mu;
 uint64_t g_gemv_wait_ns = 2000000000ull;   // 2 s, as the tensor-core path
 
@@ -791,6 +798,49 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
         else launch_dot_s<false>(p, g.pb, s);
         timing_mark(s, false);
         return last_cuda_status();
+    }
+    if (al16(p.big) && p.big_ld % 4 == 0 && p.S >= kThinTcMinS && (p.small_sk == 1 || p.small_ss == 1)) {
+        // the tensor cores (tc_thin_kernel): one CTA per SM and 128 columns p,
+        // K split by the same waves x (k per CTA + fixed cost) model, the fixed
+        // cost of a CTA being ~512 k (its pipeline fill) and ranges multiples of 32
+        const int pblocks = (p.P + 127) / 128;
+        const int64_t slots = std::max(1, sms);
+        const int64_t ks_max = std::max<int64_t>(1, std::min<int64_t>(K / 256, 64));
+        int64_t ks = 1;
+        double best = 1e30;
+        for (int64_t c = 1; c <= ks_max; ++c) {
+            const double t = (double)((pblocks * c + slots - 1) / slots) * ((double)K / (double)c + 512.0);
+            if (t < best * 0.999) {
+                best = t;
+                ks = c;
+            }
+        }
+        ThinCall tcall{};
+        tcall.S = p.S; tcall.P = p.P; tcall.K = p.K;
+        tcall.kchunk = (int)(((K + ks - 1) / ks + 31) / 32 * 32);
+        tcall.ksplit = (int)((K + tcall.kchunk - 1) / tcall.kchunk);
+        tcall.big = p.big; tcall.big_ld = p.big_ld;
+        tcall.small = p.small; tcall.small_ss = p.small_ss; tcall.small_sk = p.small_sk;
+        tcall.C = p.C; tcall.c_s = p.c_s; tcall.c_p = p.c_p;
+        tcall.rows_thin = p.rows_thin;
+        tcall.alpha = p.alpha; tcall.beta = p.beta;
+        tcall.row_scale = p.row_scale; tcall.bias = p.bias; tcall.act = p.act;
+        if (tcall.ksplit > 1) {
+            void *ws = nullptr;
+            int st = workspace(s, (size_t)tcall.ksplit * p.S * p.P * sizeof(float), &ws, 2);
+            if (st != SGEMM_OK) return st;
+            tcall.partial = static_cast<float *>(ws);
+        }
+        int st = run_tc_thin(tcall, s);
+        if (st != SGEMM_ERR_UNSUPPORTED) {
+            if (st != SGEMM_OK || tcall.ksplit == 1) return st;
+            p.ksplit = tcall.ksplit;
+            p.partial = tcall.partial;
+            const int64_t n = (int64_t)p.S * p.P;
+            const int blocks = (int)std::min<int64_t>((n + gemv::THREADS - 1) / gemv::THREADS, 4 * sms);
+            launch_dependent(gemv::gemv_ksum_kernel, dim3(blocks), dim3(gemv::THREADS), 0, s, p);
+            return last_cuda_status();
+        }
     }
     p.kchunk = g.kchunk;
     p.ksplit = g.ksplit;

@@ -185,6 +185,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same (try_wait may suspend the thread for a while;
+// a thread that polls two barriers must not sleep on either).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete.  Returns false (and
 // raises the device error word) when the limit passes first.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -1041,6 +1052,338 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- thin problems
+// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 16 outputs per column of a
+// large operand Big whose rows run along P in memory (Big(p, k) at
+// big[k ld + p]: decode's weights stored [K][N], or a transposed matrix
+// times a few vectors).  On the CUDA cores each element of Big feeds S FMAs,
+// which from S = 12 up is the bound; here the tensor cores take them.  A CTA
+// owns 128 columns p of Big and one K range (K split over CTAs, multiples of
+// 32; the partial sums go to the thin path's sum kernel):
+//   * raw Big tiles of 32 k x 128 p arrive by TMA in a ring of their own
+//     (THIN_RAW stages of 16 KB), freed as soon as the split warps have read
+//     them, so that the HBM stream runs ahead of the split and the MMAs;
+//   * 8 warps split each tile (hi = rna_tf32(x), lo = rna_tf32(x - hi)) and
+//     turn it around into the K-major 128-byte-swizzled layout of an MMA
+//     operand (128 rows p x 32 k), in a ring of THIN_OPS operand stages;
+//   * Small, split by the pre-pass into [S][Kp] hi and lo, comes by TMA as a
+//     64-row operand per stage: rows 0..15 Small_hi, 16..31 Small_lo (rows past
+//     S read as zeros), 32..63 zeros;
+//   * per 8 k the MMA thread issues Big_hi x that operand into D1 (columns
+//     0..15 hi*hi, 16..31 hi*lo) and Big_lo x it into D2 (columns 0..15
+//     lo*hi; 16..31, lo*lo, unused), M = 128, N = 64, K = 8.  Each of the
+//     4 k-slices of a block has its own D1 and D2 (8 accumulators of 64
+//     columns), which halves the error against one pair;
+//   * the epilogue adds each product's 4 accumulators, then hi*hi + (lo*hi
+//     + hi*lo) per output, and redoes NaN sums in fp32 over the CTA's K
+//     range.
+// The MMAs bound it: on GB300 an M = 128 kind::tf32 MMA costs ~120 cycles
+// whatever its N up to 256 (here ~116 at N = 64, by clock64 on the MMA
+// thread: ~930 of a block's ~1,090 cycles).  Swapping the operands (Small's
+// hi and lo stacked as M = 128, Big's 256 columns as N) makes every MMA a
+// full one but doubles the shared-memory traffic per byte of Big and leaves
+// room for only two raw stages: measured slower (16 x 16384 x 8192 NN 154 ->
+// 165 us).
+constexpr int THIN_P = 128;            // columns p per CTA (the MMA's M)
+constexpr int THIN_K = 32;             // k per block
+constexpr int THIN_RAW = 6;            // raw tile stages (16 KB)
+constexpr int THIN_OPS = 3;            // operand stages (Big_hi, Big_lo, Small: 40 KB)
+constexpr int THIN_RAW_BYTES = THIN_K * THIN_P * 4;
+constexpr int THIN_A_BYTES = THIN_P * THIN_K * 4;
+constexpr int THIN_B_BYTES = 64 * THIN_K * 4;
+constexpr int THIN_OP_BYTES = 2 * THIN_A_BYTES + THIN_B_BYTES;
+constexpr int THIN_BARS = 2 * THIN_RAW + 3 * THIN_OPS + 1;
+constexpr int THIN_SMEM = THIN_RAW * THIN_RAW_BYTES + THIN_OPS * THIN_OP_BYTES + 512 + 1024;
+static_assert(THIN_BARS * 8 + 8 <= 512, "thin barriers");
+static_assert(THIN_SMEM <= SMEM_LIMIT, "thin shared memory");
+
+struct ThinParams {
+    int S, P, K;
+    int kchunk, ksplit;                // K range of CTA y: [y kchunk, min(K, +kchunk)), kchunk % 32 == 0
+    const float *big;                  // Big(p, k) = big[k * big_ld + p]
+    int64_t big_ld;
+    const float *small;                // Small(s, k) = small[s * small_ss + k * small_sk]
+    int64_t small_ss, small_sk;
+    float *C;
+    int64_t c_s, c_p;                  // C(s, p) = C[s * c_s + p * c_p]
+    int rows_thin;                     // s is the row of C (M small), else its column
+    float alpha, beta;
+    const float *row_scale, *bias;
+    int act;
+    float *partial;                    // ksplit > 1: [ksplit][S][P]
+    unsigned long long wait_ns;
+};
+
+// 32 lanes x 8 columns of 32-bit values from tensor memory.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// sum_{k0 <= k < k1} Small(s, k) Big(p, k) in fp32 by the whole warp (lanes
+// take k = k0 + lane, + 32, ...; a butterfly adds them); every lane returns it.
+__device__ __noinline__ float thin_dot_fp32_warp(const ThinParams p, int s, int pp, int k0, int k1,
+                                                 int lane) {
+    float acc = 0.0f;
+    for (int k = k0 + lane; k < k1; k += 32)
+        acc = __fmaf_rn(p.small[(int64_t)s * p.small_ss + (int64_t)k * p.small_sk],
+                        p.big[(int64_t)k * p.big_ld + pp], acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    return acc;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_thin_kernel(const __grid_constant__ CUtensorMap tm_big,
+                   const __grid_constant__ CUtensorMap tm_shi,
+                   const __grid_constant__ CUtensorMap tm_slo, const ThinParams p) {
+    constexpr int R = THIN_RAW, O = THIN_OPS, NW = WORKERS / 32;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem0 = smem_u32(smem);
+    auto raw_at = [&](int r) { return smem0 + (uint32_t)(r * THIN_RAW_BYTES); };
+    auto hi_at = [&](int o) { return smem0 + (uint32_t)(R * THIN_RAW_BYTES + o * THIN_OP_BYTES); };
+    auto lo_at = [&](int o) { return hi_at(o) + (uint32_t)THIN_A_BYTES; };
+    auto b_at = [&](int o) { return hi_at(o) + (uint32_t)(2 * THIN_A_BYTES); };
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R * THIN_RAW_BYTES + O * THIN_OP_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + THIN_BARS);
+    const uint32_t bar0 = smem_u32(bars);
+    auto raw_full = [&](int r) { return bar0 + 8u * r; };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
+    auto op_ready = [&](int o) { return bar0 + 8u * (2 * R + o); };      // split done
+    auto op_bfull = [&](int o) { return bar0 + 8u * (2 * R + O + o); };  // Small landed
+    auto op_empty = [&](int o) { return bar0 + 8u * (2 * R + 2 * O + o); };
+    const uint32_t accf = bar0 + 8u * (2 * R + 3 * O);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int p0 = (int)blockIdx.x * THIN_P;
+    const int k0 = (int)blockIdx.y * p.kchunk;
+    const int k1 = min(p.K, k0 + p.kchunk);
+    const int nblk = (k1 - k0 + THIN_K - 1) / THIN_K;
+    const uint64_t lim = p.wait_ns;
+
+    if (warp == 0 && lane == 0) {
+        for (int r = 0; r < R; ++r) {
+            mbar_init(raw_full(r), 1);
+            mbar_init(raw_empty(r), NW);
+        }
+        for (int o = 0; o < O; ++o) {
+            mbar_init(op_ready(o), NW);
+            mbar_init(op_bfull(o), 1);
+            mbar_init(op_empty(o), 1);
+        }
+        mbar_init(accf, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_map(&tm_big);
+        prefetch_map(&tm_shi);
+        prefetch_map(&tm_slo);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(tmem_slot)), "r"(512) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // rows 32..63 of every Small operand stay zero (TMA fills rows 0..31)
+    for (int i = threadIdx.x; i < O * 32 * THIN_K / 4; i += THREADS) {
+        const int o = i / (32 * THIN_K / 4), e = i % (32 * THIN_K / 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};"
+                     :: "r"(b_at(o) + (uint32_t)(32 * THIN_K * 4 + 16 * e)), "f"(0.0f) : "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();      // the split of Small is complete
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both rings)
+        if (lane == 0) {
+            int ga = 0, gb = 0;
+            uint64_t idle0 = 0;
+            bool ok = true;
+            while (ok && (ga < nblk || gb < nblk)) {
+                bool moved = false;
+                if (ga < nblk && mbar_test(raw_empty(ga % R), ((uint32_t)(ga / R) & 1u) ^ 1u)) {
+                    const int r = ga % R;
+                    mbar_expect_tx(raw_full(r), (uint32_t)THIN_RAW_BYTES);
+                    tma_load_2d(raw_at(r), &tm_big, raw_full(r), p0, k0 + ga * THIN_K);
+                    ++ga;
+                    moved = true;
+                }
+                if (gb < nblk && mbar_test(op_empty(gb % O), ((uint32_t)(gb / O) & 1u) ^ 1u)) {
+                    const int o = gb % O;
+                    mbar_expect_tx(op_bfull(o), 2u * 16u * THIN_K * 4u);
+                    tma_load_2d(b_at(o), &tm_shi, op_bfull(o), k0 + gb * THIN_K, 0);
+                    tma_load_2d(b_at(o) + 16u * THIN_K * 4u, &tm_slo, op_bfull(o), k0 + gb * THIN_K, 0);
+                    ++gb;
+                    moved = true;
+                }
+                if (moved) {
+                    idle0 = 0;
+                } else if (idle0 == 0) {
+                    idle0 = global_timer_ns();
+                } else if (global_timer_ns() - idle0 > lim) {
+                    atomicExch(&g_error, (unsigned)SGEMM_ERR_TIMEOUT);
+                    ok = false;
+                }
+            }
+            // drain: the last filling of each slot of both rings has landed
+            for (int q = (ga > R ? ga - R : 0); q < ga; ++q)
+                mbar_wait(raw_full(q % R), (uint32_t)(q / R) & 1u, kDrainNs);
+            for (int q = (gb > O ? gb - O : 0); q < gb; ++q)
+                mbar_wait(op_bfull(q % O), (uint32_t)(q / O) & 1u, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------ MMA issuer
+            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) |
+                                   ((uint32_t)(THIN_P >> 4) << 24);
+            for (int g = 0; g < nblk; ++g) {
+                const int o = g % O;
+                const uint32_t ph = (uint32_t)(g / O) & 1u;
+                if (!mbar_wait(op_ready(o), ph, lim) || !mbar_wait(op_bfull(o), ph, lim)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < THIN_K / 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk * 32);
+                    const uint64_t bd = smem_desc<THIN_K * 4>(b_at(o) + off);
+                    // k-slice kk: D1 at columns 128 kk, D2 at 128 kk + 64
+                    const uint32_t acc = g == 0 ? 0u : 1u;
+                    const uint32_t d = tmem + (uint32_t)(128 * kk);
+                    umma_tf32(d, smem_desc<THIN_K * 4>(hi_at(o) + off), bd, idesc, acc);
+                    umma_tf32(d + 64u, smem_desc<THIN_K * 4>(lo_at(o) + off), bd, idesc, acc);
+                }
+                umma_commit(op_empty(o));
+            }
+            umma_commit(accf);          // every MMA issued above has completed
+            mbar_wait(accf, 0u, kDrainNs);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ split + epilogue (warps 2..9)
+        const int t = threadIdx.x - 64;
+        const int pl = t & (THIN_P - 1);             // this thread's column p of the tile
+        const int kh = t >> 7;                       // its half of a block's 32 k
+        const uint32_t swz = (uint32_t)(pl & 7);     // 128-byte swizzle of row pl
+        bool ok = true;
+        for (int g = 0; g < nblk; ++g) {
+            const int r = g % R, o = g % O;
+            if (!mbar_wait(raw_full(r), (uint32_t)(g / R) & 1u, lim)) { ok = false; break; }
+            // raw tile: row k (128 floats of p); this thread's 16 k of column pl
+            float hi[16], lo[16];
+            const float *raw = reinterpret_cast<const float *>(smem + r * THIN_RAW_BYTES);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float x = raw[(kh * 16 + j) * THIN_P + pl];
+                hi[j] = tf32_round(x);
+                lo[j] = tf32_round(__fsub_rn(x, hi[j]));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(raw_empty(r));
+            if (!mbar_wait(op_empty(o), ((uint32_t)(g / O) & 1u) ^ 1u, lim)) { ok = false; break; }
+            const uint32_t row = (uint32_t)(pl * THIN_K * 4);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t pos = row + ((((uint32_t)(kh * 4 + c)) ^ swz) << 4);
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                             :: "r"(hi_at(o) + pos), "f"(hi[4 * c]), "f"(hi[4 * c + 1]),
+                                "f"(hi[4 * c + 2]), "f"(hi[4 * c + 3]) : "memory");
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                             :: "r"(lo_at(o) + pos), "f"(lo[4 * c]), "f"(lo[4 * c + 1]),
+                                "f"(lo[4 * c + 2]), "f"(lo[4 * c + 3]) : "memory");
+            }
+            // generic-proxy stores must be visible to the tensor core's reads
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(op_ready(o));
+        }
+        // ---- epilogue: warp w reads TMEM lanes 32 (w % 4).. (its 32 columns
+        // p) and s = 8 half .. + 7; out = hi*hi + (lo*hi + hi*lo)
+        const bool ready = ok && mbar_wait(accf, 0u, lim);
+        tc_fence_after();
+        if (ready) {
+            const int q = warp & 3, half = (warp - 2) >> 2;
+            const int pp = p0 + q * 32 + lane;
+            const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 8);
+            // each product summed over the 4 k-slice accumulators, in slice order
+            float hh[8], hl[8], lh[8];
+#pragma unroll
+            for (int kk = 0; kk < THIN_K / 8; ++kk) {
+                uint32_t a[8], b[8], c[8];
+                const uint32_t tk = ta + (uint32_t)(128 * kk);
+                tmem_ld8(tk, a);
+                tmem_ld8(tk + 16u, b);
+                tmem_ld8(tk + 64u, c);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    hh[e] = kk == 0 ? __uint_as_float(a[e]) : __fadd_rn(hh[e], __uint_as_float(a[e]));
+                    hl[e] = kk == 0 ? __uint_as_float(b[e]) : __fadd_rn(hl[e], __uint_as_float(b[e]));
+                    lh[e] = kk == 0 ? __uint_as_float(c[e]) : __fadd_rn(lh[e], __uint_as_float(c[e]));
+                }
+            }
+            float v[8];
+            bool nan = false;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[e] = __fadd_rn(hh[e], __fadd_rn(lh[e], hl[e]));
+                nan |= v[e] != v[e];
+            }
+            // NaN sums (a split of an infinity, or of a value that rounds to
+            // one) are redone in fp32 by the warp, one output at a time
+            uint32_t bad = 0;
+            if (pp < p.P)
+                for (int e = 0; e < 8; ++e)
+                    if (half * 8 + e < p.S && v[e] != v[e]) bad |= 1u << e;
+            if (__any_sync(0xffffffffu, nan)) {
+                while (true) {
+                    const uint32_t lanes = __ballot_sync(0xffffffffu, bad != 0);
+                    if (lanes == 0) break;
+                    const int src = __ffs(lanes) - 1;
+                    const int e = __ffs(__shfl_sync(0xffffffffu, bad, src)) - 1;
+                    const float d = thin_dot_fp32_warp(p, half * 8 + e, p0 + q * 32 + src, k0, k1, lane);
+                    if (lane == src) {
+                        v[e] = d;
+                        bad &= ~(1u << e);
+                    }
+                }
+            }
+            if (pp < p.P) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int sidx = half * 8 + e;
+                    if (sidx >= p.S) break;
+                    if (p.ksplit > 1) {
+                        p.partial[((int64_t)blockIdx.y * p.S + sidx) * p.P + pp] = v[e];
+                        continue;
+                    }
+                    float *dst = p.C + (int64_t)sidx * p.c_s + (int64_t)pp * p.c_p;
+                    const int crow = p.rows_thin ? sidx : pp, ccol = p.rows_thin ? pp : sidx;
+                    const float a = epi_alpha(p.alpha, p.row_scale, crow);
+                    const float tt = p.beta == 0.0f ? __fmul_rn(a, v[e])
+                                                    : __fmaf_rn(a, v[e], __fmul_rn(p.beta, *dst));
+                    *dst = epi_tail(tt, p.bias, ccol, p.act);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(512) : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- stream-K fixup
 // CTA (t, y) finishes tile t: when the tile's k-blocks were shared by
 // several CTAs, it adds their partial sums in ascending k order (the CTAs'
@@ -1453,6 +1796,72 @@ static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int
                bk == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int run_tc_thin(const ThinCall &c, cudaStream_t s) {
+    if (c.S < 1 || c.S > 16 || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
+        return SGEMM_ERR_UNSUPPORTED;
+    // Small(s, k) = small[s * ss + k * sk]: K-contiguous (sk == 1) or stored k-major (ss == 1)
+    const bool s_direct = c.small_sk == 1, s_trans = !s_direct && c.small_ss == 1;
+    if (!s_direct && !s_trans) return SGEMM_ERR_UNSUPPORTED;
+    if (!aligned16(c.big) || c.big_ld % 4 != 0) return SGEMM_ERR_UNSUPPORTED;
+    const int Kp = (int)((c.K + tc::KPAD - 1) / tc::KPAD) * tc::KPAD;
+    auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
+    const size_t sm_elems = up((size_t)c.S * Kp * 4) / 4;
+    void *ws = nullptr;
+    int st = workspace(s, 2 * sm_elems * 4, &ws);
+    if (st != SGEMM_OK) return st;
+    float *s_hi = static_cast<float *>(ws), *s_lo = s_hi + sm_elems;
+    tc::SplitJob js = split_job(c.small, s_direct ? c.small_ss : c.small_sk, s_trans, c.S, c.K, Kp,
+                                s_hi, s_lo);
+    launch_split_pair(true, js, tc::SplitJob{}, s);
+    st = last_status();
+    if (st != SGEMM_OK) return st;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return SGEMM_ERR_UNSUPPORTED;
+    CUtensorMap maps[3];
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)c.P, (cuuint64_t)c.K};
+        cuuint64_t strides[1] = {(cuuint64_t)c.big_ld * sizeof(float)};
+        cuuint32_t box[2] = {(cuuint32_t)tc::THIN_P, (cuuint32_t)tc::THIN_K};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(c.big), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SGEMM_ERR_UNSUPPORTED;
+    }
+    if (!make_map(&maps[1], s_hi, c.S, Kp, 16, tc::THIN_K) || !make_map(&maps[2], s_lo, c.S, Kp, 16, tc::THIN_K))
+        return SGEMM_ERR_UNSUPPORTED;
+    tc::ThinParams p{};
+    p.S = c.S; p.P = c.P; p.K = c.K;
+    p.kchunk = c.kchunk; p.ksplit = c.ksplit;
+    p.big = c.big; p.big_ld = c.big_ld;
+    p.small = c.small; p.small_ss = c.small_ss; p.small_sk = c.small_sk;
+    p.C = c.C; p.c_s = c.c_s; p.c_p = c.c_p;
+    p.rows_thin = c.rows_thin;
+    p.alpha = c.alpha; p.beta = c.beta;
+    p.row_scale = c.row_scale; p.bias = c.bias; p.act = c.act;
+    p.partial = c.partial;
+    {
+        std::lock_guard<std::mutex> lk(g_tc_mu);
+        p.wait_ns = g_wait_ns;
+    }
+    auto kern = tc::tc_thin_kernel;
+    static uint64_t attr_done = 0;   // bit d: the shared-memory opt-in is set on device d
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::THIN_SMEM) !=
+            cudaSuccess)
+            return last_status();
+        __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
+    }
+    const dim3 grid((unsigned)((c.P + tc::THIN_P - 1) / tc::THIN_P), (unsigned)c.ksplit);
+    timing_mark(s, true);
+    launch_dependent(kern, grid, dim3(tc::THREADS), tc::THIN_SMEM, s, maps[0], maps[1], maps[2], p);
+    timing_mark(s, false);
+    return last_status();
 }
 
 int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha,

@@ -126,13 +126,15 @@ def test_gemv_forced_on_a_wide_problem_is_refused():
     assert st == sg.SGEMM_ERR_UNSUPPORTED
 
 
-def test_staged_axpy_timeout_reports_and_recovers(oracle_mod):
-    """The thin-problem kernel that stages the large operand through shared
-    memory with TMA (S = 16, large operand K x N row-major): a 1 ns wait limit
-    makes its bounded waits run out; the call raises SGEMM_ERR_TIMEOUT through
-    the device error word and the next call computes the right result."""
+@pytest.mark.parametrize("M", [8, 16])
+def test_staged_timeout_reports_and_recovers(oracle_mod, M):
+    """The thin-problem kernels that stage the large operand (K x N
+    row-major) through shared memory with TMA: on the CUDA cores at S = 8, on
+    the tensor cores at S = 16.  A 1 ns wait limit makes their bounded waits
+    run out; the call raises SGEMM_ERR_TIMEOUT through the device error word
+    and the next call computes the right result."""
     import torch
-    M, N, K = 16, 4096, 4096
+    N, K = 4096, 4096
     A = gi.random_matrix(61, M, K)
     B = gi.random_matrix(62, K, N)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
@@ -153,3 +155,40 @@ def test_staged_axpy_timeout_reports_and_recovers(oracle_mod):
     assert st == 0 and sg.sgemm_device_error(s) == 0
     ref, bound = oracle_mod.gemm_f64("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N)
     assert oracle_mod.compare(dC.cpu().numpy(), ref, bound, K, 1.0)["pass"]
+
+
+# The tensor-core form of the thin path (S >= 12 and the large operand's rows
+# along the long dimension, 16-byte aligned): 3xTF32 on tcgen05, K split into
+# ranges of multiples of 32 with the partial sums added by the sum kernel.
+TC_THIN = [
+    # (S, P, K, thin side, alpha, beta); P % 4 == 0: the large operand's rows
+    # (P floats) start 16-byte aligned, as the tensor-core form needs
+    (12, 1000, 777, "rows", 1.0, 0.0),
+    (13, 132, 31, "cols", -1.5, 0.5),        # ragged P tile, K below one block
+    (16, 16384, 2049, "rows", 0.75, 1.0),
+    (16, 300, 40000, "rows", 1.0, 0.0),      # K split across 50 CTAs
+    (15, 4100, 9000, "cols", 2.0, -1.0),
+]
+
+
+@pytest.mark.parametrize("S,P,K,thin,alpha,beta", TC_THIN)
+def test_thin_tensor_core_within_bound(oracle_mod, S, P, K, thin, alpha, beta):
+    import torch
+    M, N = (S, P) if thin == "rows" else (P, S)
+    ta, tb = ("N", "N") if thin == "rows" else ("T", "N")   # the large operand along P
+    opA = gi.random_matrix(900 + S, M, K, dist="normal")
+    opB = gi.random_matrix(901 + S, K, N, dist="normal")
+    C = gi.random_matrix(902 + S, M, N)
+    A, B = stored(opA, ta), stored(opB, tb)
+    c0 = sg.sgemm_launch_count()
+    st, out = gh.run(ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta,
+                     C if beta else None, N, path=sg.PATH_AUTO)
+    assert st == 0
+    # the split of the small operand, the tensor-core kernel, and the sum when K is split
+    assert sg.sgemm_launch_count() - c0 in (2, 3)
+    ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta,
+                                     C if beta else None, N)
+    rep = oracle_mod.compare(out, ref, bound, K, alpha)
+    assert rep["pass"], rep
+    # 3xTF32, not single-pass TF32: well inside the fp32 bound at this K
+    assert rep["max_err_over_bound"] < 0.05, rep

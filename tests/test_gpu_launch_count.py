@@ -45,5 +45,7 @@ def test_quick_returns_and_thin_problems():
     assert _launches("N", "N", 0, 64, 64) == 0               # nothing to do
     # thin: one pass over the large operand, plus the K-split sum when K is cut
     assert _launches("N", "T", 1, 4096, 4096) == 1
-    n = _launches("N", "N", 16, 16384, 8192)
+    n = _launches("N", "N", 8, 16384, 8192)
     assert n in (1, 2)
+    # S = 16 on the tensor cores: the split of the small operand and the kernel
+    assert _launches("N", "N", 16, 16384, 8192) == 2
