@@ -86,16 +86,19 @@ typedef enum {
 
 /* Arithmetic path.  AUTO lets the per-shape selector choose among the
    fp32-accurate paths: GEMV for min(M, N) <= 16 (see below for the one
-   exception), else 3xTF32 for K >= 32 and FFMA for K < 32.  TF32 is never
-   chosen by AUTO. */
+   exception); else FFMA's small-problem kernel for small problems (2MNK <=
+   1.2e8, K <= 512, at most 1024 tiles of 16 x 16); else 3xTF32 for K >= 32
+   and FFMA for K < 32.  TF32 is never chosen by AUTO. */
 typedef enum {
     SGEMM_PATH_AUTO = 0,
     SGEMM_PATH_FFMA = 1,   /* CUDA-core fp32 FMA, 128x128 block tiles, 8x16
                               register outer products ("Matmul II: register
                               blocking, warp tiling, tensor cores", sections
-                              3-5).  Sums each output in ascending k with
-                              fused multiply-adds, so with split == 1 its
-                              result is bit-identical to the naive loop
+                              3-5); small problems (the rule above, with
+                              split <= 1) run one launch of 16 x 16 tiles
+                              instead.  Both sum each output in ascending k
+                              with fused multiply-adds, so with split == 1
+                              the result is bit-identical to the naive loop
                               ("How to get a matmul kernel into the top
                               percentile (worklog)", "Optimization 1").     */
     SGEMM_PATH_3XTF32 = 2, /* tensor cores (tcgen05 kind::tf32, TMEM
@@ -106,14 +109,19 @@ typedef enum {
     SGEMM_PATH_TF32 = 3,   /* the same tensor-core kernel with only hi*hi:
                               single-pass TF32, LOWER accuracy than fp32
                               ("Optimising fp32 GEMM on A100", "Kernel 1").  */
-    SGEMM_PATH_GEMV = 4    /* thin problems, min(M, N) <= 16: CUDA-core fp32
-                              FMAs streaming the large operand once, no tiles
-                              ("Matmul II", section 8: dedicated GEMV kernels
-                              for decode's M = 1 to a few dozen).  AUTO takes
-                              it whenever min(M, N) <= 16, except with K >= 32,
-                              min(M, N) > 4 and the large operand's rows along
-                              K (weights stored [N][K]): those go to 3xTF32.
-                              Forced on a larger problem it returns
+    SGEMM_PATH_GEMV = 4    /* thin problems, min(M, N) <= 16: the large
+                              operand streamed once, no tiles ("Matmul II",
+                              section 8: dedicated GEMV kernels for decode's
+                              M = 1 to a few dozen).  CUDA-core fp32 FMAs,
+                              except with min(M, N) >= 12 and the large
+                              operand's rows along the long dimension (16-byte
+                              aligned, leading dimension a multiple of 4):
+                              those run 3xTF32 on the tensor cores.  AUTO
+                              takes this path whenever min(M, N) <= 16, except
+                              with K >= 32, min(M, N) > 4 and the large
+                              operand's rows along K (weights stored [N][K]):
+                              those go to the 3xTF32 tiles.  Forced on a
+                              larger problem it returns
                               SGEMM_ERR_UNSUPPORTED.                          */
 } sgemm_path;
 
