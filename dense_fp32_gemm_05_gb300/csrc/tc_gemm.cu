@@ -1812,11 +1812,7 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
     int st = workspace(s, 2 * sm_elems * 4, &ws);
     if (st != SGEMM_OK) return st;
     float *s_hi = static_cast<float *>(ws), *s_lo = s_hi + sm_elems;
-    tc::SplitJob js = split_job(c.small, s_direct ? c.small_ss : c.small_sk, s_trans, c.S, c.K, Kp,
-                                s_hi, s_lo);
-    launch_split_pair(true, js, tc::SplitJob{}, s);
-    st = last_status();
-    if (st != SGEMM_OK) return st;
+    // every check before the first launch: UNSUPPORTED means nothing ran
     EncodeTiledFn enc = encode_fn();
     if (!enc) return SGEMM_ERR_UNSUPPORTED;
     CUtensorMap maps[3];
@@ -1832,6 +1828,22 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
     }
     if (!make_map(&maps[1], s_hi, c.S, Kp, 16, tc::THIN_K) || !make_map(&maps[2], s_lo, c.S, Kp, 16, tc::THIN_K))
         return SGEMM_ERR_UNSUPPORTED;
+    auto kern = tc::tc_thin_kernel;
+    static uint64_t attr_done = 0;   // bit d: the shared-memory opt-in is set on device d
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::THIN_SMEM) !=
+            cudaSuccess)
+            return last_status();
+        __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
+    }
+    tc::SplitJob js = split_job(c.small, s_direct ? c.small_ss : c.small_sk, s_trans, c.S, c.K, Kp,
+                                s_hi, s_lo);
+    launch_split_pair(true, js, tc::SplitJob{}, s);
+    st = last_status();
+    if (st != SGEMM_OK) return st;
     tc::ThinParams p{};
     p.S = c.S; p.P = c.P; p.K = c.K;
     p.kchunk = c.kchunk; p.ksplit = c.ksplit;
@@ -1845,17 +1857,6 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lk(g_tc_mu);
         p.wait_ns = g_wait_ns;
-    }
-    auto kern = tc::tc_thin_kernel;
-    static uint64_t attr_done = 0;   // bit d: the shared-memory opt-in is set on device d
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
-    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
-    if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::THIN_SMEM) !=
-            cudaSuccess)
-            return last_status();
-        __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
     }
     const dim3 grid((unsigned)((c.P + tc::THIN_P - 1) / tc::THIN_P), (unsigned)c.ksplit);
     timing_mark(s, true);
