@@ -29,6 +29,7 @@ CASES = [
     ("tc_narrow_tt", sg.PATH_3XTF32, 0, "T", "T", 257, 64, 129),
     ("gemv_dot", sg.PATH_GEMV, 0, "N", "T", 3, 700, 500),
     ("gemv_axpy", sg.PATH_GEMV, 0, "T", "N", 900, 5, 400),
+    ("gemv_tensor_core", sg.PATH_GEMV, 0, "N", "N", 16, 1000, 500),
 ]
 
 EPILOGUES = [
