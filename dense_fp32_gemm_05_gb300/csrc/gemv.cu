@@ -677,6 +677,41 @@ int last_cuda_status() {
 
 }  // namespace
 
+// The thin path's tensor-core form (tc_thin_kernel) takes S >= kThinTcMinS
+// with the large operand's rows along the long dimension, 16-byte aligned
+// with a leading dimension that is a multiple of 4.
+bool thin_on_tensor_cores(char ta, char tb, int64_t M, int64_t N, int64_t lda, int64_t ldb,
+                          bool a_al, bool b_al) {
+    const bool rows_thin = M <= N;
+    const int64_t S = rows_thin ? M : N;
+    const bool big_mn = rows_thin ? is_notrans(tb) : !is_notrans(ta);
+    const bool big_al = rows_thin ? (b_al && ldb % 4 == 0) : (a_al && lda % 4 == 0);
+    return S >= kThinTcMinS && S <= kGemvMaxSmall && big_mn && big_al;
+}
+
+// Its grid: one CTA per SM and 128 columns p; K split by the same waves x (k
+// per CTA + fixed cost) model as the axpy form, the fixed cost of a CTA
+// being ~512 k (its pipeline fill) and the ranges multiples of 32.
+ThinTc thin_tc_geometry(int64_t P, int64_t K, int sms) {
+    const int64_t pblocks = (P + 127) / 128;
+    const int64_t slots = std::max(1, sms);
+    const int64_t ks_max = std::max<int64_t>(1, std::min<int64_t>(K / 256, 64));
+    int64_t ks = 1;
+    double best = 1e30;
+    for (int64_t c = 1; c <= ks_max; ++c) {
+        const double t = (double)((pblocks * c + slots - 1) / slots) * ((double)K / (double)c + 512.0);
+        if (t < best * 0.999) {
+            best = t;
+            ks = c;
+        }
+    }
+    ThinTc g;
+    g.kchunk = (int)(((K + ks - 1) / ks + 31) / 32 * 32);
+    g.ksplit = (int)((K + g.kchunk - 1) / g.kchunk);
+    g.ctas = (int)(pblocks * g.ksplit);
+    return g;
+}
+
 namespace {
 
 // Launch geometry shared by run_gemv and gemv_ctas.
@@ -743,7 +778,10 @@ int gemv_take_device_error() {
     return v == 0 ? SGEMM_OK : (int)v;
 }
 
-int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms) {
+int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              bool a_al, bool b_al, int sms) {
+    if (thin_on_tensor_cores(ta, tb, M, N, lda, ldb, a_al, b_al))
+        return thin_tc_geometry(std::max(M, N), std::max<int64_t>(K, 1), sms).ctas;
     return geometry(ta, tb, M, N, std::max<int64_t>(K, 1), sms).ctas;
 }
 
@@ -799,26 +837,13 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
         timing_mark(s, false);
         return last_cuda_status();
     }
-    if (al16(p.big) && p.big_ld % 4 == 0 && p.S >= kThinTcMinS && (p.small_sk == 1 || p.small_ss == 1)) {
-        // the tensor cores (tc_thin_kernel): one CTA per SM and 128 columns p,
-        // K split by the same waves x (k per CTA + fixed cost) model, the fixed
-        // cost of a CTA being ~512 k (its pipeline fill) and ranges multiples of 32
-        const int pblocks = (p.P + 127) / 128;
-        const int64_t slots = std::max(1, sms);
-        const int64_t ks_max = std::max<int64_t>(1, std::min<int64_t>(K / 256, 64));
-        int64_t ks = 1;
-        double best = 1e30;
-        for (int64_t c = 1; c <= ks_max; ++c) {
-            const double t = (double)((pblocks * c + slots - 1) / slots) * ((double)K / (double)c + 512.0);
-            if (t < best * 0.999) {
-                best = t;
-                ks = c;
-            }
-        }
+    if (thin_on_tensor_cores(ta, tb, M, N, lda, ldb, al16(A), al16(B)) &&
+        (p.small_sk == 1 || p.small_ss == 1)) {
+        const ThinTc tg = thin_tc_geometry(p.P, K, sms);
         ThinCall tcall{};
         tcall.S = p.S; tcall.P = p.P; tcall.K = p.K;
-        tcall.kchunk = (int)(((K + ks - 1) / ks + 31) / 32 * 32);
-        tcall.ksplit = (int)((K + tcall.kchunk - 1) / tcall.kchunk);
+        tcall.kchunk = tg.kchunk;
+        tcall.ksplit = tg.ksplit;
         tcall.big = p.big; tcall.big_ld = p.big_ld;
         tcall.small = p.small; tcall.small_ss = p.small_ss; tcall.small_sk = p.small_sk;
         tcall.C = p.C; tcall.c_s = p.c_s; tcall.c_p = p.c_p;

@@ -12,7 +12,20 @@ namespace sgemm_gb300 {
 constexpr int64_t kGemvMaxSmall = 16;
 
 // CTAs of the main GEMV launch for this problem (what run_gemv launches).
-int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int sms);
+int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              bool a_al, bool b_al, int sms);
+
+// Whether the thin problem runs on the tensor cores (tc_thin_kernel): S =
+// min(M, N) >= 12 and the large operand's rows along the long dimension,
+// 16-byte aligned with a leading dimension that is a multiple of 4.
+bool thin_on_tensor_cores(char ta, char tb, int64_t M, int64_t N, int64_t lda, int64_t ldb,
+                          bool a_al, bool b_al);
+
+// The tensor-core form's K split and grid for P columns of the large operand.
+struct ThinTc {
+    int kchunk, ksplit, ctas;
+};
+ThinTc thin_tc_geometry(int64_t P, int64_t K, int sms);
 
 // Bounded-wait limit of the staged kernel (ns; 0 = the default 2 s).
 void gemv_set_wait_limit(uint64_t ns);

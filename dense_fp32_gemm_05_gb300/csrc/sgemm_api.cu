@@ -334,7 +334,8 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
         if (pl.path == SGEMM_PATH_FFMA) {
             *out_ctas = pl.dp_tiles + pl.ctas;
         } else if (pl.path == SGEMM_PATH_GEMV) {
-            *out_ctas = gemv_ctas(transA, transB, M, N, K, num_sms);
+            *out_ctas = gemv_ctas(transA, transB, M, N, K, lda, ldb, a_aligned != 0,
+                                  b_aligned != 0, num_sms);
         } else if (pl.tc_sk > 0) {
             *out_ctas = pl.tc_sk;   // stream-K: one CTA per share of the iterations
         } else {
@@ -366,6 +367,15 @@ extern "C" int sgemm_plan_detail(char transA, char transB, int64_t M, int64_t N,
     make_plan(transA, transB, M, N, K, lda, ldb, ldc, a_aligned != 0, b_aligned != 0,
               c_aligned != 0, path, split, num_sms, &pl);
     info.dp_tiles = pl.path == SGEMM_PATH_GEMV ? 0 : pl.dp_tiles;
+    if (pl.path == SGEMM_PATH_GEMV &&
+        thin_on_tensor_cores(transA, transB, M, N, lda, ldb, a_aligned != 0, b_aligned != 0)) {
+        // the tensor-core form: 128 columns of the large operand per CTA,
+        // 32-wide k-blocks, 8 accumulators; split = the CTAs along K
+        info.tile_n = 128;
+        info.k_block = 32;
+        info.accumulators = 8;
+        info.split = thin_tc_geometry(std::max(M, N), std::max<int64_t>(K, 1), num_sms).ksplit;
+    }
     if (pl.path == SGEMM_PATH_3XTF32 || pl.path == SGEMM_PATH_TF32) {
         const TcVariant v = tc_variant(pl);
         info.pair = v.pair;

@@ -237,7 +237,9 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
 typedef struct {
     int path;          /* sgemm_path actually run                               */
     int tile_m;        /* tile rows: 128, or 256 on an SM pair; GEMV: min(M, N)  */
-    int tile_n;        /* tile columns: 64, 128 or 256 (FFMA: 128; GEMV: 0)     */
+    int tile_n;        /* tile columns: 64, 128 or 256 (FFMA: 128, or 16 for the
+                          small-problem kernel; GEMV: 0, or 128 columns of the
+                          large operand per CTA on the tensor cores)          */
     int vector;        /* FFMA / GEMV: 16-byte operand loads (else 4-byte)      */
     int ctas;          /* CTAs of the main kernel, as sgemm_plan's out_ctas     */
     int split;         /* as sgemm_plan's out_split                             */
@@ -249,7 +251,8 @@ typedef struct {
     int wide;          /* 3xTF32 with 32-wide k-blocks: A_hi in tensor memory,
                           A_lo in shared memory, one MMA over [B_hi | B_lo]     */
     int accumulators;  /* independent accumulators per tile, summed by the
-                          epilogue (1, 2 or 3)                                  */
+                          epilogue (1, 2 or 3; 8 in the thin path's
+                          tensor-core form)                                   */
     int k_block;       /* k-block width of a pipeline stage, in floats          */
     int tail_nsplit;   /* column slices of each tile after the last full wave   */
     int sk_ctas;       /* stream-K over every tile: CTAs sharing the k-blocks   */

@@ -356,3 +356,25 @@ def test_small_kernel_selector_boundaries(lib):
     assert not small(256, 256, 256, sg.PATH_FFMA, 2)              # forced split-K
     assert not small(256, 256, 256, sg.PATH_3XTF32)               # forced tensor cores
     assert not small(8, 256, 256)                                 # thin: GEMV
+
+
+def test_plan_detail_thin_problems_on_the_tensor_cores(lib):
+    """S >= 12 with the large operand's rows along the long dimension (16-byte
+    aligned, leading dimension a multiple of 4): the thin path's tensor-core
+    form, 128 columns per CTA; otherwise the CUDA-core forms (tile_n 0)."""
+    def detail(ta, tb, M, N, K, lda, ldb, a_al=1, b_al=1):
+        st, info = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N, a_al, b_al, 1, 0, 0, 152)
+        assert st == 0 and info["path"] == sg.PATH_GEMV
+        return info
+    i = detail("N", "N", 16, 16384, 8192, 8192, 16384)
+    assert (i["tile_n"], i["ctas"], i["split"], i["k_block"], i["accumulators"]) == (128, 128, 1, 32, 8)
+    i = detail("T", "N", 16384, 12, 8192, 16384, 12)          # N small: A ('T') is the large operand
+    assert i["tile_n"] == 128 and i["ctas"] == 128
+    i = detail("N", "N", 16, 300, 40000, 40000, 300)          # few columns, long K: split over CTAs
+    assert i["tile_n"] == 128 and i["split"] == 50 and i["ctas"] == 150
+    for args in [("N", "N", 11, 16384, 8192, 8192, 16384),     # S below 12
+                 ("N", "N", 16, 1001, 500, 500, 1001),         # ldb not a multiple of 4
+                 ("N", "N", 16, 16384, 8192, 8192, 16384, 1, 0),   # B not 16-byte aligned
+                 ("N", "T", 16, 4096, 4096, 4096, 4096)]:      # rows along K (dot form)
+        st, info = sg.sgemm_plan_detail(*args[:7], args[3], *(args[7:] or (1, 1)), 1, 4, 0, 152)
+        assert st == 0 and info["tile_n"] == 0, args
