@@ -57,7 +57,8 @@ class PlanInfo(ctypes.Structure):
     """sgemm_plan_info of the C header, field for field."""
     _fields_ = [(n, ctypes.c_int) for n in (
         "path", "tile_m", "tile_n", "vector", "ctas", "split", "dp_tiles", "pair", "fuse_a",
-        "fuse_b", "wide", "accumulators", "k_block", "tail_nsplit", "sk_ctas", "sk_tail")]
+        "fuse_b", "wide", "accumulators", "k_block", "tail_nsplit", "sk_ctas", "sk_tail",
+        "pre_transpose")]
 
 
 def library_path() -> str:

@@ -401,6 +401,7 @@ template <bool A_KMAJOR, bool B_KMAJOR, bool VEC>
 __global__ void __launch_bounds__(THREADS, 2) ffma_gemm_kernel(const Params p) {
     __shared__ __align__(16) float sA[3][BK * BM];
     __shared__ __align__(16) float sB[3][BK * BN];
+    pdl_wait();      // after a transpose pre-pass: its copies are complete
     pdl_trigger();   // the stream-K fixup may launch; it waits for this grid
     if ((int)blockIdx.x < p.dp_tiles) {
         run_share<A_KMAJOR, B_KMAJOR, VEC>(p, sA, sB, blockIdx.x, 0, p.kt, 0);
@@ -470,6 +471,44 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const Params p) {
             s.z = __fadd_rn(s.z, v.z); s.w = __fadd_rn(s.w, v.w);
         }
         store_quad(p, m0 + r, n0 + col, s);
+    }
+}
+
+// The FFMA path's pre-pass: a K-contiguous operand copied transposed, so
+// that the kernel reads it as it reads an M- or N-contiguous one (cp.async,
+// no register staging): dst[c * ldd + r] = src[r * lds + c] for r < rows, c
+// < cols.  32 x 32 tiles turned around in shared memory (padded rows: no bank
+// conflicts), reads and writes coalesced; job 0 takes CTAs [0, j0.tiles), job
+// 1 the rest.
+struct TransposeJob {
+    const float *src;
+    int64_t lds;
+    float *dst;
+    int64_t ldd;
+    int rows, cols;     // of src
+    int tiles_c;        // ceil(cols / 32)
+    int tiles;          // CTAs of this job
+};
+
+__global__ void __launch_bounds__(256) transpose_pair_kernel(const TransposeJob j0,
+                                                             const TransposeJob j1) {
+    pdl_trigger();   // the GEMM may launch; it waits for this grid's writes
+    __shared__ float tile[32][33];
+    const bool second = (int)blockIdx.x >= j0.tiles;
+    const TransposeJob &j = second ? j1 : j0;
+    const int b = second ? (int)blockIdx.x - j0.tiles : (int)blockIdx.x;
+    const int r0 = (b / j.tiles_c) * 32, c0 = (b % j.tiles_c) * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + ty + 8 * i, c = c0 + tx;
+        if (r < j.rows && c < j.cols) tile[ty + 8 * i][tx] = __ldg(j.src + (int64_t)r * j.lds + c);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = c0 + ty + 8 * i, r = r0 + tx;
+        if (r < j.rows && c < j.cols) j.dst[(int64_t)c * j.ldd + r] = tile[tx][ty + 8 * i];
     }
 }
 

@@ -128,10 +128,16 @@ static int grid_for(int64_t total, int sms) {
 }
 
 // ------------------------------------------------------------ FFMA launch
+// dep: launched as the programmatic dependent of the transpose pre-pass
 template <bool AK, bool BK_, bool V>
-static void launch_ffma_t(const ffma::Params &p, int grid, cudaStream_t s) {
+static void launch_ffma_t(const ffma::Params &p, int grid, cudaStream_t s, bool dep) {
+    auto kern = ffma::ffma_gemm_kernel<AK, BK_, V>;
+    if (dep) {
+        launch_dependent(kern, dim3(grid), dim3(ffma::THREADS), 0, s, p);
+        return;
+    }
     count_launch();
-    ffma::ffma_gemm_kernel<AK, BK_, V><<<grid, ffma::THREADS, 0, s>>>(p);
+    kern<<<grid, ffma::THREADS, 0, s>>>(p);
 }
 
 // Fills the FFMA kernel parameters of a plan (shared by sgemm_ex and the
@@ -171,17 +177,18 @@ static int ffma_fix_tiles(const ffma::Params &p) {
     return p.tiles_m * p.tiles_n - p.dp_tiles;
 }
 
-static int launch_ffma(const ffma::Params &p, char ta, char tb, bool vec, cudaStream_t s) {
+static int launch_ffma(const ffma::Params &p, char ta, char tb, bool vec, cudaStream_t s,
+                       bool dep = false) {
     const bool ak = is_notrans(ta), bk = !is_notrans(tb);
     const int grid = ffma_grid(p);
-    if (ak && !bk && vec) launch_ffma_t<true, false, true>(p, grid, s);
-    else if (ak && !bk && !vec) launch_ffma_t<true, false, false>(p, grid, s);
-    else if (ak && bk && vec) launch_ffma_t<true, true, true>(p, grid, s);
-    else if (ak && bk && !vec) launch_ffma_t<true, true, false>(p, grid, s);
-    else if (!ak && !bk && vec) launch_ffma_t<false, false, true>(p, grid, s);
-    else if (!ak && !bk && !vec) launch_ffma_t<false, false, false>(p, grid, s);
-    else if (!ak && bk && vec) launch_ffma_t<false, true, true>(p, grid, s);
-    else launch_ffma_t<false, true, false>(p, grid, s);
+    if (ak && !bk && vec) launch_ffma_t<true, false, true>(p, grid, s, dep);
+    else if (ak && !bk && !vec) launch_ffma_t<true, false, false>(p, grid, s, dep);
+    else if (ak && bk && vec) launch_ffma_t<true, true, true>(p, grid, s, dep);
+    else if (ak && bk && !vec) launch_ffma_t<true, true, false>(p, grid, s, dep);
+    else if (!ak && !bk && vec) launch_ffma_t<false, false, true>(p, grid, s, dep);
+    else if (!ak && !bk && !vec) launch_ffma_t<false, false, false>(p, grid, s, dep);
+    else if (!ak && bk && vec) launch_ffma_t<false, true, true>(p, grid, s, dep);
+    else launch_ffma_t<false, true, false>(p, grid, s, dep);
     return launch_status();
 }
 
@@ -221,17 +228,52 @@ static int run_ffma(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int6
                     float beta, float *C, int64_t ldc, cudaStream_t s, const Epilogue &epi) {
     if (pl.small)
         return run_ffma_small(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, epi);
+    // a K-contiguous operand copied transposed first (pl.t_a, pl.t_b): the
+    // kernel then reads it as op(A) 'T' ([K][Mp]) or op(B) 'N' ([K][Np]),
+    // rows padded to 16 bytes
+    auto up = [](size_t bytes) { return (bytes + 255) & ~size_t(255); };
+    const int64_t mp = (M + 3) / 4 * 4, np = (N + 3) / 4 * 4;
+    const size_t a_t = pl.t_a ? up((size_t)K * mp * 4) : 0, b_t = pl.t_b ? up((size_t)K * np * 4) : 0;
+    const char ta_k = pl.t_a ? 'T' : ta, tb_k = pl.t_b ? 'N' : tb;
+    const float *a_k = A, *b_k = B;
+    int64_t lda_k = lda, ldb_k = ldb;
     ffma::Params p = ffma_params(pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi);
     const bool partials = ffma_has_partials(p);
-    if (partials) {
+    const size_t part_bytes = partials ? (size_t)2 * p.sk_ctas * ffma::BM * ffma::BN * sizeof(float) : 0;
+    if (a_t + b_t + part_bytes > 0) {
         void *ws = nullptr;
-        const size_t bytes = (size_t)2 * p.sk_ctas * ffma::BM * ffma::BN * sizeof(float);
-        int st = workspace(s, bytes, &ws);
+        int st = workspace(s, a_t + b_t + part_bytes, &ws);
         if (st != SGEMM_OK) return st;
-        p.partial = static_cast<float *>(ws);
+        char *w = static_cast<char *>(ws);
+        if (pl.t_a) { a_k = reinterpret_cast<float *>(w); lda_k = mp; }
+        if (pl.t_b) { b_k = reinterpret_cast<float *>(w + a_t); ldb_k = np; }
+        if (partials) p.partial = reinterpret_cast<float *>(w + a_t + b_t);
     }
+    const bool pre = pl.t_a || pl.t_b;
+    if (pre) {
+        ffma::TransposeJob ja{}, jb{};
+        if (pl.t_a) {   // A stored M x K -> [K][mp]
+            ja = ffma::TransposeJob{A, lda, const_cast<float *>(a_k), mp, (int)M, (int)K,
+                                    (int)((K + 31) / 32), 0};
+            ja.tiles = (int)(((M + 31) / 32) * ja.tiles_c);
+        }
+        if (pl.t_b) {   // B stored N x K -> [K][np]
+            jb = ffma::TransposeJob{B, ldb, const_cast<float *>(b_k), np, (int)N, (int)K,
+                                    (int)((K + 31) / 32), 0};
+            jb.tiles = (int)(((N + 31) / 32) * jb.tiles_c);
+        }
+        count_launch();
+        ffma::transpose_pair_kernel<<<ja.tiles + jb.tiles, 256, 0, s>>>(ja, jb);
+        int st = launch_status();
+        if (st != SGEMM_OK) return st;
+        p.A = a_k;
+        p.B = b_k;
+        p.lda = lda_k;
+        p.ldb = ldb_k;
+    }
+    const bool vec = (pl.t_a || (aligned16(A) && lda % 4 == 0)) && (pl.t_b || (aligned16(B) && ldb % 4 == 0));
     timing_mark(s, true);
-    int st = launch_ffma(p, ta, tb, pl.vector != 0, s);
+    int st = pre ? launch_ffma(p, ta_k, tb_k, vec, s, true) : launch_ffma(p, ta, tb, pl.vector != 0, s);
     timing_mark(s, false);
     if (st != SGEMM_OK) return st;
     if (partials) {
@@ -389,6 +431,7 @@ extern "C" int sgemm_plan_detail(char transA, char transB, int64_t M, int64_t N,
         info.sk_tail = v.sk_tail;
     } else if (pl.path == SGEMM_PATH_FFMA) {
         info.k_block = pl.small ? ffma_small::KC : ffma::BK;
+        info.pre_transpose = pl.t_a | (pl.t_b << 1);
     }
     *out = info;
     return SGEMM_OK;

@@ -100,7 +100,11 @@ typedef enum {
                               with fused multiply-adds, so with split == 1
                               the result is bit-identical to the naive loop
                               ("How to get a matmul kernel into the top
-                              percentile (worklog)", "Optimization 1").     */
+                              percentile (worklog)", "Optimization 1").  On
+                              a large grid a K-contiguous operand is first
+                              copied transposed into the workspace by one
+                              extra launch (sgemm_plan_info.pre_transpose);
+                              the sums and their order do not change.     */
     SGEMM_PATH_3XTF32 = 2, /* tensor cores (tcgen05 kind::tf32, TMEM
                               accumulators, TMA operand loads) with each
                               operand split x = hi + lo into two TF32 parts
@@ -196,7 +200,9 @@ int sgemm_epilogue(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * C when beta != 0) on an internal stream while the previous chunks'
  * GEMMs run, accumulates the chunks into C on the device (one extra fp32
  * rounding of C per chunk), runs the last chunk in row blocks and downloads
- * each block of C on a second internal stream as soon as it is final.
+ * each block of C on a second internal stream as soon as it is final.  When
+ * beta == 0 and M >= 4096 the rows of C are done in two halves: the top half's
+ * copy home runs while A's bottom rows are still being uploaded.
  * Asynchronous on `stream`: C is complete once `stream` has synchronised.
  * For the copies to overlap and to run at full speed A, B and C must be
  * page-locked (cudaHostAlloc / cudaHostRegister); pageable buffers work but
@@ -258,6 +264,9 @@ typedef struct {
     int sk_ctas;       /* stream-K over every tile: CTAs sharing the k-blocks   */
     int sk_tail;       /* 1: the tiles after the last full wave are shared in k
                           by all CTAs (pairs)                                   */
+    /* FFMA tile path only: */
+    int pre_transpose; /* K-contiguous operands copied transposed by a pre-pass
+                          launch before the kernel: bit 0 op(A), bit 1 op(B)   */
 } sgemm_plan_info;
 
 /*

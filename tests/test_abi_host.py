@@ -378,3 +378,25 @@ def test_plan_detail_thin_problems_on_the_tensor_cores(lib):
                  ("N", "T", 16, 4096, 4096, 4096, 4096)]:      # rows along K (dot form)
         st, info = sg.sgemm_plan_detail(*args[:7], args[3], *(args[7:] or (1, 1)), 1, 4, 0, 152)
         assert st == 0 and info["tile_n"] == 0, args
+
+
+def test_ffma_pre_transpose_selector():
+    """The FFMA tile path copies a K-contiguous operand transposed when the
+    grid is large (M, N >= 128, K >= 256) and the problem's other side is at
+    least 2048: bit 0 op(A) (A 'N'), bit 1 op(B) (B 'T')."""
+    cases = [("N", "N", 4096, 4096, 4096, 1), ("N", "T", 4096, 4096, 4096, 3),
+             ("T", "N", 4096, 4096, 4096, 0), ("T", "T", 4096, 4096, 4096, 2),
+             ("N", "N", 4096, 2047, 4096, 0), ("N", "T", 2047, 4096, 4096, 1),
+             ("N", "N", 4096, 4096, 255, 0), ("N", "N", 127, 4096, 4096, 0)]
+    for ta, tb, M, N, K, want in cases:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, info = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N, path=sg.PATH_FFMA)
+        assert st == 0 and info["path"] == sg.PATH_FFMA, (ta, tb, M, N, K)
+        assert info["pre_transpose"] == want, (ta, tb, M, N, K, info)
+    # the small-problem kernel, the tensor cores and the thin path never copy
+    for args, path in [(("N", "N", 256, 256, 256, 256, 256, 256), sg.PATH_FFMA),
+                       (("N", "N", 4096, 4096, 4096, 4096, 4096, 4096), sg.PATH_AUTO),
+                       (("N", "T", 4, 4096, 4096, 4096, 4096, 4096), sg.PATH_AUTO)]:
+        st, info = sg.sgemm_plan_detail(*args, path=path)
+        assert st == 0 and info["pre_transpose"] == 0, (args, info)

@@ -3,7 +3,8 @@ path and kernel variant:
 
   C(i,j) = act(alpha * s_i * (op(A) op(B))(i,j) + beta * C(i,j) + bias_j)
 
-FFMA (whole tiles, and stream-K with its fixup), 3xTF32 (operands split in
+FFMA (whole tiles, stream-K with its fixup, and after the transpose
+pre-pass), 3xTF32 (operands split in
 the kernel, pre-split operands, SM pairs), the thin-problem kernels (both
 forms), and the K == 0 / alpha == 0 quick return; exact on small integers,
 within the epilogue oracle's bound on random inputs, and bit for bit the
@@ -23,6 +24,7 @@ CASES = [
     ("ffma_small", sg.PATH_FFMA, 1, "N", "N", 300, 260, 200),
     ("ffma_whole", sg.PATH_FFMA, 1, "N", "T", 300, 260, 700),
     ("ffma_stream_k", sg.PATH_FFMA, 0, "T", "N", 256, 256, 1024),
+    ("ffma_pre_transpose", sg.PATH_FFMA, 1, "N", "T", 300, 2100, 260),
     ("tc_fused_nn", sg.PATH_3XTF32, 0, "N", "N", 300, 260, 200),
     ("tc_fused_nt", sg.PATH_3XTF32, 0, "N", "T", 200, 136, 300),
     ("tc_pair_tn", sg.PATH_3XTF32, 0, "T", "N", 300, 260, 200),

@@ -26,6 +26,8 @@ def test_ffma_counts():
     # whole tiles: one kernel; shared K ranges: the kernel and its fixup
     assert _launches("N", "N", 256, 256, 256, sg.PATH_FFMA, 1) == 1
     assert _launches("N", "N", 256, 256, 256, sg.PATH_FFMA, 4) == 2
+    # a K-contiguous operand of a large grid: the transpose pre-pass, then the kernel
+    assert _launches("N", "N", 300, 2100, 260, sg.PATH_FFMA, 1) == 2
 
 
 def test_tensor_core_counts():

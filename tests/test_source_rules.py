@@ -59,9 +59,11 @@ def test_dependent_kernels_wait_for_their_predecessor():
     texts = dict(_sources())
     # kernels passed to launch_dependent() or launched with the programmatic
     # attribute: the K-split sum, both stream-K fixups, the tensor-core main
-    # kernel (after the split pre-pass)
+    # kernel (after the split pre-pass), the FFMA kernel (after the transpose
+    # pre-pass)
     dependents = [("gemv.cu", "gemv_ksum_kernel"), ("ffma_kernel.cuh", "sk_fixup_kernel"),
-                  ("tc_gemm.cu", "sk_fixup_kernel"), ("tc_gemm.cu", "tc_gemm_kernel")]
+                  ("tc_gemm.cu", "sk_fixup_kernel"), ("tc_gemm.cu", "tc_gemm_kernel"),
+                  ("ffma_kernel.cuh", "ffma_gemm_kernel")]
     for f, name in dependents:
         body = _kernel_body(texts[f], name)
         assert body is not None, (f, name)
