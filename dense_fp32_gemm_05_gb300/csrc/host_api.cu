@@ -3,15 +3,22 @@
 //
 // K is cut into chunks: C = alpha*op(A)[:, K_0]*op(B)[K_0, :] + beta*C, then
 // C += alpha*op(A)[:, K_c]*op(B)[K_c, :] for each later chunk.  An internal
-// upload stream sends C (when beta != 0) and then each chunk's slices of A
-// and B; the caller's stream runs each chunk's GEMM (the selector's path, on
-// the whole M x N, so every chunk keeps full tile parallelism and splits only
+// upload stream sends C (when beta != 0) and then each chunk's slices of
+// op(A) and op(B); the caller's stream runs each chunk's GEMM (the selector's
+// path on rows x N: every chunk keeps its tile parallelism and splits only
 // its own slice of the operands) as soon as its slices have landed; the last
-// chunk runs in row blocks and an internal download stream sends each block
-// of C back as soon as it is final.  So the uploads overlap the computation
-// of earlier chunks and the download overlaps the last chunk.  Each chunk
-// after the first adds one fp32 rounding of C, well inside the 4*K*2^-24
-// bound.  The caller's stream finishes after the last download.
+// chunk runs in row blocks, and an internal download stream sends each block
+// of C home as soon as it is final.
+// With beta == 0, at least two chunks and M >= 4096, the rows of C are done
+// in two phases, top half then bottom half, because the link carries both
+// directions at once (measured on GB300: ~320 GB/s together against ~205 and
+// ~190 alone).  The first phase uploads op(B) and op(A)'s top rows chunk by
+// chunk and computes the top rows whole.  Their copy home then runs while
+// op(A)'s bottom rows come in, and the second phase computes those (op(B)
+// resident) in kPhase2Chunks chunks, its last in row blocks sent home as
+// above.  Each chunk after the first adds one fp32 rounding
+// of C, well inside the 4*K*2^-24 bound.  The caller's stream finishes after
+// the last download.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -27,12 +34,22 @@ namespace sgemm_gb300 {
 
 constexpr int kMaxChunks = 4;
 constexpr int kLastBlocks = 4;
+constexpr int kMaxPhases = 2;
+// The second phase sends only op(A)'s bottom rows (op(B) is resident), so its
+// GEMMs, not its copies, are the tail: fewer, larger ones there.  Measured on
+// GB300 against the one-phase pipeline (4096^3 NN 1.091 -> 1.025 ms, 6144 x
+// 4096 x 4096 TN 1.458 -> 1.317, 8192 x 2048 x 4096 1.248 -> 1.147); with 4
+// chunks and 4 row blocks there the gain was 0-8 %, with 1 chunk none.
+constexpr int kPhase2Chunks = 2;    // K-chunks of the second phase
+constexpr int kPhase2Blocks = 2;    // row blocks of its last chunk
+static_assert(kPhase2Chunks >= 1 && kPhase2Chunks <= kMaxChunks, "second-phase chunks");
+static_assert(kPhase2Blocks >= 1 && kPhase2Blocks <= kLastBlocks, "second-phase row blocks");
 
 struct HostPipe {
     bool ready = false;
     cudaStream_t up = nullptr, down = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t uploaded[kMaxChunks] = {}, computed[kLastBlocks] = {};
+    cudaEvent_t uploaded[kMaxPhases * kMaxChunks] = {}, computed[kMaxPhases * kLastBlocks] = {};
 };
 
 static std::mutex g_host_mu;                 // one enqueue at a time per process
@@ -47,9 +64,9 @@ static int host_pipe(HostPipe **out) {
                   cudaStreamCreateWithFlags(&h.down, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
                   cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess;
-        for (int i = 0; ok && i < kMaxChunks; ++i)
+        for (int i = 0; ok && i < kMaxPhases * kMaxChunks; ++i)
             ok = cudaEventCreateWithFlags(&h.uploaded[i], cudaEventDisableTiming) == cudaSuccess;
-        for (int i = 0; ok && i < kLastBlocks; ++i)
+        for (int i = 0; ok && i < kMaxPhases * kLastBlocks; ++i)
             ok = cudaEventCreateWithFlags(&h.computed[i], cudaEventDisableTiming) == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
@@ -85,7 +102,6 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
     // chunks of K (multiples of 32, at least 512 deep), whole when K is short
     int nk = need_ab ? (int)std::min<int64_t>(kMaxChunks, Ke / 512) : 1;
     nk = std::max(nk, 1);
-    const int64_t kc_full = ((Ke + nk - 1) / nk + 31) / 32 * 32;
 
     // device staging: the chunks of A and of B packed one after another, C (ld = N)
     auto up = [](size_t e) { return (e * 4 + 255) & ~size_t(255); };
@@ -107,65 +123,90 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
     if ((st = copy_status(cudaStreamWaitEvent(h->up, h->start, 0))) != SGEMM_OK) return st;
     if ((st = copy_status(cudaStreamWaitEvent(h->down, h->start, 0))) != SGEMM_OK) return st;
 
-    if (beta != 0.0f) {
-        st = copy_status(cudaMemcpy2DAsync(dC, N * 4, C, ldc * 4, N * 4, M,
-                                           cudaMemcpyHostToDevice, h->up));
-        if (st != SGEMM_OK) return st;
-    }
-
-    size_t a_off = 0, b_off = 0;
-    for (int c = 0; c < nk; ++c) {
-        const int64_t k0 = (int64_t)c * kc_full;
-        const int64_t kc = need_ab ? std::max<int64_t>(0, std::min<int64_t>(kc_full, Ke - k0)) : 0;
-        // the chunk's slices, packed: op(A)[:, k0:k0+kc] and op(B)[k0:k0+kc, :]
-        float *a_c = dA + a_off, *b_c = dB + b_off;
-        int64_t lda_c = a_n ? std::max<int64_t>(1, kc) : M;
-        int64_t ldb_c = b_n ? N : std::max<int64_t>(1, kc);
-        if (kc > 0) {
-            if (a_n)   // M rows, columns k0.. of each
-                st = copy_status(cudaMemcpy2DAsync(a_c, kc * 4, A + k0, lda * 4, kc * 4, M,
-                                                   cudaMemcpyHostToDevice, h->up));
-            else       // rows k0 .. k0+kc of the stored K x M array
-                st = copy_status(cudaMemcpy2DAsync(a_c, M * 4, A + k0 * lda, lda * 4, M * 4, kc,
-                                                   cudaMemcpyHostToDevice, h->up));
+    // phases: row ranges of C done one after the other.  Two only when C is
+    // not read (beta == 0): with beta != 0 the call's uploads grow by C and
+    // bound it, and a download beside them slows them (4096^3 NT, beta 0.5:
+    // 1.42 ms in one phase, 1.46-1.50 in two); and only from 4096 rows (at
+    // 2048 the halves' GEMMs are too small to gain).
+    const int nph = (need_ab && beta == 0.0f && nk >= 2 && M >= 4096) ? 2 : 1;
+    int64_t prow[kMaxPhases + 1] = {0, M, M};
+    if (nph == 2) prow[1] = (M / 2 + 127) / 128 * 128;
+    // op(B) staged in its stored shape (K x N for 'N', N x K for 'T'), so that
+    // any K range of it is one strided operand
+    const int64_t ldb_d = b_n ? N : std::max<int64_t>(1, Ke);
+    auto b_at = [&](int64_t k0) { return b_n ? dB + k0 * N : dB + k0; };
+    size_t a_off = 0;
+    for (int ph = 0; ph < nph; ++ph) {
+        const int64_t r0 = prow[ph], rows = prow[ph + 1] - prow[ph];
+        // the second phase's operands are short to send (op(B) is resident):
+        // fewer, larger GEMMs there
+        const int nkp = ph == 0 ? nk : std::max(1, std::min(nk, kPhase2Chunks));
+        const int64_t kcp = ((Ke + nkp - 1) / nkp + 31) / 32 * 32;
+        if (beta != 0.0f) {
+            st = copy_status(cudaMemcpy2DAsync(dC + r0 * N, N * 4, C + r0 * ldc, ldc * 4, N * 4, rows,
+                                               cudaMemcpyHostToDevice, h->up));
             if (st != SGEMM_OK) return st;
-            if (b_n)   // rows k0 .. k0+kc of the stored K x N array
-                st = copy_status(cudaMemcpy2DAsync(b_c, N * 4, B + k0 * ldb, ldb * 4, N * 4, kc,
-                                                   cudaMemcpyHostToDevice, h->up));
-            else       // N rows, columns k0.. of each
-                st = copy_status(cudaMemcpy2DAsync(b_c, kc * 4, B + k0, ldb * 4, kc * 4, N,
-                                                   cudaMemcpyHostToDevice, h->up));
-            if (st != SGEMM_OK) return st;
-            a_off += (size_t)M * kc;
-            b_off += (size_t)kc * N;
         }
-        if ((st = copy_status(cudaEventRecord(h->uploaded[c], h->up))) != SGEMM_OK) return st;
-        if ((st = copy_status(cudaStreamWaitEvent(s, h->uploaded[c], 0))) != SGEMM_OK) return st;
-        const float beta_c = c == 0 ? beta : 1.0f;
-        const float *a_arg = kc > 0 ? a_c : nullptr, *b_arg = kc > 0 ? b_c : nullptr;
-        if (c + 1 < nk) {
-            st = gemm_impl(transA, transB, M, N, kc, alpha, a_arg, lda_c, b_arg, ldb_c, beta_c,
-                           dC, N, s, SGEMM_PATH_AUTO, 0);
-            if (st != SGEMM_OK) return st;
-            continue;
-        }
-        // last chunk: row blocks, each sent home as soon as it is final
-        const int nb = (int)std::max<int64_t>(1, std::min<int64_t>(kLastBlocks, M / 512));
-        const int64_t per = ((M + nb - 1) / nb + 127) / 128 * 128;
-        for (int b = 0; b < nb; ++b) {
-            const int64_t r0 = (int64_t)b * per;
-            if (r0 >= M) break;
-            const int64_t rows = std::min<int64_t>(per, M - r0);
-            const float *a_blk = a_arg ? (a_n ? a_arg + r0 * lda_c : a_arg + r0) : nullptr;
-            st = gemm_impl(transA, transB, rows, N, kc, alpha, a_blk, a_n ? lda_c : M, b_arg,
-                           ldb_c, beta_c, dC + r0 * N, N, s, SGEMM_PATH_AUTO, 0);
-            if (st != SGEMM_OK) return st;
-            if ((st = copy_status(cudaEventRecord(h->computed[b], s))) != SGEMM_OK) return st;
-            if ((st = copy_status(cudaStreamWaitEvent(h->down, h->computed[b], 0))) != SGEMM_OK)
-                return st;
-            st = copy_status(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * N, N * 4, N * 4,
-                                               rows, cudaMemcpyDeviceToHost, h->down));
-            if (st != SGEMM_OK) return st;
+        for (int c = 0; c < nkp; ++c) {
+            const int64_t k0 = (int64_t)c * kcp;
+            const int64_t kc = need_ab ? std::max<int64_t>(0, std::min<int64_t>(kcp, Ke - k0)) : 0;
+            // the chunk's slices: op(A)[r0:r0+rows, k0:k0+kc] packed, and
+            // (first phase) op(B)[k0:k0+kc, :] into its place
+            float *a_c = dA + a_off;
+            const int64_t lda_c = a_n ? std::max<int64_t>(1, kc) : rows;
+            if (kc > 0) {
+                if (a_n)   // rows r0.. of A, columns k0..
+                    st = copy_status(cudaMemcpy2DAsync(a_c, kc * 4, A + r0 * lda + k0, lda * 4, kc * 4,
+                                                       rows, cudaMemcpyHostToDevice, h->up));
+                else       // rows k0 .. k0+kc of the stored K x M array, columns r0..
+                    st = copy_status(cudaMemcpy2DAsync(a_c, rows * 4, A + k0 * lda + r0, lda * 4,
+                                                       rows * 4, kc, cudaMemcpyHostToDevice, h->up));
+                if (st != SGEMM_OK) return st;
+                a_off += (size_t)rows * kc;
+                if (ph == 0) {
+                    if (b_n)   // rows k0 .. k0+kc of the stored K x N array
+                        st = copy_status(cudaMemcpy2DAsync(b_at(k0), N * 4, B + k0 * ldb, ldb * 4,
+                                                           N * 4, kc, cudaMemcpyHostToDevice, h->up));
+                    else       // N rows, columns k0.. of each
+                        st = copy_status(cudaMemcpy2DAsync(b_at(k0), ldb_d * 4, B + k0, ldb * 4, kc * 4,
+                                                           N, cudaMemcpyHostToDevice, h->up));
+                    if (st != SGEMM_OK) return st;
+                }
+            }
+            cudaEvent_t up_ev = h->uploaded[ph * kMaxChunks + c];
+            if ((st = copy_status(cudaEventRecord(up_ev, h->up))) != SGEMM_OK) return st;
+            if ((st = copy_status(cudaStreamWaitEvent(s, up_ev, 0))) != SGEMM_OK) return st;
+            const float beta_c = c == 0 ? beta : 1.0f;
+            const float *a_arg = kc > 0 ? a_c : nullptr, *b_arg = kc > 0 ? b_at(k0) : nullptr;
+            float *c_ph = dC + r0 * N;
+            if (c + 1 < nkp) {
+                st = gemm_impl(transA, transB, rows, N, kc, alpha, a_arg, lda_c, b_arg, ldb_d, beta_c,
+                               c_ph, N, s, SGEMM_PATH_AUTO, 0);
+                if (st != SGEMM_OK) return st;
+                continue;
+            }
+            // last chunk: the first phase whole (its copy home runs under the
+            // next phase's uploads), the last phase in row blocks, each sent
+            // home as soon as it is final
+            const int nbmax = nph == 1 ? kLastBlocks : kPhase2Blocks;
+            const int nb = ph + 1 < nph ? 1
+                                        : (int)std::max<int64_t>(1, std::min<int64_t>(nbmax, rows / 512));
+            const int64_t per = ((rows + nb - 1) / nb + 127) / 128 * 128;
+            for (int b = 0; b < nb; ++b) {
+                const int64_t q0 = (int64_t)b * per;
+                if (q0 >= rows) break;
+                const int64_t qn = std::min<int64_t>(per, rows - q0);
+                const float *a_blk = a_arg ? (a_n ? a_arg + q0 * lda_c : a_arg + q0) : nullptr;
+                st = gemm_impl(transA, transB, qn, N, kc, alpha, a_blk, lda_c, b_arg, ldb_d, beta_c,
+                               c_ph + q0 * N, N, s, SGEMM_PATH_AUTO, 0);
+                if (st != SGEMM_OK) return st;
+                cudaEvent_t done_ev = h->computed[ph * kLastBlocks + b];
+                if ((st = copy_status(cudaEventRecord(done_ev, s))) != SGEMM_OK) return st;
+                if ((st = copy_status(cudaStreamWaitEvent(h->down, done_ev, 0))) != SGEMM_OK) return st;
+                st = copy_status(cudaMemcpy2DAsync(C + (r0 + q0) * ldc, ldc * 4, c_ph + q0 * N, N * 4,
+                                                   N * 4, qn, cudaMemcpyDeviceToHost, h->down));
+                if (st != SGEMM_OK) return st;
+            }
         }
     }
     if ((st = copy_status(cudaEventRecord(h->done, h->down))) != SGEMM_OK) return st;

@@ -2,8 +2,10 @@
 computation in K-chunks and row blocks.  Checked against the oracle (within
 the fp32 bound) for every layout, beta != 0, odd leading dimensions,
 page-locked and pageable buffers, shapes that make one, several and ragged
-row blocks, and K long enough for 2 to 4 chunks (each chunk after the first
-adds into C with beta = 1; the last chunk may be shorter)."""
+row blocks, K long enough for 2 to 4 chunks (each chunk after the first
+adds into C with beta = 1; the last chunk may be shorter), and the two-phase
+form (beta = 0 and M >= 4096: the top rows of C computed and sent home while
+the bottom rows' operands still arrive)."""
 import numpy as np
 import pytest
 
@@ -40,6 +42,10 @@ def stored(op_mat, trans, pad):
     (2100, 520, 2050, 1.0, 0.5, 3, True),        # 4 chunks of 544, 544, 544, 418
     (1537, 1025, 1500, -1.0, 1.0, 1, False),     # 2 chunks (768, 732), pageable
     (700, 300, 1024, 1.0, 0.0, 0, True),         # 2 equal chunks, beta = 0 over NaN
+    # two row phases (beta = 0, M >= 4096): top rows, then bottom rows in
+    # 2 chunks whose last runs in 2 row blocks
+    (4100, 130, 1100, -1.0, 0.0, 2, True),       # first phase 2 chunks (544, 544 + 12)
+    (4097, 64, 2050, 1.0, 0.0, 0, False),        # 4 chunks then 2, pageable
 ])
 def test_host_api_matches_oracle(oracle_mod, ta, tb, M, N, K, alpha, beta, pad, pinned):
     import torch
