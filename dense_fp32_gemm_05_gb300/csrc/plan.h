@@ -197,14 +197,20 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         pl.tile_m = 128;
         pl.tile_n = N > 128 ? 256 : (N > 64 ? 128 : 64);
         pl.split = 1;
-        // Splitting an operand in shared memory saves its pre-pass (12 bytes
-        // of HBM traffic per element) but slows the main loop by ~10 %; the
-        // pre-pass of A costs ~285/N of the tensor work (at the measured HBM
-        // and TF32 rates), so A is split in the kernel when N <= 2048, B when
-        // M <= 2048, and only when the operand is K-contiguous and 16-byte
-        // aligned (TMA reads it raw).
+        // Splitting an operand in the kernel saves its pre-pass (12 bytes of
+        // HBM traffic per element) but slows the main loop; the pre-pass of A
+        // costs ~285/N of the tensor work (at the measured HBM and TF32
+        // rates), so A is split in the kernel (into TMEM) when N <= 2048, and
+        // only when the operand is K-contiguous and 16-byte aligned (TMA reads
+        // it raw).  B's split lands in shared memory, beside the MMAs' own
+        // operand reads, and the split warps then carry both operands: on
+        // wide tiles it pays only up to M = 1024 (measured on GB300, split in
+        // the kernel against the pre-pass: 2048^3 NT 101.0 against 78.5 us, TT
+        // 104.1 against 84.6, 1536 x 4096 x 1536 NT 127.6 against 93.8;
+        // 1024^3 and below equal or slightly ahead).  A narrow B (N <= 128:
+        // 64 or 128 rows per stage) stays split in the kernel at any M.
         pl.fuse_a = N <= 2048 && is_notrans(ta) && a_al && lda % 4 == 0;
-        pl.fuse_b = M <= 2048 && is_trans(tb) && b_al && ldb % 4 == 0;
+        pl.fuse_b = (M <= 1024 || N <= 128) && M <= 2048 && is_trans(tb) && b_al && ldb % 4 == 0;
         // 256-row tiles on an SM pair when both operands come pre-split and
         // M fills them: each SM holds half of B, a third less shared-memory
         // traffic per flop (+6 % at 4096^3 and 8192^3 on GB300).  With an

@@ -400,3 +400,21 @@ def test_ffma_pre_transpose_selector():
                        (("N", "T", 4, 4096, 4096, 4096, 4096, 4096), sg.PATH_AUTO)]:
         st, info = sg.sgemm_plan_detail(*args, path=path)
         assert st == 0 and info["pre_transpose"] == 0, (args, info)
+
+
+def test_b_split_in_the_kernel_only_for_short_m_or_narrow_n():
+    """B (K-contiguous) is split in shared memory inside the tensor-core
+    kernel only up to M = 1024, or for a narrow B (N <= 128, M <= 2048);
+    wider problems take the pre-pass (measured faster from M = 1536 on)."""
+    cases = [(("N", "T", 1024, 1024, 1024, 1024, 1024, 1024), 1, 1),
+             (("N", "T", 2048, 2048, 2048, 2048, 2048, 2048), 1, 0),
+             (("N", "T", 1536, 4096, 1536, 1536, 1536, 4096), 0, 0),
+             (("N", "T", 2048, 64, 8192, 8192, 8192, 64), 1, 1),
+             (("N", "T", 16384, 64, 8192, 8192, 8192, 64), 1, 0),
+             (("T", "T", 2048, 1024, 2048, 2048, 2048, 1024), 0, 0)]
+    for args, fa, fb in cases:
+        st, d = sg.sgemm_plan_detail(*args, path=sg.PATH_3XTF32)
+        assert st == 0 and (d["fuse_a"], d["fuse_b"]) == (fa, fb), (args, d)
+    # both operands pre-split and enough rows: the SM-pair kernel
+    st, d = sg.sgemm_plan_detail("T", "T", 2048, 1024, 2048, 2048, 2048, 1024)
+    assert st == 0 and d["pair"] == 1
