@@ -73,6 +73,9 @@ constexpr double kSmallFlops = 1.2e8;
 // The FFMA tile path copies a K-contiguous operand transposed first when the
 // other side of the problem is at least this long (see make_plan).
 constexpr int64_t kFfmaTransposeMin = 2048;
+// Stream-K over every tensor-core tile stays open at any grid fill while the
+// operands, as the kernel reads them, fit in this much of L2 (see make_plan).
+constexpr double kStreamKL2Bytes = 96e6;
 constexpr int64_t kSmallMaxK = 512;
 constexpr int64_t kSmallMaxTiles = 1024;
 
@@ -207,10 +210,14 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // wide tiles it pays only up to M = 1024 (measured on GB300, split in
         // the kernel against the pre-pass: 2048^3 NT 101.0 against 78.5 us, TT
         // 104.1 against 84.6, 1536 x 4096 x 1536 NT 127.6 against 93.8;
-        // 1024^3 and below equal or slightly ahead).  A narrow B (N <= 128:
-        // 64 or 128 rows per stage) stays split in the kernel at any M.
+        // 1024^3 and below equal or slightly ahead; 2048 x 512 x 8192 NT
+        // 100.5 against 85.7).  A narrow B (N <= 128: 64 or 128 rows per
+        // stage), or a problem under a GFLOP, whose pre-pass launch would
+        // cost more than the split (1536 x 256 x 256 NT 17.1 against 19.1),
+        // stays split in the kernel up to M = 2048.
         pl.fuse_a = N <= 2048 && is_notrans(ta) && a_al && lda % 4 == 0;
-        pl.fuse_b = (M <= 1024 || N <= 128) && M <= 2048 && is_trans(tb) && b_al && ldb % 4 == 0;
+        pl.fuse_b = (M <= 1024 || N <= 128 || 2.0 * (double)M * (double)N * (double)K < 1e9) &&
+                    M <= 2048 && is_trans(tb) && b_al && ldb % 4 == 0;
         // 256-row tiles on an SM pair when both operands come pre-split and
         // M fills them: each SM holds half of B, a third less shared-memory
         // traffic per flop (+6 % at 4096^3 and 8192^3 on GB300).  With an
@@ -282,12 +289,34 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         // stream-K with min(s x tiles, 8 x SMs, iterations) CTAs; split = 1
         // never does.
         const int64_t nkb = kp / ((three && !(pl.tile_n <= 128 && pl.fuse_a)) ? 16 : 32);
-        const int64_t tiles1 = ((M + 127) / 128) * ((N + pl.tile_n - 1) / pl.tile_n);
+        const int64_t tm1 = (M + 127) / 128, tn1 = (N + pl.tile_n - 1) / pl.tile_n;
+        const int64_t tiles1 = tm1 * tn1;
+        // Whole tiles instead of stream-K over every tile, an empirical rule:
+        // ranges that start at scattered k positions share no operand panel
+        // with their neighbours in L2.  Whole tiles won where they already
+        // fill >= 60 % of the SMs, the panels that tiles share (A's across a
+        // tile row, B's down a tile column, as the kernel reads them) do not
+        // fit in L2, and the grid has at least as many tile rows as columns,
+        // and 4 columns or more.  Measured on GB300, whole tiles against
+        // stream-K, us (NN unless noted):
+        //   * won: 2048 x 2048 x 8192 286 / 393; 3072 x 1280 x 8192 270 /
+        //     320; 1536 x 2048 x 8192 286 / 309; 4096 x 1024 x 8192 265 /
+        //     276;
+        //   * lost: TT 768 x 4096 x 8192 345 / 257; NT 1024 x 4096 x 8192
+        //     349 / 328; 8192 x 512 x 8192 264 / 249; 1280 x 2048 x 8192
+        //     (80 tiles) 286 / 270; 1280 x 2048 x 4096 (operands in L2) 150 /
+        //     118;
+        //   * even: 2048 x 1536 x 8192 274 / 270.
+        const double shared_operand_bytes =
+            (tn1 > 1 ? (double)M * kp * (pl.fuse_a ? 4 : (three ? 8 : 4)) : 0.0) +
+            (tm1 > 1 ? (double)N * kp * (pl.fuse_b ? 4 : (three ? 8 : 4)) : 0.0);
+        const bool whole_fills = 5 * tiles1 >= 3 * sms && shared_operand_bytes > kStreamKL2Bytes &&
+                                 tm1 >= tn1 && tn1 >= 4;
         const int64_t iters = tiles1 * nkb;
         int64_t g_sk = 0;
         if (split > 1) {
             g_sk = std::min<int64_t>(std::min<int64_t>(tiles1 * split, 8LL * sms), iters);
-        } else if (split == 0 && tiles1 < sms) {
+        } else if (split == 0 && tiles1 < sms && !whole_fills) {
             // g CTAs: most ranges straddle two tiles (two partial epilogues,
             // back to back where A is split into TMEM); a multiple of the
             // tile count keeps every range inside one tile (one epilogue)

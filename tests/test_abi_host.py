@@ -404,17 +404,40 @@ def test_ffma_pre_transpose_selector():
 
 def test_b_split_in_the_kernel_only_for_short_m_or_narrow_n():
     """B (K-contiguous) is split in shared memory inside the tensor-core
-    kernel only up to M = 1024, or for a narrow B (N <= 128, M <= 2048);
-    wider problems take the pre-pass (measured faster from M = 1536 on)."""
+    kernel only up to M = 1024, or up to M = 2048 for a narrow B (N <= 128)
+    or a problem under a GFLOP; wider problems take the pre-pass (measured
+    faster from M = 1536 on)."""
     cases = [(("N", "T", 1024, 1024, 1024, 1024, 1024, 1024), 1, 1),
              (("N", "T", 2048, 2048, 2048, 2048, 2048, 2048), 1, 0),
              (("N", "T", 1536, 4096, 1536, 1536, 1536, 4096), 0, 0),
              (("N", "T", 2048, 64, 8192, 8192, 8192, 64), 1, 1),
              (("N", "T", 16384, 64, 8192, 8192, 8192, 64), 1, 0),
-             (("T", "T", 2048, 1024, 2048, 2048, 2048, 1024), 0, 0)]
+             (("T", "T", 2048, 1024, 2048, 2048, 2048, 1024), 0, 0),
+             # under a GFLOP the pre-pass launch costs more than the split
+             (("N", "T", 1536, 256, 256, 256, 256, 256), 1, 1)]
     for args, fa, fb in cases:
         st, d = sg.sgemm_plan_detail(*args, path=sg.PATH_3XTF32)
         assert st == 0 and (d["fuse_a"], d["fuse_b"]) == (fa, fb), (args, d)
     # both operands pre-split and enough rows: the SM-pair kernel
     st, d = sg.sgemm_plan_detail("T", "T", 2048, 1024, 2048, 2048, 2048, 1024)
     assert st == 0 and d["pair"] == 1
+
+
+def test_stream_k_over_every_tile_only_when_it_pays():
+    """Stream-K over every tile (single SMs), or whole tiles: whole tiles only
+    where they already fill >= 60 % of the SMs, the operand panels that tiles
+    share do not fit in L2, and the tile grid is at least as tall as wide
+    with 4 columns or more (the measured cases of the selector's comment)."""
+    cases = [(("N", "N"), (2048, 2048, 8192), 0), (("N", "N"), (3072, 1280, 8192), 0),
+             (("N", "N"), (4096, 1024, 8192), 0), (("T", "T"), (768, 4096, 8192), 152),
+             (("N", "T"), (1024, 4096, 8192), 152), (("N", "N"), (8192, 512, 8192), 152),
+             (("N", "N"), (1280, 2048, 8192), 152), (("N", "N"), (1280, 2048, 4096), 152),
+             (("N", "T"), (16384, 64, 8192), 152), (("N", "N"), (1024, 1024, 1024), 128)]
+    for (ta, tb), (M, N, K), sk in cases:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N)
+        assert st == 0 and d["sk_ctas"] == sk, ((ta, tb, M, N, K), d)
+    # a forced split still shares the k-blocks
+    st, d = sg.sgemm_plan_detail("N", "N", 2048, 2048, 8192, 8192, 2048, 2048, split=2)
+    assert st == 0 and d["sk_ctas"] > 0

@@ -99,6 +99,8 @@ CASES = [
     ("N", "N", 300, 260, 700, sg.PATH_FFMA, 1, "FFMA, whole tiles"),
     ("T", "T", 100, 77, 300, sg.PATH_AUTO, 0, "FFMA, small-problem kernel"),
     ("T", "N", 300, 260, 700, sg.PATH_FFMA, 3, "FFMA, split-K"),
+    ("N", "T", 300, 2100, 700, sg.PATH_FFMA, 1, "FFMA, A copied transposed first"),
+    ("T", "T", 2100, 130, 700, sg.PATH_FFMA, 1, "FFMA, B copied transposed first"),
     ("N", "T", 8, 700, 500, sg.PATH_GEMV, 0, "thin problem, dot form"),
     ("N", "N", 16, 700, 500, sg.PATH_GEMV, 0, "thin problem on the tensor cores"),
     ("T", "N", 700, 8, 500, sg.PATH_GEMV, 0, "thin problem, axpy form"),
