@@ -1,4 +1,4 @@
-// Thin GEMMs: min(M, N) <= 16 (SGEMM_PATH_GEMV).
+// Thin GEMMs: min(M, N) <= 16, or <= 32 on the tensor cores (SGEMM_PATH_GEMV).
 //
 // "Matmul II: register blocking, warp tiling, tensor cores", section 8
 // ("What cuBLAS does that we do not"): when M is 1 (decode) to a few dozen,
@@ -677,16 +677,16 @@ int last_cuda_status() {
 
 }  // namespace
 
-// The thin path's tensor-core form (tc_thin_kernel) takes S >= kThinTcMinS
-// with the large operand's rows along the long dimension, 16-byte aligned
-// with a leading dimension that is a multiple of 4.
+// The thin path's tensor-core form (tc_thin_kernel) takes kThinTcMinS <= S
+// <= kThinTcMaxS with the large operand's rows along the long dimension,
+// 16-byte aligned with a leading dimension that is a multiple of 4.
 bool thin_on_tensor_cores(char ta, char tb, int64_t M, int64_t N, int64_t lda, int64_t ldb,
                           bool a_al, bool b_al) {
     const bool rows_thin = M <= N;
     const int64_t S = rows_thin ? M : N;
     const bool big_mn = rows_thin ? is_notrans(tb) : !is_notrans(ta);
     const bool big_al = rows_thin ? (b_al && ldb % 4 == 0) : (a_al && lda % 4 == 0);
-    return S >= kThinTcMinS && S <= kGemvMaxSmall && big_mn && big_al;
+    return S >= kThinTcMinS && S <= kThinTcMaxS && big_mn && big_al;
 }
 
 // Its grid: one CTA per SM and 128 columns p; K split by the same waves x (k
@@ -788,7 +788,9 @@ int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda, in
 int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
              int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
              cudaStream_t s, int sms, const Epilogue &epi) {
-    if (std::min(M, N) > kGemvMaxSmall) return SGEMM_ERR_UNSUPPORTED;
+    // S above the CUDA-core forms' 16 only on the tensor cores
+    const bool tc_form = thin_on_tensor_cores(ta, tb, M, N, lda, ldb, al16(A), al16(B));
+    if (std::min(M, N) > (tc_form ? kThinTcMaxS : kGemvMaxSmall)) return SGEMM_ERR_UNSUPPORTED;
     const bool a_n = is_notrans(ta), b_n = is_notrans(tb);
     gemv::Params p{};
     p.K = (int)K;
@@ -837,8 +839,7 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
         timing_mark(s, false);
         return last_cuda_status();
     }
-    if (thin_on_tensor_cores(ta, tb, M, N, lda, ldb, al16(A), al16(B)) &&
-        (p.small_sk == 1 || p.small_ss == 1)) {
+    if (tc_form && (p.small_sk == 1 || p.small_ss == 1)) {
         const ThinTc tg = thin_tc_geometry(p.P, K, sms);
         ThinCall tcall{};
         tcall.S = p.S; tcall.P = p.P; tcall.K = p.K;
@@ -867,6 +868,7 @@ int run_gemv(char ta, char tb, int64_t M, int64_t N, int64_t K, float alpha, con
             return last_cuda_status();
         }
     }
+    if (p.S > kGemvMaxSmall) return SGEMM_ERR_UNSUPPORTED;   // the CUDA-core forms take S <= 16
     p.kchunk = g.kchunk;
     p.ksplit = g.ksplit;
     if (p.ksplit > 1) {

@@ -99,8 +99,18 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
     const bool big_kcontig = M <= N ? !is_notrans(tb) : is_notrans(ta);
     const bool big_al = M <= N ? (b_al && ldb % 4 == 0) : (a_al && lda % 4 == 0);
     const bool thin_on_tc = thin > 4 && big_kcontig && big_al && K >= 32;
-    if (path == SGEMM_PATH_GEMV || (path == SGEMM_PATH_AUTO && thin <= 16 && !thin_on_tc)) {
-        if (std::min(M, N) > 16) return SGEMM_ERR_UNSUPPORTED;
+    // 16 < S <= 32 with the large operand's rows along the long side, aligned:
+    // the thin path's tensor-core form (its MMAs cost the same up to S = 32),
+    // where the tile path would compute mostly padding and pre-split the
+    // whole large operand.  K >= 32 as for the tensor cores in general.
+    const bool tc_form = thin >= 12 && thin <= 32 && !big_kcontig && big_al;   // as run_gemv's
+    const bool small = 2.0 * (double)M * (double)N * (double)K <= kSmallFlops && K <= kSmallMaxK &&
+                       ((M + 15) / 16) * ((N + 15) / 16) <= kSmallMaxTiles;
+    // (problems small enough for the one-launch FFMA kernel stay there)
+    const bool thin_tc_wide = thin > 16 && tc_form && K >= 32 && !small;
+    if (path == SGEMM_PATH_GEMV ||
+        (path == SGEMM_PATH_AUTO && ((thin <= 16 && !thin_on_tc) || thin_tc_wide))) {
+        if (thin > 16 && !tc_form) return SGEMM_ERR_UNSUPPORTED;
         pl.path = SGEMM_PATH_GEMV;
         pl.tile_m = (int)std::min(M, N);
         pl.tile_n = 0;
@@ -109,8 +119,6 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
         *out = pl;
         return 0;
     }
-    const bool small = 2.0 * (double)M * (double)N * (double)K <= kSmallFlops && K <= kSmallMaxK &&
-                       ((M + 15) / 16) * ((N + 15) / 16) <= kSmallMaxTiles;
     if ((path == SGEMM_PATH_AUTO || path == SGEMM_PATH_FFMA) && small && split <= 1) {
         // One launch of 16 x 16 tiles, every output summed in ascending k
         // (ffma_small.cuh): below the crossover the fixed costs of the

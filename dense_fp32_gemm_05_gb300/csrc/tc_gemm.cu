@@ -1053,7 +1053,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- thin problems
-// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 16 outputs per column of a
+// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 32 outputs per column of a
 // large operand Big whose rows run along P in memory (Big(p, k) at
 // big[k ld + p]: decode's weights stored [K][N], or a transposed matrix
 // times a few vectors).  On the CUDA cores each element of Big feeds S FMAs,
@@ -1067,11 +1067,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 //     turn it around into the K-major 128-byte-swizzled layout of an MMA
 //     operand (128 rows p x 32 k), in a ring of THIN_OPS operand stages;
 //   * Small, split by the pre-pass into [S][Kp] hi and lo, comes by TMA as a
-//     64-row operand per stage: rows 0..15 Small_hi, 16..31 Small_lo (rows past
-//     S read as zeros), 32..63 zeros;
+//     64-row operand per stage: rows 0..31 Small_hi, 32..63 Small_lo (rows past
+//     S read as zeros), so any S up to 32 costs the same MMAs;
 //   * per 8 k the MMA thread issues Big_hi x that operand into D1 (columns
-//     0..15 hi*hi, 16..31 hi*lo) and Big_lo x it into D2 (columns 0..15
-//     lo*hi; 16..31, lo*lo, unused), M = 128, N = 64, K = 8.  Each of the
+//     0..31 hi*hi, 32..63 hi*lo) and Big_lo x it into D2 (columns 0..31
+//     lo*hi; 32..63, lo*lo, unused), M = 128, N = 64, K = 8.  Each of the
 //     4 k-slices of a block has its own D1 and D2 (8 accumulators of 64
 //     columns), which halves the error against one pair;
 //   * the epilogue adds each product's 4 accumulators, then hi*hi + (lo*hi
@@ -1085,6 +1085,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // room for only two raw stages: measured slower (16 x 16384 x 8192 NN 154 ->
 // 165 us).
 constexpr int THIN_P = 128;            // columns p per CTA (the MMA's M)
+constexpr int THIN_SMAX = 32;          // rows of Small per part in the operand (S <= 32)
 constexpr int THIN_K = 32;             // k per block
 constexpr int THIN_RAW = 6;            // raw tile stages (16 KB)
 constexpr int THIN_OPS = 3;            // operand stages (Big_hi, Big_lo, Small: 40 KB)
@@ -1188,13 +1189,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                      :: "r"(smem_u32(tmem_slot)), "r"(512) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // rows 32..63 of every Small operand stay zero (TMA fills rows 0..31)
-    for (int i = threadIdx.x; i < O * 32 * THIN_K / 4; i += THREADS) {
-        const int o = i / (32 * THIN_K / 4), e = i % (32 * THIN_K / 4);
-        asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};"
-                     :: "r"(b_at(o) + (uint32_t)(32 * THIN_K * 4 + 16 * e)), "f"(0.0f) : "memory");
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1219,9 +1213,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (gb < nblk && mbar_test(op_empty(gb % O), ((uint32_t)(gb / O) & 1u) ^ 1u)) {
                     const int o = gb % O;
-                    mbar_expect_tx(op_bfull(o), 2u * 16u * THIN_K * 4u);
+                    // both parts' boxes are THIN_SMAX rows; rows past S are zero-filled
+                    mbar_expect_tx(op_bfull(o), 2u * THIN_SMAX * THIN_K * 4u);
                     tma_load_2d(b_at(o), &tm_shi, op_bfull(o), k0 + gb * THIN_K, 0);
-                    tma_load_2d(b_at(o) + 16u * THIN_K * 4u, &tm_slo, op_bfull(o), k0 + gb * THIN_K, 0);
+                    tma_load_2d(b_at(o) + (uint32_t)(THIN_SMAX * THIN_K * 4), &tm_slo, op_bfull(o),
+                                k0 + gb * THIN_K, 0);
                     ++gb;
                     moved = true;
                 }
@@ -1306,70 +1302,73 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) mbar_arrive(op_ready(o));
         }
         // ---- epilogue: warp w reads TMEM lanes 32 (w % 4).. (its 32 columns
-        // p) and s = 8 half .. + 7; out = hi*hi + (lo*hi + hi*lo)
+        // p) and s = 16 half .. + 15, 8 at a time; out = hi*hi + (lo*hi + hi*lo)
         const bool ready = ok && mbar_wait(accf, 0u, lim);
         tc_fence_after();
         if (ready) {
             const int q = warp & 3, half = (warp - 2) >> 2;
             const int pp = p0 + q * 32 + lane;
-            const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 8);
-            // each product summed over the 4 k-slice accumulators, in slice order
-            float hh[8], hl[8], lh[8];
+#pragma unroll 1
+            for (int s0 = 16 * half; s0 < 16 * half + 16 && s0 < p.S; s0 += 8) {   // warp-uniform
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)s0;
+                // each product summed over the 4 k-slice accumulators, in slice order
+                float hh[8], hl[8], lh[8];
 #pragma unroll
-            for (int kk = 0; kk < THIN_K / 8; ++kk) {
-                uint32_t a[8], b[8], c[8];
-                const uint32_t tk = ta + (uint32_t)(128 * kk);
-                tmem_ld8(tk, a);
-                tmem_ld8(tk + 16u, b);
-                tmem_ld8(tk + 64u, c);
+                for (int kk = 0; kk < THIN_K / 8; ++kk) {
+                    uint32_t a[8], b[8], c[8];
+                    const uint32_t tk = ta + (uint32_t)(128 * kk);
+                    tmem_ld8(tk, a);
+                    tmem_ld8(tk + (uint32_t)THIN_SMAX, b);
+                    tmem_ld8(tk + 64u, c);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    hh[e] = kk == 0 ? __uint_as_float(a[e]) : __fadd_rn(hh[e], __uint_as_float(a[e]));
-                    hl[e] = kk == 0 ? __uint_as_float(b[e]) : __fadd_rn(hl[e], __uint_as_float(b[e]));
-                    lh[e] = kk == 0 ? __uint_as_float(c[e]) : __fadd_rn(lh[e], __uint_as_float(c[e]));
-                }
-            }
-            float v[8];
-            bool nan = false;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                v[e] = __fadd_rn(hh[e], __fadd_rn(lh[e], hl[e]));
-                nan |= v[e] != v[e];
-            }
-            // NaN sums (a split of an infinity, or of a value that rounds to
-            // one) are redone in fp32 by the warp, one output at a time
-            uint32_t bad = 0;
-            if (pp < p.P)
-                for (int e = 0; e < 8; ++e)
-                    if (half * 8 + e < p.S && v[e] != v[e]) bad |= 1u << e;
-            if (__any_sync(0xffffffffu, nan)) {
-                while (true) {
-                    const uint32_t lanes = __ballot_sync(0xffffffffu, bad != 0);
-                    if (lanes == 0) break;
-                    const int src = __ffs(lanes) - 1;
-                    const int e = __ffs(__shfl_sync(0xffffffffu, bad, src)) - 1;
-                    const float d = thin_dot_fp32_warp(p, half * 8 + e, p0 + q * 32 + src, k0, k1, lane);
-                    if (lane == src) {
-                        v[e] = d;
-                        bad &= ~(1u << e);
+                    for (int e = 0; e < 8; ++e) {
+                        hh[e] = kk == 0 ? __uint_as_float(a[e]) : __fadd_rn(hh[e], __uint_as_float(a[e]));
+                        hl[e] = kk == 0 ? __uint_as_float(b[e]) : __fadd_rn(hl[e], __uint_as_float(b[e]));
+                        lh[e] = kk == 0 ? __uint_as_float(c[e]) : __fadd_rn(lh[e], __uint_as_float(c[e]));
                     }
                 }
-            }
-            if (pp < p.P) {
+                float v[8];
+                bool nan = false;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int sidx = half * 8 + e;
-                    if (sidx >= p.S) break;
-                    if (p.ksplit > 1) {
-                        p.partial[((int64_t)blockIdx.y * p.S + sidx) * p.P + pp] = v[e];
-                        continue;
+                    v[e] = __fadd_rn(hh[e], __fadd_rn(lh[e], hl[e]));
+                    nan |= v[e] != v[e];
+                }
+                // NaN sums (a split of an infinity, or of a value that rounds to
+                // one) are redone in fp32 by the warp, one output at a time
+                uint32_t bad = 0;
+                if (pp < p.P)
+                    for (int e = 0; e < 8; ++e)
+                        if (s0 + e < p.S && v[e] != v[e]) bad |= 1u << e;
+                if (__any_sync(0xffffffffu, nan)) {
+                    while (true) {
+                        const uint32_t lanes = __ballot_sync(0xffffffffu, bad != 0);
+                        if (lanes == 0) break;
+                        const int src = __ffs(lanes) - 1;
+                        const int e = __ffs(__shfl_sync(0xffffffffu, bad, src)) - 1;
+                        const float d = thin_dot_fp32_warp(p, s0 + e, p0 + q * 32 + src, k0, k1, lane);
+                        if (lane == src) {
+                            v[e] = d;
+                            bad &= ~(1u << e);
+                        }
                     }
-                    float *dst = p.C + (int64_t)sidx * p.c_s + (int64_t)pp * p.c_p;
-                    const int crow = p.rows_thin ? sidx : pp, ccol = p.rows_thin ? pp : sidx;
-                    const float a = epi_alpha(p.alpha, p.row_scale, crow);
-                    const float tt = p.beta == 0.0f ? __fmul_rn(a, v[e])
-                                                    : __fmaf_rn(a, v[e], __fmul_rn(p.beta, *dst));
-                    *dst = epi_tail(tt, p.bias, ccol, p.act);
+                }
+                if (pp < p.P) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int sidx = s0 + e;
+                        if (sidx >= p.S) break;
+                        if (p.ksplit > 1) {
+                            p.partial[((int64_t)blockIdx.y * p.S + sidx) * p.P + pp] = v[e];
+                            continue;
+                        }
+                        float *dst = p.C + (int64_t)sidx * p.c_s + (int64_t)pp * p.c_p;
+                        const int crow = p.rows_thin ? sidx : pp, ccol = p.rows_thin ? pp : sidx;
+                        const float a = epi_alpha(p.alpha, p.row_scale, crow);
+                        const float tt = p.beta == 0.0f ? __fmul_rn(a, v[e])
+                                                        : __fmaf_rn(a, v[e], __fmul_rn(p.beta, *dst));
+                        *dst = epi_tail(tt, p.bias, ccol, p.act);
+                    }
                 }
             }
         }
@@ -1799,7 +1798,7 @@ static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int
 }
 
 int run_tc_thin(const ThinCall &c, cudaStream_t s) {
-    if (c.S < 1 || c.S > 16 || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
+    if (c.S < 1 || c.S > tc::THIN_SMAX || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
         return SGEMM_ERR_UNSUPPORTED;
     // Small(s, k) = small[s * ss + k * sk]: K-contiguous (sk == 1) or stored k-major (ss == 1)
     const bool s_direct = c.small_sk == 1, s_trans = !s_direct && c.small_ss == 1;
@@ -1826,7 +1825,8 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return SGEMM_ERR_UNSUPPORTED;
     }
-    if (!make_map(&maps[1], s_hi, c.S, Kp, 16, tc::THIN_K) || !make_map(&maps[2], s_lo, c.S, Kp, 16, tc::THIN_K))
+    if (!make_map(&maps[1], s_hi, c.S, Kp, tc::THIN_SMAX, tc::THIN_K) ||
+        !make_map(&maps[2], s_lo, c.S, Kp, tc::THIN_SMAX, tc::THIN_K))
         return SGEMM_ERR_UNSUPPORTED;
     auto kern = tc::tc_thin_kernel;
     static uint64_t attr_done = 0;   // bit d: the shared-memory opt-in is set on device d

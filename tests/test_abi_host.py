@@ -276,9 +276,25 @@ def test_plan_thin_problems_take_the_gemv_path(lib):
     assert st == 0 and p["path"] == sg.PATH_GEMV
     st, p = sg.sgemm_plan("N", "T", 16, 16384, 8192, 8192, 8192, 16384, True, False, True)
     assert st == 0 and p["path"] == sg.PATH_GEMV
-    # 17 and up: the tile paths
-    st, p = sg.sgemm_plan("N", "N", 17, 4096, 4096, 4096, 4096, 4096)
-    assert st == 0 and p["path"] != sg.PATH_GEMV
+    # 17 to 32 with the large operand's rows along the long side (aligned):
+    # the thin path's tensor-core form; otherwise, and from 33, the tile paths
+    for (ta, tb, M, N, K) in [("N", "N", 17, 4096, 4096), ("N", "N", 32, 16384, 8192),
+                              ("T", "T", 16384, 24, 8192)]:
+        lda = K if ta == "N" else M
+        ldb = N if tb == "N" else K
+        st, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N)
+        assert st == 0 and d["path"] == sg.PATH_GEMV and d["tile_n"] == 128, (ta, tb, M, N, K)
+    for args in [("N", "N", 33, 4096, 4096, 4096, 4096, 4096),       # S = 33
+                 ("N", "T", 24, 4096, 4096, 4096, 4096, 4096),       # large operand K-contiguous
+                 ("N", "N", 24, 4094, 4096, 4096, 4094, 4094),       # its ld not a multiple of 4
+                 ("N", "N", 24, 4096, 16, 16, 4096, 4096)]:          # K < 32
+        st, p = sg.sgemm_plan(*args)
+        assert st == 0 and p["path"] != sg.PATH_GEMV, args
+    # forced: 17..32 only where the tensor-core form applies
+    st, p = sg.sgemm_plan("N", "N", 24, 4096, 16, 16, 4096, 4096, path=sg.PATH_GEMV)
+    assert st == 0 and p["path"] == sg.PATH_GEMV
+    st, _ = sg.sgemm_plan("N", "T", 24, 4096, 4096, 4096, 4096, 4096, path=sg.PATH_GEMV)
+    assert st == sg.SGEMM_ERR_UNSUPPORTED
     # forced on a wide problem: refused
     st, _ = sg.sgemm_plan("N", "N", 64, 64, 64, 64, 64, 64, path=sg.PATH_GEMV)
     assert st == sg.SGEMM_ERR_UNSUPPORTED

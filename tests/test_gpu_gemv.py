@@ -132,15 +132,20 @@ def test_staged_timeout_reports_and_recovers(oracle_mod, M):
     row-major) through shared memory with TMA: on the CUDA cores at S = 8, on
     the tensor cores at S = 16.  A 1 ns wait limit makes their bounded waits
     run out; the call raises SGEMM_ERR_TIMEOUT through the device error word
-    and the next call computes the right result."""
+    and the next call computes the right result.  The limit is a suspend hint
+    of mbarrier.try_wait, so the waits must meet real memory latency: the
+    large operand (256 MB) is larger than L2, and L2 is flushed before the
+    call (with the operand resident in L2 every copy could land in time)."""
     import torch
-    N, K = 4096, 4096
+    N, K = 8192, 8192
     A = gi.random_matrix(61, M, K)
     B = gi.random_matrix(62, K, N)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.zeros((M, N), device="cuda")
     s = torch.cuda.current_stream()
     assert sg.sgemm_device_error(s) == 0
+    flush = torch.empty(64 << 20, device="cuda")
+    flush.fill_(1.0)
     assert sg.sgemm_set_wait_limit(1) == 0
     try:
         st = sg.sgemm_ex("N", "N", M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
@@ -168,6 +173,11 @@ TC_THIN = [
     (16, 16384, 2049, "rows", 0.75, 1.0),
     (16, 300, 40000, "rows", 1.0, 0.0),      # K split across 50 CTAs
     (15, 4100, 9000, "cols", 2.0, -1.0),
+    # 16 < S <= 32: the same kernel, Small's hi and lo filling the 64-row operand
+    (17, 1000, 777, "rows", 1.0, 0.0),
+    (24, 4100, 3000, "cols", -0.5, 0.25),     # ragged P tile
+    (32, 2048, 20000, "rows", 1.0, 1.0),      # K split across CTAs
+    (29, 16384, 33, "rows", 1.5, 0.0),        # K one block and a bit
 ]
 
 
@@ -186,6 +196,9 @@ def test_thin_tensor_core_within_bound(oracle_mod, S, P, K, thin, alpha, beta):
     assert st == 0
     # the split of the small operand, the tensor-core kernel, and the sum when K is split
     assert sg.sgemm_launch_count() - c0 in (2, 3)
+    lda, ldb = A.shape[1], B.shape[1]
+    st, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N)
+    assert st == 0 and d["path"] == sg.PATH_GEMV and d["tile_n"] == 128 and d["accumulators"] == 8
     ref, bound = oracle_mod.gemm_f64(ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta,
                                      C if beta else None, N)
     rep = oracle_mod.compare(out, ref, bound, K, alpha)

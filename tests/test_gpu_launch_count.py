@@ -51,3 +51,5 @@ def test_quick_returns_and_thin_problems():
     assert n in (1, 2)
     # S = 16 on the tensor cores: the split of the small operand and the kernel
     assert _launches("N", "N", 16, 16384, 8192) == 2
+    # and S = 32 the same way
+    assert _launches("N", "N", 32, 16384, 8192) == 2

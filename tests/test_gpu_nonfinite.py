@@ -103,6 +103,7 @@ CASES = [
     ("T", "T", 2100, 130, 700, sg.PATH_FFMA, 1, "FFMA, B copied transposed first"),
     ("N", "T", 8, 700, 500, sg.PATH_GEMV, 0, "thin problem, dot form"),
     ("N", "N", 16, 700, 500, sg.PATH_GEMV, 0, "thin problem on the tensor cores"),
+    ("N", "N", 32, 700, 500, sg.PATH_AUTO, 0, "thin problem on the tensor cores, S = 32"),
     ("T", "N", 700, 8, 500, sg.PATH_GEMV, 0, "thin problem, axpy form"),
 ]
 
