@@ -1053,7 +1053,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- thin problems
-// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 32 outputs per column of a
+// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 64 outputs per column of a
 // large operand Big whose rows run along P in memory (Big(p, k) at
 // big[k ld + p]: decode's weights stored [K][N], or a transposed matrix
 // times a few vectors).  On the CUDA cores each element of Big feeds S FMAs,
@@ -1061,19 +1061,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 // owns 128 columns p of Big and one K range (K split over CTAs, multiples of
 // 32; the partial sums go to the thin path's sum kernel):
 //   * raw Big tiles of 32 k x 128 p arrive by TMA in a ring of their own
-//     (THIN_RAW stages of 16 KB), freed as soon as the split warps have read
+//     (ThinCfg::RAW stages of 16 KB), freed as soon as the split warps have read
 //     them, so that the HBM stream runs ahead of the split and the MMAs;
 //   * 8 warps split each tile (hi = rna_tf32(x), lo = rna_tf32(x - hi)) and
 //     turn it around into the K-major 128-byte-swizzled layout of an MMA
-//     operand (128 rows p x 32 k), in a ring of THIN_OPS operand stages;
+//     operand (128 rows p x 32 k), in a ring of ThinCfg::OPS operand stages;
 //   * Small, split by the pre-pass into [S][Kp] hi and lo, comes by TMA as a
-//     64-row operand per stage: rows 0..31 Small_hi, 32..63 Small_lo (rows past
-//     S read as zeros), so any S up to 32 costs the same MMAs;
+//     2 SMAX-row operand per stage (SMAX = 32 for S <= 32, else 64): rows
+//     0..SMAX-1 Small_hi, SMAX.. Small_lo (rows past S read as zeros), so any
+//     S up to SMAX costs the same MMAs;
 //   * per 8 k the MMA thread issues Big_hi x that operand into D1 (columns
-//     0..31 hi*hi, 32..63 hi*lo) and Big_lo x it into D2 (columns 0..31
-//     lo*hi; 32..63, lo*lo, unused), M = 128, N = 64, K = 8.  Each of the
-//     4 k-slices of a block has its own D1 and D2 (8 accumulators of 64
-//     columns), which halves the error against one pair;
+//     0..SMAX-1 hi*hi, SMAX.. hi*lo) and Big_lo x it into D2 (lo*hi, then
+//     lo*lo, unused), M = 128, N = 2 SMAX, K = 8.  The k-slices of a block
+//     take turns on NSETS accumulator sets (4 of D1 and D2 for SMAX = 32, 2
+//     for 64), which roughly halves the error against one set;
 //   * the epilogue adds each product's 4 accumulators, then hi*hi + (lo*hi
 //     + hi*lo) per output, and redoes NaN sums in fp32 over the CTA's K
 //     range.
@@ -1085,18 +1086,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 // room for only two raw stages: measured slower (16 x 16384 x 8192 NN 154 ->
 // 165 us).
 constexpr int THIN_P = 128;            // columns p per CTA (the MMA's M)
-constexpr int THIN_SMAX = 32;          // rows of Small per part in the operand (S <= 32)
 constexpr int THIN_K = 32;             // k per block
-constexpr int THIN_RAW = 6;            // raw tile stages (16 KB)
-constexpr int THIN_OPS = 3;            // operand stages (Big_hi, Big_lo, Small: 40 KB)
 constexpr int THIN_RAW_BYTES = THIN_K * THIN_P * 4;
 constexpr int THIN_A_BYTES = THIN_P * THIN_K * 4;
-constexpr int THIN_B_BYTES = 64 * THIN_K * 4;
-constexpr int THIN_OP_BYTES = 2 * THIN_A_BYTES + THIN_B_BYTES;
-constexpr int THIN_BARS = 2 * THIN_RAW + 3 * THIN_OPS + 1;
-constexpr int THIN_SMEM = THIN_RAW * THIN_RAW_BYTES + THIN_OPS * THIN_OP_BYTES + 512 + 1024;
-static_assert(THIN_BARS * 8 + 8 <= 512, "thin barriers");
-static_assert(THIN_SMEM <= SMEM_LIMIT, "thin shared memory");
+// SMAX: rows of Small per part in the operand, S <= SMAX (32 or 64).  The
+// MMA's N is 2 SMAX; each accumulator set holds D1 and D2 (2 x 2 SMAX
+// columns), and 512 columns of TMEM hold NSETS of them, taken by the k-slices
+// of a block in turn.  SMAX = 64 has a 16 KB Small operand per stage, so one
+// raw stage fewer fits.
+template <int SMAX>
+struct ThinCfg {
+    static constexpr int RAW = SMAX == 32 ? 6 : 5;       // raw tile stages (16 KB)
+    static constexpr int OPS = 3;                         // operand stages (Big_hi, Big_lo, Small)
+    static constexpr int B_BYTES = 2 * SMAX * THIN_K * 4;
+    static constexpr int OP_BYTES = 2 * THIN_A_BYTES + B_BYTES;
+    static constexpr int BARS = 2 * RAW + 3 * OPS + 1;
+    static constexpr int SMEM = RAW * THIN_RAW_BYTES + OPS * OP_BYTES + 512 + 1024;
+    static constexpr int SET_COLS = 4 * SMAX;
+    static constexpr int NSETS = 512 / SET_COLS;
+    static_assert(SMAX == 32 || SMAX == 64, "operand height");
+    static_assert(BARS * 8 + 8 <= 512, "thin barriers");
+    static_assert(SMEM <= SMEM_LIMIT, "thin shared memory");
+    static_assert(NSETS >= 1 && (THIN_K / 8) % NSETS == 0, "k-slices per accumulator set");
+};
 
 struct ThinParams {
     int S, P, K;
@@ -1137,21 +1149,23 @@ __device__ __noinline__ float thin_dot_fp32_warp(const ThinParams p, int s, int 
     return acc;
 }
 
+template <int SMAX>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_thin_kernel(const __grid_constant__ CUtensorMap tm_big,
                    const __grid_constant__ CUtensorMap tm_shi,
                    const __grid_constant__ CUtensorMap tm_slo, const ThinParams p) {
-    constexpr int R = THIN_RAW, O = THIN_OPS, NW = WORKERS / 32;
+    using TC = ThinCfg<SMAX>;
+    constexpr int R = TC::RAW, O = TC::OPS, NW = WORKERS / 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t smem0 = smem_u32(smem);
     auto raw_at = [&](int r) { return smem0 + (uint32_t)(r * THIN_RAW_BYTES); };
-    auto hi_at = [&](int o) { return smem0 + (uint32_t)(R * THIN_RAW_BYTES + o * THIN_OP_BYTES); };
+    auto hi_at = [&](int o) { return smem0 + (uint32_t)(R * THIN_RAW_BYTES + o * TC::OP_BYTES); };
     auto lo_at = [&](int o) { return hi_at(o) + (uint32_t)THIN_A_BYTES; };
     auto b_at = [&](int o) { return hi_at(o) + (uint32_t)(2 * THIN_A_BYTES); };
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R * THIN_RAW_BYTES + O * THIN_OP_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + THIN_BARS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R * THIN_RAW_BYTES + O * TC::OP_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + TC::BARS);
     const uint32_t bar0 = smem_u32(bars);
     auto raw_full = [&](int r) { return bar0 + 8u * r; };
     auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
@@ -1213,10 +1227,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (gb < nblk && mbar_test(op_empty(gb % O), ((uint32_t)(gb / O) & 1u) ^ 1u)) {
                     const int o = gb % O;
-                    // both parts' boxes are THIN_SMAX rows; rows past S are zero-filled
-                    mbar_expect_tx(op_bfull(o), 2u * THIN_SMAX * THIN_K * 4u);
+                    // both parts' boxes are SMAX rows; rows past S are zero-filled
+                    mbar_expect_tx(op_bfull(o), (uint32_t)TC::B_BYTES);
                     tma_load_2d(b_at(o), &tm_shi, op_bfull(o), k0 + gb * THIN_K, 0);
-                    tma_load_2d(b_at(o) + (uint32_t)(THIN_SMAX * THIN_K * 4), &tm_slo, op_bfull(o),
+                    tma_load_2d(b_at(o) + (uint32_t)(SMAX * THIN_K * 4), &tm_slo, op_bfull(o),
                                 k0 + gb * THIN_K, 0);
                     ++gb;
                     moved = true;
@@ -1240,8 +1254,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------ MMA issuer
-            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) |
-                                   ((uint32_t)(THIN_P >> 4) << 24);
+            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                                   ((uint32_t)((2 * SMAX) >> 3) << 17) | ((uint32_t)(THIN_P >> 4) << 24);
             for (int g = 0; g < nblk; ++g) {
                 const int o = g % O;
                 const uint32_t ph = (uint32_t)(g / O) & 1u;
@@ -1251,11 +1265,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kk = 0; kk < THIN_K / 8; ++kk) {
                     const uint32_t off = (uint32_t)(kk * 32);
                     const uint64_t bd = smem_desc<THIN_K * 4>(b_at(o) + off);
-                    // k-slice kk: D1 at columns 128 kk, D2 at 128 kk + 64
-                    const uint32_t acc = g == 0 ? 0u : 1u;
-                    const uint32_t d = tmem + (uint32_t)(128 * kk);
+                    // k-slice kk into set kk % NSETS: D1 at its column 0, D2 at 2 SMAX
+                    const uint32_t acc = (g == 0 && kk < TC::NSETS) ? 0u : 1u;
+                    const uint32_t d = tmem + (uint32_t)((kk % TC::NSETS) * TC::SET_COLS);
                     umma_tf32(d, smem_desc<THIN_K * 4>(hi_at(o) + off), bd, idesc, acc);
-                    umma_tf32(d + 64u, smem_desc<THIN_K * 4>(lo_at(o) + off), bd, idesc, acc);
+                    umma_tf32(d + (uint32_t)(2 * SMAX), smem_desc<THIN_K * 4>(lo_at(o) + off), bd, idesc,
+                              acc);
                 }
                 umma_commit(op_empty(o));
             }
@@ -1302,29 +1317,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) mbar_arrive(op_ready(o));
         }
         // ---- epilogue: warp w reads TMEM lanes 32 (w % 4).. (its 32 columns
-        // p) and s = 16 half .. + 15, 8 at a time; out = hi*hi + (lo*hi + hi*lo)
+        // p) and s = SMAX/2 half .. + SMAX/2 - 1, 8 at a time; out = hi*hi +
+        // (lo*hi + hi*lo)
         const bool ready = ok && mbar_wait(accf, 0u, lim);
         tc_fence_after();
         if (ready) {
             const int q = warp & 3, half = (warp - 2) >> 2;
             const int pp = p0 + q * 32 + lane;
 #pragma unroll 1
-            for (int s0 = 16 * half; s0 < 16 * half + 16 && s0 < p.S; s0 += 8) {   // warp-uniform
+            for (int s0 = (SMAX / 2) * half; s0 < (SMAX / 2) * (half + 1) && s0 < p.S; s0 += 8) {
+                // (warp-uniform bounds)
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)s0;
-                // each product summed over the 4 k-slice accumulators, in slice order
+                // each product summed over the accumulator sets, in set order
                 float hh[8], hl[8], lh[8];
 #pragma unroll
-                for (int kk = 0; kk < THIN_K / 8; ++kk) {
+                for (int j = 0; j < TC::NSETS; ++j) {
                     uint32_t a[8], b[8], c[8];
-                    const uint32_t tk = ta + (uint32_t)(128 * kk);
+                    const uint32_t tk = ta + (uint32_t)(j * TC::SET_COLS);
                     tmem_ld8(tk, a);
-                    tmem_ld8(tk + (uint32_t)THIN_SMAX, b);
-                    tmem_ld8(tk + 64u, c);
+                    tmem_ld8(tk + (uint32_t)SMAX, b);
+                    tmem_ld8(tk + (uint32_t)(2 * SMAX), c);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        hh[e] = kk == 0 ? __uint_as_float(a[e]) : __fadd_rn(hh[e], __uint_as_float(a[e]));
-                        hl[e] = kk == 0 ? __uint_as_float(b[e]) : __fadd_rn(hl[e], __uint_as_float(b[e]));
-                        lh[e] = kk == 0 ? __uint_as_float(c[e]) : __fadd_rn(lh[e], __uint_as_float(c[e]));
+                        hh[e] = j == 0 ? __uint_as_float(a[e]) : __fadd_rn(hh[e], __uint_as_float(a[e]));
+                        hl[e] = j == 0 ? __uint_as_float(b[e]) : __fadd_rn(hl[e], __uint_as_float(b[e]));
+                        lh[e] = j == 0 ? __uint_as_float(c[e]) : __fadd_rn(lh[e], __uint_as_float(c[e]));
                     }
                 }
                 float v[8];
@@ -1798,7 +1815,7 @@ static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int
 }
 
 int run_tc_thin(const ThinCall &c, cudaStream_t s) {
-    if (c.S < 1 || c.S > tc::THIN_SMAX || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
+    if (c.S < 1 || c.S > 64 || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
         return SGEMM_ERR_UNSUPPORTED;
     // Small(s, k) = small[s * ss + k * sk]: K-contiguous (sk == 1) or stored k-major (ss == 1)
     const bool s_direct = c.small_sk == 1, s_trans = !s_direct && c.small_ss == 1;
@@ -1825,19 +1842,22 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return SGEMM_ERR_UNSUPPORTED;
     }
-    if (!make_map(&maps[1], s_hi, c.S, Kp, tc::THIN_SMAX, tc::THIN_K) ||
-        !make_map(&maps[2], s_lo, c.S, Kp, tc::THIN_SMAX, tc::THIN_K))
+    const int smax = c.S <= 32 ? 32 : 64;   // the operand's rows per part
+    if (!make_map(&maps[1], s_hi, c.S, Kp, smax, tc::THIN_K) ||
+        !make_map(&maps[2], s_lo, c.S, Kp, smax, tc::THIN_K))
         return SGEMM_ERR_UNSUPPORTED;
-    auto kern = tc::tc_thin_kernel;
-    static uint64_t attr_done = 0;   // bit d: the shared-memory opt-in is set on device d
+    auto kern = smax == 32 ? tc::tc_thin_kernel<32> : tc::tc_thin_kernel<64>;
+    const int smem_bytes = smax == 32 ? tc::ThinCfg<32>::SMEM : tc::ThinCfg<64>::SMEM;
+    static uint64_t attr_done[2] = {0, 0};   // bit d: the shared-memory opt-in is set on device d
+    uint64_t &done = attr_done[smax == 32 ? 0 : 1];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
-    if (!bit || !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::THIN_SMEM) !=
+    if (!bit || !(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
             cudaSuccess)
             return last_status();
-        __atomic_fetch_or(&attr_done, bit, __ATOMIC_RELEASE);
+        __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
     }
     tc::SplitJob js = split_job(c.small, s_direct ? c.small_ss : c.small_sk, s_trans, c.S, c.K, Kp,
                                 s_hi, s_lo);
@@ -1860,7 +1880,7 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
     }
     const dim3 grid((unsigned)((c.P + tc::THIN_P - 1) / tc::THIN_P), (unsigned)c.ksplit);
     timing_mark(s, true);
-    launch_dependent(kern, grid, dim3(tc::THREADS), tc::THIN_SMEM, s, maps[0], maps[1], maps[2], p);
+    launch_dependent(kern, grid, dim3(tc::THREADS), smem_bytes, s, maps[0], maps[1], maps[2], p);
     timing_mark(s, false);
     return last_status();
 }
