@@ -1,4 +1,4 @@
-// Thin GEMMs: min(M, N) <= 16, or <= 64 on the tensor cores (SGEMM_PATH_GEMV).
+// Thin GEMMs: min(M, N) <= 16, or <= 128 on the tensor cores (SGEMM_PATH_GEMV).
 //
 // "Matmul II: register blocking, warp tiling, tensor cores", section 8
 // ("What cuBLAS does that we do not"): when M is 1 (decode) to a few dozen,

@@ -11,7 +11,7 @@ namespace sgemm_gb300 {
 
 constexpr int64_t kGemvMaxSmall = 16;
 // ... and up to kThinTcMaxS on the tensor cores (tc_thin_kernel)
-constexpr int64_t kThinTcMaxS = 64;
+constexpr int64_t kThinTcMaxS = 128;
 
 // CTAs of the main GEMV launch for this problem (what run_gemv launches).
 int gemv_ctas(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,

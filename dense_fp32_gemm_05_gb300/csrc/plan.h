@@ -99,15 +99,16 @@ inline int make_plan(char ta, char tb, int64_t M, int64_t N, int64_t K, int64_t 
     const bool big_kcontig = M <= N ? !is_notrans(tb) : is_notrans(ta);
     const bool big_al = M <= N ? (b_al && ldb % 4 == 0) : (a_al && lda % 4 == 0);
     const bool thin_on_tc = thin > 4 && big_kcontig && big_al && K >= 32;
-    // 16 < S <= 64 with the large operand's rows along the long side, aligned:
-    // the thin path's tensor-core form (its MMAs cost about the same up to S
-    // = 64), where the tile path would compute mostly padding and pre-split
+    // 16 < S <= 128 with the large operand's rows along the long side,
+    // aligned: the thin path's tensor-core form (its MMAs cost about the same
+    // up to S = 128), where the tile path would compute padding and pre-split
     // the whole large operand.  K >= 32 as for the tensor cores in general.
-    const bool tc_form = thin >= 12 && thin <= 64 && !big_kcontig && big_al;   // as run_gemv's
+    const bool tc_form = thin >= 12 && thin <= 128 && !big_kcontig && big_al;   // as run_gemv's
     const bool small = 2.0 * (double)M * (double)N * (double)K <= kSmallFlops && K <= kSmallMaxK &&
                        ((M + 15) / 16) * ((N + 15) / 16) <= kSmallMaxTiles;
-    // (problems small enough for the one-launch FFMA kernel stay there)
-    const bool thin_tc_wide = thin > 16 && tc_form && K >= 32 && !small;
+    // (problems small enough for the one-launch FFMA kernel stay there, and
+    // the other side must be long: the form's CTAs are 128 of its columns)
+    const bool thin_tc_wide = thin > 16 && tc_form && K >= 32 && !small && std::max(M, N) >= 8 * thin;
     if (path == SGEMM_PATH_GEMV ||
         (path == SGEMM_PATH_AUTO && ((thin <= 16 && !thin_on_tc) || thin_tc_wide))) {
         if (thin > 16 && !tc_form) return SGEMM_ERR_UNSUPPORTED;

@@ -1053,7 +1053,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- thin problems
-// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 64 outputs per column of a
+// out(s, p) = sum_k Small(s, k) Big(p, k) for S <= 128 outputs per column of a
 // large operand Big whose rows run along P in memory (Big(p, k) at
 // big[k ld + p]: decode's weights stored [K][N], or a transposed matrix
 // times a few vectors).  On the CUDA cores each element of Big feeds S FMAs,
@@ -1067,14 +1067,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 //     turn it around into the K-major 128-byte-swizzled layout of an MMA
 //     operand (128 rows p x 32 k), in a ring of ThinCfg::OPS operand stages;
 //   * Small, split by the pre-pass into [S][Kp] hi and lo, comes by TMA as a
-//     2 SMAX-row operand per stage (SMAX = 32 for S <= 32, else 64): rows
+//     2 SMAX-row operand per stage (SMAX = 32, 64 or 128, the least >= S): rows
 //     0..SMAX-1 Small_hi, SMAX.. Small_lo (rows past S read as zeros), so any
 //     S up to SMAX costs the same MMAs;
 //   * per 8 k the MMA thread issues Big_hi x that operand into D1 (columns
 //     0..SMAX-1 hi*hi, SMAX.. hi*lo) and Big_lo x it into D2 (lo*hi, then
 //     lo*lo, unused), M = 128, N = 2 SMAX, K = 8.  The k-slices of a block
 //     take turns on NSETS accumulator sets (4 of D1 and D2 for SMAX = 32, 2
-//     for 64), which roughly halves the error against one set;
+//     for 64, 1 for 128), which roughly halves the error against one set;
 //   * the epilogue adds each product's 4 accumulators, then hi*hi + (lo*hi
 //     + hi*lo) per output, and redoes NaN sums in fp32 over the CTA's K
 //     range.
@@ -1089,22 +1089,22 @@ constexpr int THIN_P = 128;            // columns p per CTA (the MMA's M)
 constexpr int THIN_K = 32;             // k per block
 constexpr int THIN_RAW_BYTES = THIN_K * THIN_P * 4;
 constexpr int THIN_A_BYTES = THIN_P * THIN_K * 4;
-// SMAX: rows of Small per part in the operand, S <= SMAX (32 or 64).  The
-// MMA's N is 2 SMAX; each accumulator set holds D1 and D2 (2 x 2 SMAX
+// SMAX: rows of Small per part in the operand, S <= SMAX (32, 64 or 128).
+// The MMA's N is 2 SMAX; each accumulator set holds D1 and D2 (2 x 2 SMAX
 // columns), and 512 columns of TMEM hold NSETS of them, taken by the k-slices
-// of a block in turn.  SMAX = 64 has a 16 KB Small operand per stage, so one
-// raw stage fewer fits.
+// of a block in turn.  A larger Small operand per stage (16 KB at SMAX = 64,
+// 32 KB at 128) leaves room for fewer stages.
 template <int SMAX>
 struct ThinCfg {
     static constexpr int RAW = SMAX == 32 ? 6 : 5;       // raw tile stages (16 KB)
-    static constexpr int OPS = 3;                         // operand stages (Big_hi, Big_lo, Small)
+    static constexpr int OPS = SMAX == 128 ? 2 : 3;       // operand stages (Big_hi, Big_lo, Small)
     static constexpr int B_BYTES = 2 * SMAX * THIN_K * 4;
     static constexpr int OP_BYTES = 2 * THIN_A_BYTES + B_BYTES;
     static constexpr int BARS = 2 * RAW + 3 * OPS + 1;
     static constexpr int SMEM = RAW * THIN_RAW_BYTES + OPS * OP_BYTES + 512 + 1024;
     static constexpr int SET_COLS = 4 * SMAX;
     static constexpr int NSETS = 512 / SET_COLS;
-    static_assert(SMAX == 32 || SMAX == 64, "operand height");
+    static_assert(SMAX == 32 || SMAX == 64 || SMAX == 128, "operand height");
     static_assert(BARS * 8 + 8 <= 512, "thin barriers");
     static_assert(SMEM <= SMEM_LIMIT, "thin shared memory");
     static_assert(NSETS >= 1 && (THIN_K / 8) % NSETS == 0, "k-slices per accumulator set");
@@ -1815,7 +1815,7 @@ static bool make_raw_map(CUtensorMap *m, const float *base, int rows, int K, int
 }
 
 int run_tc_thin(const ThinCall &c, cudaStream_t s) {
-    if (c.S < 1 || c.S > 64 || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
+    if (c.S < 1 || c.S > 128 || c.P < 1 || c.K < 1 || c.kchunk % tc::THIN_K != 0)
         return SGEMM_ERR_UNSUPPORTED;
     // Small(s, k) = small[s * ss + k * sk]: K-contiguous (sk == 1) or stored k-major (ss == 1)
     const bool s_direct = c.small_sk == 1, s_trans = !s_direct && c.small_ss == 1;
@@ -1842,14 +1842,16 @@ int run_tc_thin(const ThinCall &c, cudaStream_t s) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return SGEMM_ERR_UNSUPPORTED;
     }
-    const int smax = c.S <= 32 ? 32 : 64;   // the operand's rows per part
+    const int smax = c.S <= 32 ? 32 : c.S <= 64 ? 64 : 128;   // the operand's rows per part
     if (!make_map(&maps[1], s_hi, c.S, Kp, smax, tc::THIN_K) ||
         !make_map(&maps[2], s_lo, c.S, Kp, smax, tc::THIN_K))
         return SGEMM_ERR_UNSUPPORTED;
-    auto kern = smax == 32 ? tc::tc_thin_kernel<32> : tc::tc_thin_kernel<64>;
-    const int smem_bytes = smax == 32 ? tc::ThinCfg<32>::SMEM : tc::ThinCfg<64>::SMEM;
-    static uint64_t attr_done[2] = {0, 0};   // bit d: the shared-memory opt-in is set on device d
-    uint64_t &done = attr_done[smax == 32 ? 0 : 1];
+    auto kern = smax == 32 ? tc::tc_thin_kernel<32>
+                : smax == 64 ? tc::tc_thin_kernel<64> : tc::tc_thin_kernel<128>;
+    const int smem_bytes = smax == 32   ? tc::ThinCfg<32>::SMEM
+                           : smax == 64 ? tc::ThinCfg<64>::SMEM : tc::ThinCfg<128>::SMEM;
+    static uint64_t attr_done[3] = {0, 0, 0};   // bit d: the shared-memory opt-in is set on device d
+    uint64_t &done = attr_done[smax == 32 ? 0 : smax == 64 ? 1 : 2];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;

@@ -16,7 +16,7 @@ int run_tc(const Plan &pl, char ta, char tb, int64_t M, int64_t N, int64_t K, fl
            int64_t ldc, cudaStream_t s, int sms, const Epilogue &epi = Epilogue{});
 
 // A thin problem on the tensor cores (3xTF32): out(s, p) = sum_k Small(s, k)
-// Big(p, k) for S <= 64, Big stored with its rows along P (Big(p, k) =
+// Big(p, k) for S <= 128, Big stored with its rows along P (Big(p, k) =
 // big[k * big_ld + p], 16-byte aligned, big_ld % 4 == 0), Small(s, k) =
 // small[s * small_ss + k * small_sk] with small_sk == 1 or small_ss == 1.
 // K is cut into ksplit ranges of kchunk (a multiple of 32); with ksplit > 1

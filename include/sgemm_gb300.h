@@ -85,7 +85,7 @@ typedef enum {
 } sgemm_activation;
 
 /* Arithmetic path.  AUTO lets the per-shape selector choose among the
-   fp32-accurate paths: GEMV for min(M, N) <= 16, and up to 64 where its
+   fp32-accurate paths: GEMV for min(M, N) <= 16, and up to 128 where its
    tensor-core form applies (see below for the details); else FFMA's small-problem kernel for small problems (2MNK <=
    1.2e8, K <= 512, at most 1024 tiles of 16 x 16); else 3xTF32 for K >= 32
    and FFMA for K < 32.  TF32 is never chosen by AUTO. */
@@ -113,20 +113,21 @@ typedef enum {
     SGEMM_PATH_TF32 = 3,   /* the same tensor-core kernel with only hi*hi:
                               single-pass TF32, LOWER accuracy than fp32
                               ("Optimising fp32 GEMM on A100", "Kernel 1").  */
-    SGEMM_PATH_GEMV = 4    /* thin problems, min(M, N) <= 16 (64 on the
+    SGEMM_PATH_GEMV = 4    /* thin problems, min(M, N) <= 16 (128 on the
                               tensor cores): the large operand streamed once,
                               no tiles ("Matmul II", section 8: dedicated GEMV
                               kernels for decode's M = 1 to a few dozen).
                               CUDA-core fp32 FMAs, except with 12 <= min(M, N)
-                              <= 64 and the large operand's rows along the
+                              <= 128 and the large operand's rows along the
                               long dimension (16-byte aligned, leading
                               dimension a multiple of 4): those run 3xTF32 on
                               the tensor cores.  AUTO takes this path whenever
                               min(M, N) <= 16, except with K >= 32, min(M, N)
                               > 4 and the large operand's rows along K
                               (weights stored [N][K]): those go to the 3xTF32
-                              tiles; and for 16 < min(M, N) <= 64 when the
-                              tensor-core form applies and K >= 32.  Forced on
+                              tiles; and for 16 < min(M, N) <= 128 when the
+                              tensor-core form applies, K >= 32 and max(M, N)
+                              >= 8 min(M, N).  Forced on
                               any other problem it returns
                               SGEMM_ERR_UNSUPPORTED.                          */
 } sgemm_path;

@@ -276,16 +276,17 @@ def test_plan_thin_problems_take_the_gemv_path(lib):
     assert st == 0 and p["path"] == sg.PATH_GEMV
     st, p = sg.sgemm_plan("N", "T", 16, 16384, 8192, 8192, 8192, 16384, True, False, True)
     assert st == 0 and p["path"] == sg.PATH_GEMV
-    # 17 to 64 with the large operand's rows along the long side (aligned):
-    # the thin path's tensor-core form; otherwise, and from 65, the tile paths
+    # 17 to 128 with the large operand's rows along the long side (aligned):
+    # the thin path's tensor-core form; otherwise, and from 129, the tile paths
     for (ta, tb, M, N, K) in [("N", "N", 17, 4096, 4096), ("N", "N", 32, 16384, 8192),
                               ("T", "T", 16384, 24, 8192), ("N", "N", 33, 4096, 4096),
-                              ("N", "N", 64, 16384, 8192), ("T", "T", 16384, 48, 8192)]:
+                              ("N", "N", 64, 16384, 8192), ("T", "T", 16384, 48, 8192),
+                              ("N", "N", 65, 16384, 8192), ("N", "N", 128, 16384, 8192)]:
         lda = K if ta == "N" else M
         ldb = N if tb == "N" else K
         st, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, N)
         assert st == 0 and d["path"] == sg.PATH_GEMV and d["tile_n"] == 128, (ta, tb, M, N, K)
-    for args in [("N", "N", 65, 4096, 4096, 4096, 4096, 4096),       # S = 65
+    for args in [("N", "N", 129, 4096, 4096, 4096, 4096, 4096),      # S = 129
                  ("N", "T", 24, 4096, 4096, 4096, 4096, 4096),       # large operand K-contiguous
                  ("N", "N", 24, 4094, 4096, 4096, 4094, 4094),       # its ld not a multiple of 4
                  ("N", "N", 24, 4096, 16, 16, 4096, 4096)]:          # K < 32
@@ -297,7 +298,7 @@ def test_plan_thin_problems_take_the_gemv_path(lib):
     st, _ = sg.sgemm_plan("N", "T", 24, 4096, 4096, 4096, 4096, 4096, path=sg.PATH_GEMV)
     assert st == sg.SGEMM_ERR_UNSUPPORTED
     # forced on a wide problem: refused
-    st, _ = sg.sgemm_plan("N", "N", 65, 65, 65, 65, 65, 65, path=sg.PATH_GEMV)
+    st, _ = sg.sgemm_plan("N", "N", 129, 129, 129, 129, 129, 129, path=sg.PATH_GEMV)
     assert st == sg.SGEMM_ERR_UNSUPPORTED
     st, _ = sg.sgemm_plan("N", "N", 64, 64, 64, 64, 64, 64, path=5)
     assert st == sg.SGEMM_ERR_ARG

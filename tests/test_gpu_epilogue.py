@@ -32,7 +32,7 @@ CASES = [
     ("gemv_dot", sg.PATH_GEMV, 0, "N", "T", 3, 700, 500),
     ("gemv_axpy", sg.PATH_GEMV, 0, "T", "N", 900, 5, 400),
     ("gemv_tensor_core", sg.PATH_GEMV, 0, "N", "N", 16, 1000, 500),
-    ("gemv_tensor_core_s24", sg.PATH_AUTO, 0, "T", "N", 24, 1000, 500),
+    ("gemv_tensor_core_s24", sg.PATH_AUTO, 0, "T", "N", 24, 4100, 600),
 ]
 
 EPILOGUES = [

@@ -120,9 +120,9 @@ def test_gemv_special_cases(oracle_mod):
 
 def test_gemv_forced_on_a_wide_problem_is_refused():
     import torch
-    x = torch.zeros(65 * 65, device="cuda")
-    st = sg.sgemm_ex("N", "N", 65, 65, 65, 1.0, x.data_ptr(), 65, x.data_ptr(), 65, 0.0,
-                     x.data_ptr(), 65, torch.cuda.current_stream(), sg.PATH_GEMV, 0)
+    x = torch.zeros(129 * 129, device="cuda")
+    st = sg.sgemm_ex("N", "N", 129, 129, 129, 1.0, x.data_ptr(), 129, x.data_ptr(), 129, 0.0,
+                     x.data_ptr(), 129, torch.cuda.current_stream(), sg.PATH_GEMV, 0)
     assert st == sg.SGEMM_ERR_UNSUPPORTED
 
 
@@ -173,8 +173,8 @@ TC_THIN = [
     (16, 16384, 2049, "rows", 0.75, 1.0),
     (16, 300, 40000, "rows", 1.0, 0.0),      # K split across 50 CTAs
     (15, 4100, 9000, "cols", 2.0, -1.0),
-    # 16 < S <= 64: the same kernel, Small's hi and lo filling the 64-row
-    # operand (S <= 32) or a 128-row one
+    # 16 < S <= 128: the same kernel, Small's hi and lo filling a 64-, 128- or
+    # 256-row operand
     (17, 1000, 777, "rows", 1.0, 0.0),
     (24, 4100, 3000, "cols", -0.5, 0.25),     # ragged P tile
     (32, 2048, 20000, "rows", 1.0, 1.0),      # K split across CTAs
@@ -182,6 +182,9 @@ TC_THIN = [
     (33, 1000, 777, "rows", 1.0, 0.0),
     (48, 4100, 3000, "cols", -0.5, 0.25),     # ragged P tile
     (64, 2048, 20000, "rows", 1.0, 1.0),      # K split across CTAs
+    (65, 1000, 777, "rows", 1.0, 0.0),
+    (100, 4100, 3000, "cols", -0.5, 0.25),    # ragged P tile
+    (128, 2048, 20000, "rows", 1.0, 1.0),     # K split across CTAs
 ]
 
 

@@ -51,6 +51,7 @@ def test_quick_returns_and_thin_problems():
     assert n in (1, 2)
     # S = 16 on the tensor cores: the split of the small operand and the kernel
     assert _launches("N", "N", 16, 16384, 8192) == 2
-    # and S = 32 and 64 the same way
+    # and S = 32, 64 and 128 the same way
     assert _launches("N", "N", 32, 16384, 8192) == 2
     assert _launches("N", "N", 64, 16384, 8192) == 2
+    assert _launches("N", "N", 128, 16384, 8192) == 2

@@ -103,8 +103,9 @@ CASES = [
     ("T", "T", 2100, 130, 700, sg.PATH_FFMA, 1, "FFMA, B copied transposed first"),
     ("N", "T", 8, 700, 500, sg.PATH_GEMV, 0, "thin problem, dot form"),
     ("N", "N", 16, 700, 500, sg.PATH_GEMV, 0, "thin problem on the tensor cores"),
-    ("N", "N", 32, 700, 500, sg.PATH_AUTO, 0, "thin problem on the tensor cores, S = 32"),
+    ("N", "N", 32, 4100, 600, sg.PATH_AUTO, 0, "thin problem on the tensor cores, S = 32"),
     ("T", "N", 64, 4100, 600, sg.PATH_AUTO, 0, "thin problem on the tensor cores, S = 64"),
+    ("N", "N", 128, 4100, 600, sg.PATH_AUTO, 0, "thin problem on the tensor cores, S = 128"),
     ("T", "N", 700, 8, 500, sg.PATH_GEMV, 0, "thin problem, axpy form"),
 ]
 
