@@ -70,9 +70,11 @@ WORKLOADS = {w.name: w for w in [
        std=8192 ** -0.25, seed=4),
     _w("skinny_nt", 16384, 64, 8192, "N", "T", seed=5),
     # thin problems: decode's M = 1 to a few dozen ("Matmul II", section 8),
-    # and their mirror, a few columns of C; a 512 MB operand streamed once
+    # up to a batch of 128, and their mirror, a few columns of C; a 512 MB
+    # operand streamed once
     _w("decode_m1_nt", 1, 16384, 8192, "N", "T", seed=6),
     _w("decode_m16_nn", 16, 16384, 8192, "N", "N", seed=7),
+    _w("decode_m128_nn", 128, 16384, 8192, "N", "N", seed=10),
     _w("matvec_n1_nn", 16384, 1, 8192, "N", "N", beta=1.0, seed=8),
     _w("matvec_n8_tn", 16384, 8, 8192, "T", "N", seed=9),
 ]}
