@@ -372,6 +372,14 @@ extern "C" int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_
     if (out_tile_m) *out_tile_m = pl.tile_m;
     if (out_tile_n) *out_tile_n = pl.tile_n;
     if (out_vector) *out_vector = pl.vector;
+    if (pl.path == SGEMM_PATH_GEMV &&
+        thin_on_tensor_cores(transA, transB, M, N, lda, ldb, a_aligned != 0, b_aligned != 0)) {
+        // the thin path's tensor-core form: 128 columns of the large operand
+        // per CTA, and split = the CTAs along K
+        if (out_tile_n) *out_tile_n = 128;
+        if (out_split)
+            *out_split = thin_tc_geometry(std::max(M, N), std::max<int64_t>(K, 1), num_sms).ksplit;
+    }
     if (out_ctas) {
         if (pl.path == SGEMM_PATH_FFMA) {
             *out_ctas = pl.dp_tiles + pl.ctas;
@@ -411,12 +419,10 @@ extern "C" int sgemm_plan_detail(char transA, char transB, int64_t M, int64_t N,
     info.dp_tiles = pl.path == SGEMM_PATH_GEMV ? 0 : pl.dp_tiles;
     if (pl.path == SGEMM_PATH_GEMV &&
         thin_on_tensor_cores(transA, transB, M, N, lda, ldb, a_aligned != 0, b_aligned != 0)) {
-        // the tensor-core form: 128 columns of the large operand per CTA,
-        // 32-wide k-blocks, 8 accumulators; split = the CTAs along K
-        info.tile_n = 128;
+        // the tensor-core form (tile_n and split from sgemm_plan above):
+        // 32-wide k-blocks, 8 accumulators
         info.k_block = 32;
         info.accumulators = 8;
-        info.split = thin_tc_geometry(std::max(M, N), std::max<int64_t>(K, 1), num_sms).ksplit;
     }
     if (pl.path == SGEMM_PATH_3XTF32 || pl.path == SGEMM_PATH_TF32) {
         const TcVariant v = tc_variant(pl);

@@ -225,9 +225,10 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * a_aligned/b_aligned/c_aligned say whether the base pointer is 16-byte
  * aligned.  On success writes the chosen path (sgemm_path), the CTAs per
  * output tile rounded up (FFMA or tensor-core stream-K, or the column slices
- * of the tensor cores' last-wave tiles; 1 = every tile whole), the tile rows
- * and
- * columns, whether the FFMA path uses 16-byte loads (1) or the 4-byte edge
+ * of the tensor cores' last-wave tiles, or the thin path's CTAs along K on the
+ * tensor cores; 1 = every tile whole), the tile rows and columns (the thin
+ * path: min(M, N), and 0, or 128 columns of the large operand per CTA on the
+ * tensor cores), whether the FFMA path uses 16-byte loads (1) or the 4-byte edge
  * path (0), and the number of CTAs of the main kernel.  Any output pointer
  * may be NULL.  Returns SGEMM_OK or a negative argument index as sgemm.
  */

@@ -459,3 +459,55 @@ def test_stream_k_over_every_tile_only_when_it_pays():
     # a forced split still shares the k-blocks
     st, d = sg.sgemm_plan_detail("N", "N", 2048, 2048, 8192, 8192, 2048, 2048, split=2)
     assert st == 0 and d["sk_ctas"] > 0
+
+
+def test_plan_invariants_over_random_shapes():
+    """The selector's decisions over 3000 seeded random problems (sizes
+    around every threshold, all layouts, padded leading dimensions,
+    misaligned bases, forced paths and splits): sgemm_plan and
+    sgemm_plan_detail agree field for field, forced paths are honoured, and
+    each plan is one the launchers accept (pairs never split an operand in
+    the kernel, an operand is split in the kernel only when TMA may read it
+    raw, the thin path stays within its range, the FFMA pre-pass only copies
+    K-contiguous operands)."""
+    import random
+    rng = random.Random(1234)
+    dims = [1, 2, 3, 5, 8, 12, 16, 17, 24, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 200, 255,
+            256, 257, 500, 511, 512, 513, 1000, 1023, 1024, 1500, 2047, 2048, 2049, 3000, 4095,
+            4096, 6000, 8192, 16384, 65536]
+    for _ in range(3000):
+        M, N, K = rng.choice(dims), rng.choice(dims), rng.choice(dims)
+        ta, tb = rng.choice("NT"), rng.choice("NT")
+        lda = (K if ta == "N" else M) + rng.choice([0, 0, 1, 3, 4])
+        ldb = (N if tb == "N" else K) + rng.choice([0, 0, 1, 4])
+        ldc = N + rng.choice([0, 1])
+        al = [rng.random() < 0.85 for _ in range(3)]
+        path = rng.choice([0, 0, 0, 1, 2, 3, 4])
+        split = rng.choice([0, 0, 1, 2, 5])
+        key = (ta, tb, M, N, K, lda, ldb, ldc, al, path, split)
+        st, d = sg.sgemm_plan_detail(ta, tb, M, N, K, lda, ldb, ldc, *al, path, split, 152)
+        st2, p = sg.sgemm_plan(ta, tb, M, N, K, lda, ldb, ldc, *al, path, split, 152)
+        assert st == st2, key
+        if st != 0:
+            assert path == sg.PATH_GEMV and st == sg.SGEMM_ERR_UNSUPPORTED, key
+            continue
+        for f in ("path", "tile_m", "tile_n", "ctas", "split", "vector"):
+            assert d[f] == p[f], (f, key, d, p)
+        assert d["path"] in (1, 2, 3, 4) and d["ctas"] >= 1 and d["split"] >= 1, (key, d)
+        if path:
+            assert d["path"] == path, (key, d)
+        if d["path"] == sg.PATH_GEMV:
+            assert min(M, N) <= 128 and d["tile_m"] == min(M, N), (key, d)
+        if d["path"] in (sg.PATH_3XTF32, sg.PATH_TF32):
+            assert d["tile_n"] in (64, 128, 256) and d["k_block"] in (16, 32), (key, d)
+            assert d["pair"] == (d["tile_m"] == 256), (key, d)
+            assert not (d["pair"] and (d["fuse_a"] or d["fuse_b"])), (key, d)
+            assert d["sk_ctas"] <= 8 * 152 and d["pre_transpose"] == 0, (key, d)
+            if d["fuse_a"]:
+                assert ta == "N" and al[0] and lda % 4 == 0, (key, d)
+            if d["fuse_b"]:
+                assert tb == "T" and al[1] and ldb % 4 == 0, (key, d)
+        if d["path"] == sg.PATH_FFMA:
+            assert not (d["tile_n"] == 16 and d["pre_transpose"]), (key, d)
+            assert not (d["pre_transpose"] & 1 and ta != "N"), (key, d)
+            assert not (d["pre_transpose"] & 2 and tb != "T"), (key, d)
