@@ -498,6 +498,14 @@ def test_plan_invariants_over_random_shapes():
             assert d["path"] == path, (key, d)
         if d["path"] == sg.PATH_GEMV:
             assert min(M, N) <= 128 and d["tile_m"] == min(M, N), (key, d)
+            if d["tile_n"] == 128:
+                # the tensor-core form: 128 columns of the long side per CTA,
+                # split = CTAs along K (at least 32 k each), 8 accumulators
+                P = max(M, N)
+                assert d["ctas"] == (P + 127) // 128 * d["split"], (key, d)
+                assert d["split"] <= max(1, K // 32) and d["accumulators"] == 8, (key, d)
+            else:
+                assert min(M, N) <= 16 and d["tile_n"] == 0, (key, d)
         if d["path"] in (sg.PATH_3XTF32, sg.PATH_TF32):
             assert d["tile_n"] in (64, 128, 256) and d["k_block"] in (16, 32), (key, d)
             assert d["pair"] == (d["tile_m"] == 256), (key, d)
